@@ -1,0 +1,210 @@
+/*
+ * spectree.h -- tree verification for Medusa/EAGLE-style speculative decoding on one GB300
+ * (sm_103a).  C ABI of libspectree.so.
+ *
+ * What the three calls compute (sources are cited by page title and section):
+ *
+ *   spec_tree_attention  One target-model attention layer over a draft tree.  Every tree node
+ *       attends to the request's KV-cache prefix plus only its own ancestors and itself
+ *       (tech-tldr "多トークン予測（Medusa・EAGLE）", section "ツリー検証"; qiita "EAGLE-3と
+ *       Medusaで実装するSpeculative Decoding実践ガイド", sections "並列検証" and "Tree Attention").
+ *   spec_verify_accept   The LM head z = W h at every node (tech-tldr, section "Medusa": linear
+ *       layer + softmax), then per-node acceptance by one of three rules -- greedy argmax match;
+ *       typical acceptance (jisaku glossary "Medusa", section "Medusa-1: 典型的採択");
+ *       rejection sampling with min(1, T[x]/D[x]) and resampling from norm(relu(T - D)) (qiita,
+ *       section "棄却サンプリング") -- and the longest accepted root path plus a bonus token.
+ *   spec_compact_kv      Keeps the accepted path's K/V entries right after the prefix (qiita,
+ *       section "棄却サンプリング": everything after a rejection is discarded).
+ *
+ * Conventions shared by every call
+ *   - Node 0 of a tree is its root (the last accepted token); parent[0] = -1 and
+ *     0 <= parent[i] < i for 0 < i < n_nodes[b], so nodes are in topological order and siblings
+ *     are ordered by index.  Entries at i >= n_nodes[b] are padding and are ignored.
+ *   - KV cache layout [B][Hkv][L_cap][head_dim]: request b's prefix occupies slots
+ *     [0, prefix_len[b]); tree node i occupies slot prefix_len[b] + i.
+ *   - All array arguments are caller-owned, contiguous, row-major DEVICE memory with 16-byte
+ *     aligned base addresses.  The library never allocates: scratch space is the caller's
+ *     `workspace`, sized by the matching *_workspace() query.  It keeps no global state and
+ *     every call may be issued from any host thread.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Errors found on the host (NULL pointer, unsupported size or dtype, short workspace) are
+ *     returned before anything is launched.  Errors that depend on device data (a bad parent
+ *     array, prefix_len + n_nodes > L_cap, a token outside the vocabulary, an accepted path
+ *     longer than path_cap) are written to *dev_status with first-error-wins semantics
+ *     (atomicCAS from SPEC_OK); the offending request's outputs are zeroed (attention rows 0;
+ *     accept_len 0, path {0, -1, ...}, bonus -1).  The caller zeroes *dev_status before the
+ *     calls it wants checked and reads it after synchronising.  No kernel traps; every wait
+ *     inside a kernel is bounded and reports SPEC_ERR_TIMEOUT instead of hanging.
+ */
+#ifndef SPECTREE_H_
+#define SPECTREE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t spec_status;
+
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARGUMENT 1   /* host: NULL pointer, non-positive or inconsistent size */
+#define SPEC_ERR_UNSUPPORTED 2        /* host: dtype / head_dim / size outside what is built */
+#define SPEC_ERR_WORKSPACE_TOO_SMALL 3 /* host: workspace_bytes below the *_workspace() query */
+#define SPEC_ERR_BAD_TREE 4           /* device: parent array is not a valid rooted tree */
+#define SPEC_ERR_CUDA 5               /* host: a CUDA runtime call failed (launch, attribute) */
+#define SPEC_ERR_BAD_TOKEN 6          /* device: token or draft map entry outside the vocabulary */
+#define SPEC_ERR_CAPACITY 7           /* device: prefix_len + n_nodes > L_cap, or a path longer
+                                         than path_cap */
+#define SPEC_ERR_TIMEOUT 8            /* device: a bounded wait in a kernel ran out */
+
+#define SPEC_DTYPE_F32 0   /* float32 tensors (exact path; SIMT kernels) */
+#define SPEC_DTYPE_BF16 1  /* bfloat16 tensors, float32 accumulation (tensor-core kernels) */
+
+#define SPEC_RULE_GREEDY 0
+#define SPEC_RULE_TYPICAL 1
+#define SPEC_RULE_REJECTION 2
+
+#define SPEC_MAX_NODES 255 /* n_max limit (the largest Medusa tree named on the pages) */
+
+/* ---------------------------------------------------------------------------------------
+ * Tree attention.
+ *
+ * For request b, query head h, node i < n_nodes[b], with G = Hq / Hkv and KV head g = h / G:
+ *   visible(i) = prefix slots [0, L_b)  +  tree slots {L_b + a : a ancestor of i, or a = i}
+ *   out[b][i][h] = sum_j softmax_j(scale * q[b][i][h] . k[b][g][j]) v[b][g][j]   (j visible)
+ *   lse[b][i][h] = ln sum_j exp(scale * q[b][i][h] . k[b][g][j])
+ * Padded nodes (i >= n_nodes[b]) get out = 0 and lse = 0.
+ * ------------------------------------------------------------------------------------- */
+typedef struct spec_attn_args {
+  int32_t dtype;          /* SPEC_DTYPE_F32 or SPEC_DTYPE_BF16 (q, caches and out) */
+  int32_t batch;          /* B >= 1 */
+  int32_t n_max;          /* N, padded nodes per request incl. root, 1..SPEC_MAX_NODES */
+  int32_t num_q_heads;    /* Hq, a multiple of num_kv_heads */
+  int32_t num_kv_heads;   /* Hkv >= 1 */
+  int32_t head_dim;       /* d: 64 or 128 */
+  int64_t kv_capacity;    /* L_cap, slots per (request, KV head) in the caches */
+  float scale;            /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
+  int32_t reserved0;      /* must be 0 */
+  const void* q;          /* [B][N][Hq][d] */
+  const void* k_cache;    /* [B][Hkv][L_cap][d] */
+  const void* v_cache;    /* [B][Hkv][L_cap][d] */
+  const int32_t* prefix_len; /* [B], L_b >= 0 */
+  const int32_t* n_nodes;    /* [B], 1 <= n_b <= N */
+  const int32_t* parent;     /* [B][N] */
+  void* out;              /* [B][N][Hq][d], same dtype as q */
+  float* lse;             /* [B][N][Hq] natural-log LSE, or NULL */
+  void* timing_begin;     /* optional cudaEvent_t recorded on `stream` right before the split-KV
+                             attention kernel (bf16) or the fp32 attention kernel; NULL = none */
+  void* timing_end;       /* optional cudaEvent_t recorded right after that kernel */
+} spec_attn_args;
+
+/* Bytes of workspace spec_tree_attention needs for these shapes (0 on invalid args). */
+size_t spec_tree_attention_workspace(const spec_attn_args* args);
+
+spec_status spec_tree_attention(const spec_attn_args* args, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * LM head, acceptance, longest accepted path, bonus token.
+ *
+ * z[b][i] = lm_head_weight . hidden_states[b][i] (no bias), for every real node.  Node c != 0
+ * carries tokens[b][c] and is judged with the distribution at its parent p = parent[b][c]:
+ *   GREEDY     accept iff tokens[c] == argmax_v z[p][v] (lowest index on ties).
+ *   TYPICAL    p_p = softmax(z[p] / temperature), H = -sum p_p ln p_p (nats);
+ *              accept iff p_p(x) >= min(eps, delta * exp(-H)).
+ *   REJECTION  walk from the root: R = softmax(z[e] / temperature); for each child c of e in
+ *              index order, u = U(seed, b, c, 0): accept iff u < min(1, R[x] / D_e[x]) (ratio 1
+ *              when D_e[x] = 0 < R[x], 0 when both are 0); on acceptance e = c and R restarts
+ *              from e's distribution; on rejection R = relu(R - D_e) / sum (kept if the sum is 0).
+ *              D_e = draft_probs[b][e], scattered into the target vocabulary by
+ *              draft_to_target (zero outside the map).
+ * Path: greedy/typical take the deepest node whose whole root chain is accepted (lowest index
+ * on ties); rejection takes the walk's last node e.  accept_len = depth(e); path = root..e.
+ * Bonus token: argmax z[e] (greedy/typical); for rejection the inverse-CDF sample of R at
+ * u' = U(seed, b, e, 1) -- the smallest j with sum_{v<=j} R[v] > u' sum R.
+ * U(seed, b, node, purpose) = (2 * (x0 >> 9) + 1) * 2^-24 where x0 is the first output word of
+ * Philox4x32-10 (Salmon et al., SC'11) with key (seed & 0xffffffff, seed >> 32) and counter
+ * (b, node, purpose, 0).
+ * Margin cases -- decisions within 1e-4 of their threshold (greedy: top-2 logit gap; typical:
+ * |ln p(x) - ln thr|; rejection: |u - min(1, R[x]/D[x])|) among the decisions the walk
+ * evaluates -- are counted in margin_count; bonus_margin flags a bonus decision within 1e-4
+ * (greedy/typical: top-2 gap of z[e]; rejection: u' sum R within 1e-4 sum R of a cumulative
+ * boundary).
+ * ------------------------------------------------------------------------------------- */
+typedef struct spec_verify_args {
+  int32_t dtype;          /* dtype of hidden_states and lm_head_weight */
+  int32_t batch;          /* B >= 1 */
+  int32_t n_max;          /* N, 1..SPEC_MAX_NODES */
+  int32_t hidden;         /* Hd: a multiple of 64 for BF16, of 4 for F32 */
+  int32_t vocab;          /* V >= 2 */
+  int32_t rule;           /* SPEC_RULE_* */
+  float temperature;      /* tau > 0 for TYPICAL / REJECTION; ignored by GREEDY */
+  float eps;              /* TYPICAL: epsilon */
+  float delta;            /* TYPICAL: delta */
+  int32_t draft_vocab;    /* REJECTION: Vd (= vocab when draft_to_target is NULL) */
+  int32_t path_cap;       /* entries per request in `path`: >= deepest accepted depth + 1 */
+  int32_t reserved0;      /* must be 0 */
+  uint64_t seed;          /* key of the acceptance uniforms */
+  const void* hidden_states;      /* [B][N][Hd] */
+  const void* lm_head_weight;     /* [V][Hd] (each vocab row contiguous in Hd) */
+  const int32_t* tokens;          /* [B][N] target-vocab ids (entry 0 unused) */
+  const int32_t* parent;          /* [B][N] */
+  const int32_t* n_nodes;         /* [B] */
+  const float* draft_probs;       /* REJECTION: [B][N][Vd]; row e = distribution of e's children */
+  const int32_t* draft_to_target; /* REJECTION: [Vd] injective map into [0, V), or NULL */
+  int32_t* accept_len;            /* out [B] */
+  int32_t* path;                  /* out [B][path_cap], -1 padded */
+  int32_t* bonus_token;           /* out [B] */
+  int32_t* margin_count;          /* out [B] or NULL */
+  int32_t* bonus_margin;          /* out [B] (0/1) or NULL */
+  float* row_max;                 /* optional out [B][N]: max_v z/tau (z for GREEDY) */
+  float* row_lse;                 /* optional out [B][N]: ln sum exp(z/tau) */
+  float* row_entropy;             /* optional out [B][N]: H in nats */
+  int32_t* row_argmax;            /* optional out [B][N]: argmax_v z */
+  void* timing_begin;             /* optional cudaEvent_t recorded on `stream` right before the
+                                     LM-head kernel; NULL = none */
+  void* timing_end;               /* optional cudaEvent_t recorded right after it */
+} spec_verify_args;
+
+size_t spec_verify_accept_workspace(const spec_verify_args* args);
+
+spec_status spec_verify_accept(const spec_verify_args* args, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * KV compaction (in place).  For j = 0..accept_len[b]:
+ *   K/V[b][g][L_b + j] <- K/V[b][g][L_b + path[b][j]] for every KV head g (reads see the
+ *   cache as it was before the call), src_slot[b][j] = L_b + path[b][j] (-1 beyond),
+ *   new_len[b] = L_b + 1 + accept_len[b].
+ * A path that is not a root path of increasing node indices, or that leaves the cache, sets
+ * SPEC_ERR_BAD_TREE / SPEC_ERR_CAPACITY and leaves that request's cache untouched.
+ * ------------------------------------------------------------------------------------- */
+typedef struct spec_compact_args {
+  int32_t dtype;          /* element type of the caches */
+  int32_t batch;
+  int32_t num_kv_heads;
+  int32_t head_dim;       /* 64 or 128 */
+  int64_t kv_capacity;    /* L_cap */
+  int32_t path_cap;
+  int32_t reserved0;      /* must be 0 */
+  void* k_cache;          /* [B][Hkv][L_cap][d], updated in place */
+  void* v_cache;
+  const int32_t* prefix_len;  /* [B] */
+  const int32_t* path;        /* [B][path_cap] */
+  const int32_t* accept_len;  /* [B] */
+  int32_t* src_slot;          /* out [B][path_cap] or NULL */
+  int32_t* new_len;           /* out [B] or NULL */
+} spec_compact_args;
+
+spec_status spec_compact_kv(const spec_compact_args* args, int32_t* dev_status, void* stream);
+
+/* Static English description of a status code (never NULL). */
+const char* spec_status_string(spec_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECTREE_H_ */

@@ -1,0 +1,106 @@
+"""GPU parity of the LM head, acceptance and longest-path selection (through the C ABI)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from gen import make_case, make_config_case, trees as T
+import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(case, requests=None, limit=None):
+    rows = [(b, i) for b in (range(case.B) if requests is None else requests) for i in range(case.n_nodes[b])]
+    return rows if limit is None else rows[:limit]
+
+
+def test_tiny_fp32_greedy():
+    d = H.dev()
+    case = H.config_case(1, 0)
+    got = H.gpu_verify(case, H.to_device(case, d))
+    assert got["status"] == 0
+    ref = H.oracle_verify(case)
+    exact, _ = H.check_verify(case, got, ref)
+    assert exact == 1
+    H.check_row_stats(case, got, _rows(case))
+
+
+@pytest.mark.parametrize("rule", ["greedy", "typical", "rejection"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_random_trees_ragged_vocab(rule, dtype):
+    d = H.dev()
+    rng = np.random.default_rng(len(rule) * 7 + len(dtype))
+    parents = [T.random_bfs_tree(rng, int(n), 6)[0] for n in (40, 7, 1, 90, 25)]
+    case = make_case(dtype=dtype, Hq=4, Hkv=1, d=64, Hd=128, V=1000, prefix_len=[5] * 5, parents=parents,
+                     rule=rule, tau=0.0 if rule == "greedy" else 0.8, eps=0.09, delta=0.3, seed=9,
+                     tokens=("iid", 0.8, 0.5) if rule == "rejection" else ("rank", 0.9), rng=rng)
+    got = H.gpu_verify(case, H.to_device(case, d))
+    assert got["status"] == 0
+    ref = H.oracle_verify(case)
+    exact, excluded = H.check_verify(case, got, ref)
+    assert exact + excluded == case.B
+    H.check_row_stats(case, got, _rows(case))
+
+
+def test_greedy_argmax_chains_reach_depth():
+    """Tokens equal to the parent's argmax (computed by the oracle) accept the deepest node."""
+    d = H.dev()
+    rng = np.random.default_rng(21)
+    parents = [T.random_bfs_tree(rng, 60, 7)[0], T.chain_tree(30)]
+    case = make_case(dtype="bf16", Hq=4, Hkv=1, d=64, Hd=256, V=3000, prefix_len=[3, 3], parents=parents,
+                     rule="greedy", tau=0.0, seed=4, tokens=("rank", 0.7), rng=rng)
+    z = oracle.logits(np.stack([case.f64("hidden")[b, i] for b in range(2) for i in range(case.N)]), case.f32("W"))
+    z = z.reshape(2, case.N, -1)
+    for b in range(2):
+        for c in range(1, case.n_nodes[b]):
+            case.tokens[b, c] = int(np.argmax(z[b, case.parent[b, c]]))
+    got = H.gpu_verify(case, H.to_device(case, d))
+    ref = H.oracle_verify(case)
+    H.check_verify(case, got, ref)
+    for b in range(2):
+        if not ref[b]["path_margins"]:
+            assert got["accept_len"][b] == T.depths(case.parent[b, : case.n_nodes[b]]).max()
+
+
+def test_llama8b_medusa63_typical_full():
+    d = H.dev()
+    case = H.config_case(2, 0)
+    got = H.gpu_verify(case, H.to_device(case, d))
+    assert got["status"] == 0
+    ref = H.oracle_verify(case)
+    exact, excluded = H.check_verify(case, got, ref)
+    assert exact + excluded == 1
+    H.check_row_stats(case, got, _rows(case, limit=16))
+
+
+def test_llama8b_b8_rejection_subset():
+    d = H.dev()
+    case = H.config_case(3, 1)
+    got = H.gpu_verify(case, H.to_device(case, d))
+    assert got["status"] == 0
+    req = [0, 3, 6]
+    ref = H.oracle_verify(case, requests=req)
+    H.check_verify(case, got, ref, requests=req)
+    H.check_row_stats(case, got, _rows(case, [0], limit=8))
+
+
+def test_eagle3_mapped_vocab_rejection_subset():
+    d = H.dev()
+    case = H.config_case(4, 2)
+    got = H.gpu_verify(case, H.to_device(case, d))
+    assert got["status"] == 0
+    req = [0, 17, 31]
+    ref = H.oracle_verify(case, requests=req)
+    H.check_verify(case, got, ref, requests=req)
+
+
+def test_llama70b_greedy_subset():
+    d = H.dev()
+    case = H.config_case(5, 3)
+    got = H.gpu_verify(case, H.to_device(case, d))
+    assert got["status"] == 0
+    req = [1]
+    ref = H.oracle_verify(case, requests=req)
+    H.check_verify(case, got, ref, requests=req)
+    H.check_row_stats(case, got, _rows(case, req, limit=8))

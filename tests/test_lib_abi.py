@@ -1,0 +1,110 @@
+"""C ABI checks that need no GPU: the library loads, exports every declared function, its struct
+layouts match the header, and host-side argument errors come back before any launch."""
+
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+import tree_speculative_decoding_split_gb300 as st
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spectree.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    st.build()
+    return st.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert {"spec_tree_attention", "spec_verify_accept", "spec_compact_kv", "spec_status_string",
+            "spec_tree_attention_workspace", "spec_verify_accept_workspace"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_struct_layout_matches_header():
+    src = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "spectree.h"
+#define P(T, f) printf(#T " " #f " %zu\n", offsetof(T, f));
+int main(void) {
+  printf("spec_attn_args size %zu\n", sizeof(spec_attn_args));
+  printf("spec_verify_args size %zu\n", sizeof(spec_verify_args));
+  printf("spec_compact_args size %zu\n", sizeof(spec_compact_args));
+  P(spec_attn_args, kv_capacity) P(spec_attn_args, q) P(spec_attn_args, lse) P(spec_attn_args, timing_end)
+  P(spec_verify_args, seed) P(spec_verify_args, hidden_states) P(spec_verify_args, row_argmax) P(spec_verify_args, timing_end)
+  P(spec_compact_args, kv_capacity) P(spec_compact_args, k_cache) P(spec_compact_args, new_len)
+  return 0;
+}
+"""
+    with tempfile.TemporaryDirectory() as td:
+        c = os.path.join(td, "l.c")
+        exe = os.path.join(td, "l")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {}
+    for line in out:
+        if line:
+            t, f, v = line.split()
+            got[(t, f)] = int(v)
+    py = {"spec_attn_args": st.AttnArgs, "spec_verify_args": st.VerifyArgs, "spec_compact_args": st.CompactArgs}
+    for (t, f), v in got.items():
+        cls = py[t]
+        if f == "size":
+            assert ctypes.sizeof(cls) == v, t
+        else:
+            assert getattr(cls, f).offset == v, (t, f)
+
+
+def test_status_strings(L):
+    for code in range(9):
+        assert st.status_string(code) and st.status_string(code) != "unknown status"
+    assert st.status_string(99) == "unknown status"
+
+
+def test_host_argument_errors_return_before_launch(L):
+    assert L.spec_tree_attention(None, None, 0, None, None) == 1
+    assert L.spec_verify_accept(None, None, 0, None, None) == 1
+    assert L.spec_compact_kv(None, None, None) == 1
+    a = st.AttnArgs(dtype=1, batch=1, n_max=4, num_q_heads=4, num_kv_heads=1, head_dim=96, kv_capacity=16)
+    assert L.spec_tree_attention(ctypes.byref(a), None, 0, None, None) == 2          # head_dim 96
+    assert L.spec_tree_attention_workspace(ctypes.byref(a)) == 0
+    a.head_dim = 64
+    assert L.spec_tree_attention(ctypes.byref(a), None, 0, None, None) == 1          # null tensors
+    a.n_max = 256
+    assert L.spec_tree_attention(ctypes.byref(a), None, 0, None, None) == 2          # > 255 nodes
+    v = st.VerifyArgs(dtype=1, batch=1, n_max=4, hidden=100, vocab=50, rule=0, path_cap=4)
+    assert L.spec_verify_accept(ctypes.byref(v), None, 0, None, None) == 2           # bf16 hidden % 64
+    v.hidden, v.rule, v.temperature = 128, 2, 0.0
+    assert L.spec_verify_accept(ctypes.byref(v), None, 0, None, None) == 1           # tau must be > 0
+    c = st.CompactArgs(dtype=0, batch=1, num_kv_heads=1, head_dim=64, kv_capacity=8, path_cap=0)
+    assert L.spec_compact_kv(ctypes.byref(c), None, None) == 1                        # path_cap 0
+
+
+def test_workspace_queries_are_host_only(L):
+    fake = ctypes.c_void_p(1 << 20)  # aligned non-null pointers, never dereferenced by the query
+    a = st.AttnArgs(dtype=1, batch=2, n_max=63, num_q_heads=32, num_kv_heads=8, head_dim=128, kv_capacity=4096,
+                    q=fake, k_cache=fake, v_cache=fake, prefix_len=fake, n_nodes=fake, parent=fake, out=fake)
+    assert L.spec_tree_attention_workspace(ctypes.byref(a)) > 2 * 63 * 32 * 128 * 4
+    v = st.VerifyArgs(dtype=1, batch=1, n_max=63, hidden=4096, vocab=128256, rule=2, temperature=1.0,
+                      draft_vocab=128256, path_cap=64, hidden_states=fake, lm_head_weight=fake, tokens=fake,
+                      parent=fake, n_nodes=fake, draft_probs=fake, accept_len=fake, path=fake, bonus_token=fake)
+    need = L.spec_verify_accept_workspace(ctypes.byref(v))
+    assert need >= 63 * 128256 * 4  # rejection keeps the fp32 logits
+    v.rule = 0
+    assert L.spec_verify_accept_workspace(ctypes.byref(v)) < need

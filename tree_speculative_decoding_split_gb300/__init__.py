@@ -1,0 +1,291 @@
+"""GB300-native tree verification for Medusa/EAGLE-style speculative decoding.
+
+Thin ctypes binding of ``libspectree.so`` (C ABI in ``include/spectree.h``).  This module only
+marshals arguments: it checks tensor placement, dtype and contiguity, carves nothing itself,
+and passes raw device pointers plus the current CUDA stream.  Every step of the computation
+runs in the library's CUDA kernels; if the library has not been built, every call raises.
+
+    tree_attention(...)   -> (out, lse)          one attention layer over the draft tree
+    verify_accept(...)    -> dict of outputs      LM head, acceptance, longest path, bonus token
+    compact_kv(...)       -> (src_slot, new_len)  in-place KV compaction of the accepted path
+"""
+
+import ctypes
+import os
+
+from ._build import LIB as _LIB_PATH
+from ._build import build  # noqa: F401
+
+SPEC_OK = 0
+STATUS_NAMES = {
+    0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARGUMENT", 2: "SPEC_ERR_UNSUPPORTED",
+    3: "SPEC_ERR_WORKSPACE_TOO_SMALL", 4: "SPEC_ERR_BAD_TREE", 5: "SPEC_ERR_CUDA",
+    6: "SPEC_ERR_BAD_TOKEN", 7: "SPEC_ERR_CAPACITY", 8: "SPEC_ERR_TIMEOUT",
+}
+DTYPE_F32, DTYPE_BF16 = 0, 1
+RULES = {"greedy": 0, "typical": 1, "rejection": 2}
+MAX_NODES = 255
+
+_vp = ctypes.c_void_p
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("batch", ctypes.c_int32), ("n_max", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("kv_capacity", ctypes.c_int64), ("scale", ctypes.c_float),
+                ("reserved0", ctypes.c_int32), ("q", _vp), ("k_cache", _vp), ("v_cache", _vp),
+                ("prefix_len", _vp), ("n_nodes", _vp), ("parent", _vp), ("out", _vp), ("lse", _vp),
+                ("timing_begin", _vp), ("timing_end", _vp)]
+
+
+class VerifyArgs(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("batch", ctypes.c_int32), ("n_max", ctypes.c_int32),
+                ("hidden", ctypes.c_int32), ("vocab", ctypes.c_int32), ("rule", ctypes.c_int32),
+                ("temperature", ctypes.c_float), ("eps", ctypes.c_float), ("delta", ctypes.c_float),
+                ("draft_vocab", ctypes.c_int32), ("path_cap", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("seed", ctypes.c_uint64), ("hidden_states", _vp), ("lm_head_weight", _vp), ("tokens", _vp),
+                ("parent", _vp), ("n_nodes", _vp), ("draft_probs", _vp), ("draft_to_target", _vp),
+                ("accept_len", _vp), ("path", _vp), ("bonus_token", _vp), ("margin_count", _vp),
+                ("bonus_margin", _vp), ("row_max", _vp), ("row_lse", _vp), ("row_entropy", _vp),
+                ("row_argmax", _vp), ("timing_begin", _vp), ("timing_end", _vp)]
+
+
+class CompactArgs(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("kv_capacity", ctypes.c_int64), ("path_cap", ctypes.c_int32),
+                ("reserved0", ctypes.c_int32), ("k_cache", _vp), ("v_cache", _vp), ("prefix_len", _vp),
+                ("path", _vp), ("accept_len", _vp), ("src_slot", _vp), ("new_len", _vp)]
+
+
+_lib_handle = None
+
+
+def lib():
+    """The loaded libspectree.so (raises if it has not been built)."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "tree_speculative_decoding_split_gb300.build() (no fallback exists)")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, argt in (("spec_tree_attention", [ctypes.POINTER(AttnArgs), _vp, ctypes.c_size_t, _vp, _vp]),
+                           ("spec_verify_accept", [ctypes.POINTER(VerifyArgs), _vp, ctypes.c_size_t, _vp, _vp]),
+                           ("spec_compact_kv", [ctypes.POINTER(CompactArgs), _vp, _vp])):
+            fn = getattr(L, name)
+            fn.argtypes = argt
+            fn.restype = ctypes.c_int32
+        L.spec_tree_attention_workspace.argtypes = [ctypes.POINTER(AttnArgs)]
+        L.spec_tree_attention_workspace.restype = ctypes.c_size_t
+        L.spec_verify_accept_workspace.argtypes = [ctypes.POINTER(VerifyArgs)]
+        L.spec_verify_accept_workspace.restype = ctypes.c_size_t
+        L.spec_status_string.argtypes = [ctypes.c_int32]
+        L.spec_status_string.restype = ctypes.c_char_p
+        _lib_handle = L
+    return _lib_handle
+
+
+def status_string(code):
+    return lib().spec_status_string(int(code)).decode()
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = int(code)
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.code, self.code)} ({status_string(code)})")
+
+
+def _check(code, where):
+    if code != SPEC_OK:
+        raise SpecError(code, where)
+
+
+# ---- torch marshalling (torch is used for device memory and streams only) ---------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need(t, name, dtype=None, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return _vp(s.cuda_stream)
+
+
+def _workspace(nbytes, device, workspace):
+    torch = _torch()
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def _status_buffer(dev_status, device):
+    torch = _torch()
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=device)
+    return dev_status
+
+
+def attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=None, scale=0.0):
+    """Build the C argument struct for tree attention (tensors are validated here)."""
+    torch = _torch()
+    _need(q, "q")
+    dev = q.device
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, q.dtype, dev)
+    for name, t in (("prefix_len", prefix_len), ("n_nodes", n_nodes), ("parent", parent)):
+        _need(t, name, torch.int32, dev)
+    B, N, Hq, d = q.shape
+    Hkv, L_cap = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Hkv, L_cap, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape must be [B][Hkv][L_cap][d]")
+    if tuple(parent.shape) != (B, N) or prefix_len.numel() != B or n_nodes.numel() != B:
+        raise ValueError("parent must be [B][N], prefix_len and n_nodes [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+    _need(out, "out", q.dtype, dev)
+    _need(lse, "lse", torch.float32, dev)
+    a = AttnArgs(dtype=_dtype_code(q), batch=B, n_max=N, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
+                 kv_capacity=L_cap, scale=float(scale), reserved0=0, q=_ptr(q), k_cache=_ptr(k_cache),
+                 v_cache=_ptr(v_cache), prefix_len=_ptr(prefix_len), n_nodes=_ptr(n_nodes), parent=_ptr(parent),
+                 out=_ptr(out), lse=_ptr(lse))
+    return a, out, lse
+
+
+def tree_attention(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=None, scale=0.0,
+                   workspace=None, dev_status=None, stream=None):
+    """Tree attention (see spec_tree_attention).  Returns (out, lse)."""
+    a, out, lse = attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out, lse, scale)
+    L = lib()
+    need = L.spec_tree_attention_workspace(ctypes.byref(a))
+    if need == 0:
+        _check(L.spec_tree_attention(ctypes.byref(a), None, 0, None, None), "spec_tree_attention")
+    ws = _workspace(need, q.device, workspace)
+    st = _status_buffer(dev_status, q.device)
+    _check(L.spec_tree_attention(ctypes.byref(a), _ptr(ws), need, _ptr(st), _stream(stream)), "spec_tree_attention")
+    return out, lse
+
+
+def verify_args(hidden, weight, tokens, parent, n_nodes, rule, temperature=0.0, eps=0.09, delta=0.3,
+                seed=0, draft_probs=None, draft_to_target=None, path_cap=None, hooks=False, outputs=None):
+    """Build the C argument struct for verify_accept; returns (args, outputs dict)."""
+    torch = _torch()
+    _need(hidden, "hidden")
+    dev = hidden.device
+    _need(weight, "weight", hidden.dtype, dev)
+    for name, t in (("tokens", tokens), ("parent", parent), ("n_nodes", n_nodes)):
+        _need(t, name, torch.int32, dev)
+    B, N, Hd = hidden.shape
+    V = weight.shape[0]
+    if weight.shape[1] != Hd or tuple(tokens.shape) != (B, N) or tuple(parent.shape) != (B, N):
+        raise ValueError("shape mismatch")
+    if path_cap is None:
+        path_cap = N
+    rule_code = RULES[rule] if isinstance(rule, str) else int(rule)
+    Vd = 0
+    if draft_probs is not None:
+        _need(draft_probs, "draft_probs", torch.float32, dev)
+        Vd = draft_probs.shape[-1]
+    if draft_to_target is not None:
+        _need(draft_to_target, "draft_to_target", torch.int32, dev)
+    if outputs is None:
+        outputs = dict(
+            accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+            path=torch.empty((B, path_cap), dtype=torch.int32, device=dev),
+            bonus_token=torch.empty(B, dtype=torch.int32, device=dev),
+            margin_count=torch.empty(B, dtype=torch.int32, device=dev),
+            bonus_margin=torch.empty(B, dtype=torch.int32, device=dev))
+        if hooks:
+            outputs.update(row_max=torch.empty((B, N), dtype=torch.float32, device=dev),
+                           row_lse=torch.empty((B, N), dtype=torch.float32, device=dev),
+                           row_entropy=torch.empty((B, N), dtype=torch.float32, device=dev),
+                           row_argmax=torch.empty((B, N), dtype=torch.int32, device=dev))
+    o = outputs
+    a = VerifyArgs(dtype=_dtype_code(hidden), batch=B, n_max=N, hidden=Hd, vocab=V, rule=rule_code,
+                   temperature=float(temperature), eps=float(eps), delta=float(delta), draft_vocab=Vd,
+                   path_cap=int(path_cap), reserved0=0, seed=int(seed) & 0xFFFFFFFFFFFFFFFF,
+                   hidden_states=_ptr(hidden), lm_head_weight=_ptr(weight), tokens=_ptr(tokens),
+                   parent=_ptr(parent), n_nodes=_ptr(n_nodes), draft_probs=_ptr(draft_probs),
+                   draft_to_target=_ptr(draft_to_target), accept_len=_ptr(o["accept_len"]), path=_ptr(o["path"]),
+                   bonus_token=_ptr(o["bonus_token"]), margin_count=_ptr(o.get("margin_count")),
+                   bonus_margin=_ptr(o.get("bonus_margin")), row_max=_ptr(o.get("row_max")),
+                   row_lse=_ptr(o.get("row_lse")), row_entropy=_ptr(o.get("row_entropy")),
+                   row_argmax=_ptr(o.get("row_argmax")))
+    return a, outputs
+
+
+def verify_accept(hidden, weight, tokens, parent, n_nodes, rule, temperature=0.0, eps=0.09, delta=0.3, seed=0,
+                  draft_probs=None, draft_to_target=None, path_cap=None, hooks=False, workspace=None,
+                  dev_status=None, stream=None, outputs=None):
+    """LM head + acceptance + longest path (see spec_verify_accept).  Returns a dict of tensors."""
+    a, outputs = verify_args(hidden, weight, tokens, parent, n_nodes, rule, temperature, eps, delta, seed,
+                             draft_probs, draft_to_target, path_cap, hooks, outputs)
+    L = lib()
+    need = L.spec_verify_accept_workspace(ctypes.byref(a))
+    if need == 0:
+        _check(L.spec_verify_accept(ctypes.byref(a), None, 0, None, None), "spec_verify_accept")
+    ws = _workspace(need, hidden.device, workspace)
+    st = _status_buffer(dev_status, hidden.device)
+    _check(L.spec_verify_accept(ctypes.byref(a), _ptr(ws), need, _ptr(st), _stream(stream)), "spec_verify_accept")
+    return outputs
+
+
+def compact_args(k_cache, v_cache, prefix_len, path, accept_len, src_slot=None, new_len=None):
+    torch = _torch()
+    _need(k_cache, "k_cache")
+    dev = k_cache.device
+    _need(v_cache, "v_cache", k_cache.dtype, dev)
+    for name, t in (("prefix_len", prefix_len), ("path", path), ("accept_len", accept_len)):
+        _need(t, name, torch.int32, dev)
+    B, Hkv, L_cap, d = k_cache.shape
+    path_cap = path.shape[1]
+    if src_slot is None:
+        src_slot = torch.empty((B, path_cap), dtype=torch.int32, device=dev)
+    if new_len is None:
+        new_len = torch.empty(B, dtype=torch.int32, device=dev)
+    a = CompactArgs(dtype=_dtype_code(k_cache), batch=B, num_kv_heads=Hkv, head_dim=d, kv_capacity=L_cap,
+                    path_cap=path_cap, reserved0=0, k_cache=_ptr(k_cache), v_cache=_ptr(v_cache),
+                    prefix_len=_ptr(prefix_len), path=_ptr(path), accept_len=_ptr(accept_len),
+                    src_slot=_ptr(src_slot), new_len=_ptr(new_len))
+    return a, src_slot, new_len
+
+
+def compact_kv(k_cache, v_cache, prefix_len, path, accept_len, src_slot=None, new_len=None, dev_status=None,
+               stream=None):
+    """In-place KV compaction (see spec_compact_kv).  Returns (src_slot, new_len)."""
+    a, src_slot, new_len = compact_args(k_cache, v_cache, prefix_len, path, accept_len, src_slot, new_len)
+    st = _status_buffer(dev_status, k_cache.device)
+    _check(lib().spec_compact_kv(ctypes.byref(a), _ptr(st), _stream(stream)), "spec_compact_kv")
+    return src_slot, new_len

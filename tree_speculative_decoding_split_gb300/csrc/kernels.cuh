@@ -1,0 +1,120 @@
+// Host-side launchers of the tree-verification kernels (internal to libspectree.so).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spectree {
+
+// ---- K0: tree preparation -------------------------------------------------------------------
+// Validates each request's tree (and optionally its KV capacity and tokens) and builds
+// depth [B][N] and the ancestor-or-self bit matrix anc [B][N][W] (W = ceil(N / 32) words).
+// bad[b] receives the request's error code (0 = fine).
+void launch_tree_prep(const int32_t* parent, const int32_t* n_nodes, const int32_t* prefix_len,
+                      long long kv_capacity, const int32_t* tokens, int vocab, int B, int N,
+                      int32_t* depth, uint32_t* anc, int32_t* bad, int32_t* dev_status,
+                      cudaStream_t stream);
+
+// ---- K1: tree attention ---------------------------------------------------------------------
+struct AttnParams {
+  const void* q;
+  void* out;
+  float* lse;
+  const float* k32;  // fp32 path only (raw cache pointers)
+  const float* v32;
+  const int32_t* prefix_len;
+  const int32_t* n_nodes;
+  const uint32_t* anc;
+  const int32_t* bad;
+  float* part_o;     // [B*N*Hq][n_split][d]
+  float2* part_ml;   // [B*N*Hq][n_split] (running max in log2 units, sum)
+  int B, N, Hq, Hkv, G, W, d;
+  long long L_cap;
+  int n_prefix;      // prefix splits
+  int chunk;         // keys per prefix split
+  int n_split;       // n_prefix + 1 (the last split holds the tree tail)
+  int n_rg;          // row groups of 128 (node, head) rows per KV head
+  float scale;
+  float scale_log2;
+  int32_t* dev_status;
+};
+
+struct AttnPlan {
+  int n_rg, n_prefix, chunk, n_split;
+};
+AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_sms);
+size_t attention_smem_bytes(int d);
+cudaError_t launch_attention_bf16(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
+                                  cudaStream_t stream);
+void launch_attention_merge_bf16(const AttnParams& p, cudaStream_t stream);
+void launch_attention_f32(const AttnParams& p, cudaStream_t stream);
+
+// ---- K2: LM head + row statistics -----------------------------------------------------------
+struct LmParams {
+  int R;           // rows (B * N)
+  int V, Hd;
+  int n_vt;        // vocabulary tiles of 128
+  int n_nc;        // node chunks of BN rows
+  int BN;
+  float inv_tau;
+  float4* part;    // [n_vt][R] {max, sumexp, sumexp*y, second max}
+  int* part_idx;   // [n_vt][R] argmax
+  float* logits;   // [R][V] raw z, or nullptr
+  int32_t* dev_status;
+};
+int lmhead_pick_bn(int R);
+size_t lmhead_smem_bytes(int BN);
+cudaError_t launch_lmhead_bf16(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p,
+                               int num_sms, cudaStream_t stream);
+void launch_lmhead_f32(const float* H, const float* W, const LmParams& p, cudaStream_t stream);
+
+struct ReduceParams {
+  const float4* part;
+  const int* part_idx;
+  const float* logits;     // [R][V] or nullptr
+  const void* hidden;      // [R][Hd]
+  const void* weight;      // [V][Hd]
+  int is_bf16;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const int32_t* n_nodes;
+  const int32_t* bad;
+  int B, N, R, V, Hd, n_vt;
+  float inv_tau;
+  float* rmax;  float* rlse;  float* rent;  float* rgap;  int32_t* rarg;  float* clog;
+  float* hook_max; float* hook_lse; float* hook_ent; int32_t* hook_arg;
+};
+void launch_row_reduce(const ReduceParams& p, cudaStream_t stream);
+
+// ---- K3: acceptance + longest path ----------------------------------------------------------
+struct AcceptParams {
+  int B, N, V, Vd, rule, path_cap;
+  float inv_tau, log_eps, log_delta;
+  unsigned long long seed;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const int32_t* n_nodes;
+  const int32_t* depth;
+  const int32_t* bad;
+  const float* rmax; const float* rlse; const float* rent; const float* rgap;
+  const int32_t* rarg; const float* clog;
+  const float* logits;         // [R][V] (rejection)
+  const float* draft;          // [B][N][Vd] (rejection)
+  const int32_t* inv_map;      // [V] target -> draft index, -1 if unmapped; nullptr = identity
+  const int32_t* map_bad;      // non-zero when the draft map is invalid
+  float* rbuf;                 // [B][2][V] residual buffers (rejection)
+  int32_t* accept_len; int32_t* path; int32_t* bonus; int32_t* margin_count; int32_t* bonus_margin;
+  int32_t* dev_status;
+};
+void launch_build_inverse_map(const int32_t* map, int Vd, int V, int32_t* inv, int32_t* map_bad,
+                              int32_t* dev_status, cudaStream_t stream);
+void launch_accept(const AcceptParams& p, cudaStream_t stream);
+
+// ---- K4: KV compaction ----------------------------------------------------------------------
+void launch_compact_kv(void* k, void* v, int elem_bytes, const int32_t* prefix_len,
+                       const int32_t* path, const int32_t* accept_len, int B, int Hkv, int d,
+                       long long L_cap, int path_cap, int32_t* src_slot, int32_t* new_len,
+                       int32_t* dev_status, cudaStream_t stream);
+
+}  // namespace spectree

@@ -1,0 +1,509 @@
+// K2: LM head z = W h for every tree node, fused with per-row softmax statistics.
+// K2f: fp32 variant (SIMT).  K2r: merge of the per-vocabulary-tile statistics, child logits.
+//
+// The LM head is a linear layer followed by softmax (tech-tldr "多トークン予測（Medusa・EAGLE）",
+// section "Medusa"; jisaku glossary "Medusa", architecture table: hidden_dim x vocab_size).  It
+// is the one dense contraction of the verification step: [rows x hidden] . [hidden x vocab].
+//
+// bf16 kernel (tcgen05).  The vocabulary sits on the MMA M dimension (tiles of 128 rows of W)
+// and the tree rows on N (BN = 32..256 per tile), so a batch of 63 nodes still fills a full
+// M = 128 instruction.  A persistent grid walks (vocab tile, row chunk) units; warp 0 issues
+// TMA loads of W and hidden-state tiles (128-byte swizzle) into a shared-memory ring, warp 1
+// issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulators in tensor memory, double-buffered
+// across units), warps 2..5 drain the accumulators with tcgen05.ld and reduce every node's
+// column over the 128 vocabulary rows with warp shuffles into {max, sum exp, sum exp*y, second
+// max, argmax} at y = z / tau.  Full fp32 logits go to HBM only when the caller needs them
+// (rejection sampling), written once from the same epilogue.
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace spectree {
+
+namespace {
+
+constexpr int kBM = 128;  // vocabulary rows per tile (MMA M)
+constexpr int kBK = 64;   // hidden elements per stage (one 128-byte swizzle atom of bf16)
+constexpr int kLmThreads = 192;
+
+// ---- tcgen05 / TMEM wrappers ----------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] . B[smem]^T, both K-major, bf16 -> fp32.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with 128-byte swizzle:
+// rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset
+  d |= (uint64_t)1 << 46;            // version
+  d |= (uint64_t)2 << 61;            // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+template <int BN>
+struct LmCfg {
+  static constexpr int kStageA = kBM * kBK * 2;
+  static constexpr int kStageB = BN * kBK * 2;
+  static constexpr int kStage = kStageA + kStageB;
+  static constexpr int kStages = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+  static constexpr int kEpiBytes = 4 * BN * (int)sizeof(float4) + 4 * BN * (int)sizeof(int);
+  static constexpr int kSmem = 1024 + kStages * kStage + kEpiBytes + 256;
+};
+
+}  // namespace
+
+template <int BN>
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                     const LmParams p) {
+  using C = LmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + C::kStages * C::kStageA;
+  float4* sEpi = reinterpret_cast<float4*>(base + C::kStages * C::kStage);
+  int* sEpiIdx = reinterpret_cast<int*>(sEpi + 4 * BN);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpiIdx + 4 * BN);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drained = tempty + 2;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ uint32_t s_issued, s_consumed;
+  __shared__ int s_epi_fail;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_kb = p.Hd / kBK;
+  const int total = p.n_vt * p.n_nc;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drained, 1);
+    s_abort = 0;
+    s_epi_fail = 0;
+    s_issued = 0;
+    s_consumed = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer ----
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_h = l2_policy_evict_last();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const int vt = u / p.n_nc, nc = u % p.n_nc;
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % C::kStages;
+          if (!mbar_wait_bounded(&empty[st], ((it / C::kStages) & 1) ^ 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], C::kStage);
+          tma_load_2d(sA + st * C::kStageA, &tmW, &full[st], kb * kBK, vt * kBM, pol_w);
+          tma_load_2d(sB + st * C::kStageB, &tmH, &full[st], kb * kBK, nc * BN, pol_h);
+          s_issued = it + 1;
+        }
+      }
+      if (!ok) {
+        s_abort = 1;
+        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      constexpr uint32_t idesc = idesc_bf16(kBM, BN);
+      uint32_t it = 0;
+      int lu = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++lu) {
+        const int a = lu & 1;
+        if (!mbar_wait_bounded(&tempty[a], ((lu >> 1) & 1) ^ 1, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(a * BN);
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % C::kStages;
+          if (!mbar_wait_bounded(&full[st], (it / C::kStages) & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_sw128(smem_u32(sA + st * C::kStageA));
+          const uint64_t bd = sdesc_sw128(smem_u32(sB + st * C::kStageB));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+          umma_commit(&empty[st]);
+          s_consumed = it + 1;
+        }
+        if (ok) umma_commit(&tfull[a]);
+      }
+      if (!ok) {
+        s_abort = 1;
+        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+      }
+      // Every MMA issued by this thread has finished once `drained` completes.
+      umma_commit(drained);
+      mbar_wait_bounded(drained, 0, nullptr);
+    }
+  } else {
+    // ---- epilogue: warps 2..5, TMEM lane quarter q = warp % 4 ----
+    const int q = warp & 3;
+    const int etid = (warp - 2) * 32 + lane;
+    int lu = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++lu) {
+      const int vt = u / p.n_nc, nc = u % p.n_nc;
+      const int a = lu & 1;
+      // The four epilogue warps agree on the outcome of the wait before going on, so that
+      // none of them can be left alone at a named barrier.
+      if (!mbar_wait_bounded(&tfull[a], (lu >> 1) & 1, &s_abort) && lane == 0) s_epi_fail = 1;
+      named_bar_sync(1, 128);
+      if (s_epi_fail) {
+        if (etid == 0) {
+          s_abort = 1;
+          set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      const int v = vt * kBM + q * 32 + lane;
+      const bool vvalid = v < p.V;
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + cc * 32), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = cc * 32 + jj;
+          const int n = nc * BN + j;
+          const float z = __uint_as_float(r[jj]);
+          if (p.logits && vvalid && n < p.R) p.logits[(size_t)n * p.V + v] = z;
+          const float y = vvalid ? z * p.inv_tau : -INFINITY;
+          const float m = warp_max(y);
+          const unsigned bal = __ballot_sync(0xffffffffu, y == m);
+          const int first = __ffs(bal) - 1;
+          const float y2 = warp_max(lane == first ? -INFINITY : y);
+          const float e = (y > -INFINITY) ? expf(y - m) : 0.f;
+          const float s = warp_sum(e);
+          const float t = warp_sum(e > 0.f ? e * y : 0.f);
+          if (lane == jj) {
+            sEpi[q * BN + j] = make_float4(m, s, t, y2);
+            sEpiIdx[q * BN + j] = (m > -INFINITY) ? vt * kBM + q * 32 + first : 0x7fffffff;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+      named_bar_sync(1, 128);
+      for (int j = etid; j < BN; j += 128) {
+        const int n = nc * BN + j;
+        if (n < p.R) {
+          RowPart acc = rowpart_empty();
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const float4 f = sEpi[qq * BN + j];
+            RowPart o;
+            o.m = f.x; o.s = f.y; o.t = f.z; o.y2 = f.w; o.idx = sEpiIdx[qq * BN + j];
+            acc = rowpart_merge(acc, o);
+          }
+          p.part[(size_t)vt * p.R + n] = make_float4(acc.m, acc.s, acc.t, acc.y2);
+          p.part_idx[(size_t)vt * p.R + n] = acc.idx;
+        }
+      }
+      named_bar_sync(1, 128);
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort) {
+    // Let the copies still in flight land before shared memory is released.
+    for (uint32_t it = s_consumed; it < s_issued; ++it)
+      mbar_wait_bounded(&full[it % C::kStages], (it / C::kStages) & 1, nullptr);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+// ---- fp32 path ------------------------------------------------------------------------------
+
+// logits[R][V] = H[R][Hd] . W[V][Hd]^T, 64 x 64 output tile per CTA, 4 x 4 per thread.
+__global__ void __launch_bounds__(256) lmhead_f32_kernel(const float* __restrict__ H, const float* __restrict__ W,
+                                                         float* __restrict__ logits, int R, int V, int Hd) {
+  __shared__ float sH[16][64 + 1];
+  __shared__ float sW[16][64 + 1];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int r0 = blockIdx.y * 64, v0 = blockIdx.x * 64;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < Hd; k0 += 16) {
+    for (int e = threadIdx.x; e < 16 * 64; e += 256) {
+      const int kk = e & 15, rr = e >> 4;
+      sH[kk][rr] = (r0 + rr < R && k0 + kk < Hd) ? H[(size_t)(r0 + rr) * Hd + k0 + kk] : 0.f;
+      sW[kk][rr] = (v0 + rr < V && k0 + kk < Hd) ? W[(size_t)(v0 + rr) * Hd + k0 + kk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], bw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { a[i] = sH[kk][ty * 4 + i]; bw[i] = sW[kk][tx * 4 + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bw[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = r0 + ty * 4 + i, v = v0 + tx * 4 + j;
+      if (r < R && v < V) logits[(size_t)r * V + v] = acc[i][j];
+    }
+}
+
+// Partial statistics of logits[row][vt*128 .. +128): one warp per (tile, row).
+__global__ void __launch_bounds__(256) stats_from_logits_kernel(const float* __restrict__ logits, int R, int V,
+                                                                int n_vt, float inv_tau, float4* __restrict__ part,
+                                                                int* __restrict__ part_idx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t id = (size_t)blockIdx.x * 8 + warp;
+  if (id >= (size_t)n_vt * R) return;
+  const int vt = (int)(id / R), n = (int)(id % R);
+  RowPart acc = rowpart_empty();
+  for (int k = 0; k < 4; ++k) {
+    const int v = vt * kBM + k * 32 + lane;
+    const float y = (v < V) ? logits[(size_t)n * V + v] * inv_tau : -INFINITY;
+    const float m = warp_max(y);
+    const unsigned bal = __ballot_sync(0xffffffffu, y == m);
+    const int first = __ffs(bal) - 1;
+    const float y2 = warp_max(lane == first ? -INFINITY : y);
+    const float e = (y > -INFINITY) ? expf(y - m) : 0.f;
+    RowPart o;
+    o.m = m; o.y2 = y2;
+    o.s = warp_sum(e);
+    o.t = warp_sum(e > 0.f ? e * y : 0.f);
+    o.idx = (m > -INFINITY) ? vt * kBM + k * 32 + first : 0x7fffffff;
+    acc = rowpart_merge(acc, o);
+  }
+  if (lane == 0) {
+    part[id] = make_float4(acc.m, acc.s, acc.t, acc.y2);
+    part_idx[id] = acc.idx;
+  }
+}
+
+// ---- K2r: per-row statistics + child logits -------------------------------------------------
+
+__device__ __forceinline__ RowPart shfl_rowpart(const RowPart& a, int o) {
+  RowPart r;
+  r.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+  r.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+  r.t = __shfl_xor_sync(0xffffffffu, a.t, o);
+  r.y2 = __shfl_xor_sync(0xffffffffu, a.y2, o);
+  r.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
+  return r;
+}
+
+__global__ void __launch_bounds__(256) row_reduce_kernel(const ReduceParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + warp;
+  if (n >= p.R) return;
+  const int b = n / p.N, i = n % p.N;
+  const bool real = !p.bad[b] && i < p.n_nodes[b];
+  RowPart acc = rowpart_empty();
+  if (real) {
+    for (int vt = lane; vt < p.n_vt; vt += 32) {
+      const float4 f = p.part[(size_t)vt * p.R + n];
+      RowPart o;
+      o.m = f.x; o.s = f.y; o.t = f.z; o.y2 = f.w; o.idx = p.part_idx[(size_t)vt * p.R + n];
+      acc = rowpart_merge(acc, o);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc = rowpart_merge(acc, shfl_rowpart(acc, o));
+  }
+  float clog = 0.f;
+  if (real && i > 0) {
+    const int pn = p.parent[n];
+    const int x = p.tokens[n];
+    const size_t prow = (size_t)b * p.N + pn;
+    if (p.logits) {
+      clog = p.logits[prow * p.V + x];
+    } else if (p.is_bf16) {
+      const __nv_bfloat16* hw = static_cast<const __nv_bfloat16*>(p.hidden) + prow * p.Hd;
+      const __nv_bfloat16* ww = static_cast<const __nv_bfloat16*>(p.weight) + (size_t)x * p.Hd;
+      float d = 0.f;
+      for (int k = lane * 8; k < p.Hd; k += 256) {
+        const uint4 hv = *reinterpret_cast<const uint4*>(hw + k);
+        const uint4 wv = *reinterpret_cast<const uint4*>(ww + k);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hv);
+        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 hf = __bfloat1622float2(h2[e]);
+          const float2 wf = __bfloat1622float2(w2[e]);
+          d = fmaf(hf.x, wf.x, d);
+          d = fmaf(hf.y, wf.y, d);
+        }
+      }
+      clog = warp_sum(d);
+    } else {
+      const float* hw = static_cast<const float*>(p.hidden) + prow * p.Hd;
+      const float* ww = static_cast<const float*>(p.weight) + (size_t)x * p.Hd;
+      float d = 0.f;
+      for (int k = lane; k < p.Hd; k += 32) d = fmaf(hw[k], ww[k], d);
+      clog = warp_sum(d);
+    }
+  }
+  if (lane == 0) {
+    float mx = 0.f, lse = 0.f, ent = 0.f, gap = 0.f;
+    int am = -1;
+    if (real) {
+      mx = acc.m;
+      lse = acc.m + logf(acc.s);
+      ent = lse - acc.t / acc.s;
+      am = acc.idx;
+      gap = (acc.y2 == -INFINITY) ? INFINITY : (acc.m - acc.y2) / p.inv_tau;
+    }
+    p.rmax[n] = mx; p.rlse[n] = lse; p.rent[n] = ent; p.rgap[n] = gap; p.rarg[n] = am; p.clog[n] = clog;
+    if (p.hook_max) p.hook_max[n] = mx;
+    if (p.hook_lse) p.hook_lse[n] = lse;
+    if (p.hook_ent) p.hook_ent[n] = ent;
+    if (p.hook_arg) p.hook_arg[n] = am;
+  }
+}
+
+// ---- host side ------------------------------------------------------------------------------
+
+int lmhead_pick_bn(int R) {
+  if (R <= 32) return 32;
+  if (R <= 64) return 64;
+  if (R <= 128) return 128;
+  return 256;
+}
+
+size_t lmhead_smem_bytes(int BN) {
+  switch (BN) {
+    case 32: return LmCfg<32>::kSmem;
+    case 64: return LmCfg<64>::kSmem;
+    case 128: return LmCfg<128>::kSmem;
+    default: return LmCfg<256>::kSmem;
+  }
+}
+
+template <int BN>
+static cudaError_t launch_lm(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p, int num_sms,
+                             cudaStream_t stream) {
+  const int smem = LmCfg<BN>::kSmem;
+  cudaError_t err = cudaFuncSetAttribute(lmhead_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  const int total = p.n_vt * p.n_nc;
+  const int grid = total < num_sms ? total : num_sms;
+  lmhead_tc_kernel<BN><<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lmhead_bf16(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p, int num_sms,
+                               cudaStream_t stream) {
+  switch (p.BN) {
+    case 32: return launch_lm<32>(tmW, tmH, p, num_sms, stream);
+    case 64: return launch_lm<64>(tmW, tmH, p, num_sms, stream);
+    case 128: return launch_lm<128>(tmW, tmH, p, num_sms, stream);
+    default: return launch_lm<256>(tmW, tmH, p, num_sms, stream);
+  }
+}
+
+void launch_lmhead_f32(const float* H, const float* W, const LmParams& p, cudaStream_t stream) {
+  const dim3 grid((p.V + 63) / 64, (p.R + 63) / 64);
+  lmhead_f32_kernel<<<grid, 256, 0, stream>>>(H, W, p.logits, p.R, p.V, p.Hd);
+  const size_t units = (size_t)p.n_vt * p.R;
+  stats_from_logits_kernel<<<(unsigned)((units + 7) / 8), 256, 0, stream>>>(p.logits, p.R, p.V, p.n_vt, p.inv_tau,
+                                                                            p.part, p.part_idx);
+}
+
+void launch_row_reduce(const ReduceParams& p, cudaStream_t stream) {
+  row_reduce_kernel<<<(p.R + 7) / 8, 256, 0, stream>>>(p);
+}
+
+}  // namespace spectree
