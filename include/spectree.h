@@ -200,6 +200,32 @@ typedef struct spec_compact_args {
 
 spec_status spec_compact_kv(const spec_compact_args* args, int32_t* dev_status, void* stream);
 
+/* ---------------------------------------------------------------------------------------
+ * spec_verify_accept without a caller workspace.  (The pages have no counterpart: this is a
+ * deployment convenience, not part of the method.)
+ *
+ * For callers that cannot allocate device memory themselves -- for example code running inside
+ * a host framework's callback or plugin that has no access to the framework's allocator, or a
+ * latency-critical loop where cudaMalloc would synchronise the device -- this entry point runs
+ * exactly spec_verify_accept, but takes its scratch space from a fixed array of
+ * SPEC_NOALLOC_SCRATCH_BYTES bytes that lives in device memory for as long as the library is
+ * loaded (every GPU that loads the library holds it until process exit).  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   - Inputs and outputs are the caller's device memory, as for spec_verify_accept.
+ *   - Shapes whose spec_verify_accept_workspace() exceeds SPEC_NOALLOC_SCRATCH_BYTES are
+ *     rejected with SPEC_ERR_WORKSPACE_TOO_SMALL before anything is launched (at a 128256-token
+ *     vocabulary this fits greedy / typical verification of up to a few hundred tree rows;
+ *     rejection sampling keeps fp32 logits and fits only small rows x vocabulary products).
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's contents; every
+ *     call overwrites what it reads.  Calls whose kernels overlap on the GPU (different streams,
+ *     or different host threads without ordering) race on the array and must not be issued.
+ * Other errors are those of spec_verify_accept. */
+#define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+spec_status spec_verify_accept_noalloc(const spec_verify_args* args, int32_t* dev_status, void* stream);
+
 /* Static English description of a status code (never NULL). */
 const char* spec_status_string(spec_status status);
 

@@ -289,3 +289,27 @@ def compact_kv(k_cache, v_cache, prefix_len, path, accept_len, src_slot=None, ne
     st = _status_buffer(dev_status, k_cache.device)
     _check(lib().spec_compact_kv(ctypes.byref(a), _ptr(st), _stream(stream)), "spec_compact_kv")
     return src_slot, new_len
+
+
+def verify_accept_noalloc(hidden, weight, tokens, parent, n_nodes, rule, temperature=0.0, eps=0.09, delta=0.3,
+                          seed=0, draft_probs=None, draft_to_target=None, path_cap=None, hooks=False,
+                          dev_status=None, stream=None, outputs=None):
+    """verify_accept for callers that cannot allocate device scratch memory.
+
+    Same computation as ``verify_accept``; the library takes its scratch from a fixed device array
+    (``NOALLOC_SCRATCH_BYTES``) instead of a workspace, so nothing is allocated for scratch.  Output
+    tensors are still the caller's (created here only when ``outputs`` is None).  Calls whose
+    kernels overlap on the GPU share that array and race; the first call on a device should come
+    before any stream capture.
+    """
+    a, outputs = verify_args(hidden, weight, tokens, parent, n_nodes, rule, temperature, eps, delta, seed,
+                             draft_probs, draft_to_target, path_cap, hooks, outputs)
+    fn = lib().spec_verify_accept_noalloc
+    fn.argtypes = [ctypes.POINTER(VerifyArgs), _vp, _vp]
+    fn.restype = ctypes.c_int32
+    st = _status_buffer(dev_status, hidden.device)
+    _check(fn(ctypes.byref(a), _ptr(st), _stream(stream)), "spec_verify_accept_noalloc")
+    return outputs
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
