@@ -65,7 +65,8 @@ def test_bad_trees_and_capacity_set_status_and_zero_outputs():
     assert got["status"] == 4
     assert got["accept_len"][1] == 0 and got["bonus_token"][1] == -1 and got["path"][1, 0] == 0
     assert (got["path"][1, 1:] == -1).all()
-    # capacity: prefix + nodes beyond L_cap
+    # capacity: prefix + nodes beyond L_cap (request 1 repaired first: one error per call)
+    t["parent"][1] = t["parent"][0]
     t["prefix_len"][0] = case.L_cap
     _, _, status = H.gpu_attention(case, t)
     assert status == 7  # SPEC_ERR_CAPACITY

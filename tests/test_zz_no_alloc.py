@@ -66,13 +66,15 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     d = H.dev()
-    case = _case("bf16", 3, "typical")
-    t = H.to_device(case, d)
-    hid = torch.zeros((3, 150, 256), dtype=torch.bfloat16, device=d)  # 450 rows ...
-    W = torch.zeros((128256, 256), dtype=torch.bfloat16, device=d)     # ... x 1002 vocabulary tiles
-    tok = torch.zeros((3, 150), dtype=torch.int32, device=d)
-    par = torch.full((3, 150), -1, dtype=torch.int32, device=d)
-    a, _ = st.verify_args(hid, W, tok, par, t["n_nodes"], "typical", 1.0, 0.09, 0.3, 0, path_cap=150)
+    # rejection sampling keeps fp32 logits: 32 rows x 128256 tokens x 4 B = 16 MB of scratch
+    B, N, Hd, V = 1, 32, 256, 128256
+    hid = torch.zeros((B, N, Hd), dtype=torch.bfloat16, device=d)
+    W = torch.zeros((V, Hd), dtype=torch.bfloat16, device=d)
+    tok = torch.zeros((B, N), dtype=torch.int32, device=d)
+    par = torch.full((B, N), -1, dtype=torch.int32, device=d)
+    nn = torch.full((B,), N, dtype=torch.int32, device=d)
+    draft = torch.zeros((B, N, V), dtype=torch.float32, device=d)
+    a, _ = st.verify_args(hid, W, tok, par, nn, "rejection", 1.0, 0.09, 0.3, 0, draft_probs=draft, path_cap=N)
     assert st.lib().spec_verify_accept_workspace(ctypes.byref(a)) > st.NOALLOC_SCRATCH_BYTES
     fn = st.lib().spec_verify_accept_noalloc
     fn.argtypes = [ctypes.POINTER(st.VerifyArgs), ctypes.c_void_p, ctypes.c_void_p]

@@ -94,7 +94,7 @@ spec_status check_attn(const spec_attn_args* a) {
 }
 
 struct AttnLayout {
-  int32_t* depth; uint32_t* anc; int32_t* bad; float* part_o; float2* part_ml;
+  int32_t* depth; uint32_t* anc; int32_t* bad; float* part_o; float2* part_ml; int32_t* counters;
   AttnPlan plan;
   size_t bytes;
 };
@@ -110,10 +110,12 @@ AttnLayout layout_attn(const spec_attn_args* a, void* ws) {
   l.bad = c.take<int32_t>(B);
   l.part_o = nullptr;
   l.part_ml = nullptr;
+  l.counters = nullptr;
   if (a->dtype == SPEC_DTYPE_BF16) {
     const size_t rows = (size_t)B * N * a->num_q_heads;
     l.part_o = c.take<float>(rows * l.plan.n_split * a->head_dim);
     l.part_ml = c.take<float2>(rows * l.plan.n_split);
+    l.counters = c.take<int32_t>((size_t)B * a->num_kv_heads * l.plan.n_rg);
   }
   l.bytes = c.off;
   return l;
@@ -149,33 +151,36 @@ spec_status check_verify(const spec_verify_args* a) {
 }
 
 struct VerifyLayout {
-  int32_t* depth; uint32_t* anc; int32_t* bad;
   float4* part; int* part_idx;
   float *rmax, *rlse, *rent, *rgap, *clog; int32_t* rarg;
-  float* logits; float* rbuf; int32_t* inv; int32_t* map_bad;
-  int R, n_vt, BN, n_nc;
+  float* logits; float* rbuf; int32_t* inv; int32_t* map_bad; int32_t* counters;
+  int R, n_vt, BN, n_nc, cpc, n_parts;
   size_t bytes;
 };
 
 VerifyLayout layout_verify(const spec_verify_args* a, void* ws) {
   VerifyLayout l;
-  const int B = a->batch, N = a->n_max, W = (N + 31) / 32;
+  const int B = a->batch, N = a->n_max;
   l.R = B * N;
   l.n_vt = (a->vocab + 127) / 128;
   l.BN = lmhead_pick_bn(l.R);
   l.n_nc = (l.R + l.BN - 1) / l.BN;
+  const int sms = num_sms_current();
+  l.cpc = sms / l.n_nc;
+  if (l.cpc < 1) l.cpc = 1;
+  if (l.cpc > l.n_vt) l.cpc = l.n_vt;
+  // statistics records per row: one per CTA of the row's chunk (bf16), one per tile (fp32)
+  l.n_parts = (a->dtype == SPEC_DTYPE_BF16) ? l.cpc : l.n_vt;
   Carver c(ws);
-  l.depth = c.take<int32_t>((size_t)B * N);
-  l.anc = c.take<uint32_t>((size_t)B * N * W);
-  l.bad = c.take<int32_t>(B);
-  l.part = c.take<float4>((size_t)l.n_vt * l.R);
-  l.part_idx = c.take<int>((size_t)l.n_vt * l.R);
+  l.part = c.take<float4>((size_t)l.n_parts * l.R);
+  l.part_idx = c.take<int>((size_t)l.n_parts * l.R);
   l.rmax = c.take<float>(l.R);
   l.rlse = c.take<float>(l.R);
   l.rent = c.take<float>(l.R);
   l.rgap = c.take<float>(l.R);
   l.clog = c.take<float>(l.R);
   l.rarg = c.take<int32_t>(l.R);
+  l.counters = c.take<int32_t>(B);
   const bool need_logits = a->rule == SPEC_RULE_REJECTION || a->dtype == SPEC_DTYPE_F32;
   l.logits = need_logits ? c.take<float>((size_t)l.R * a->vocab) : nullptr;
   l.rbuf = nullptr;
@@ -223,8 +228,9 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const AttnLayout l = layout_attn(a, workspace);
   const int B = a->batch, N = a->n_max, Hq = a->num_q_heads, Hkv = a->num_kv_heads, d = a->head_dim;
-  launch_tree_prep(a->parent, a->n_nodes, a->prefix_len, a->kv_capacity, nullptr, 0, B, N, l.depth, l.anc, l.bad,
-                   dev_status, stream);
+  if (a->dtype == SPEC_DTYPE_F32)
+    launch_tree_prep(a->parent, a->n_nodes, a->prefix_len, a->kv_capacity, nullptr, 0, B, N, l.depth, l.anc, l.bad,
+                     dev_status, stream);
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
   p.q = a->q;
@@ -234,6 +240,8 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
   p.n_nodes = a->n_nodes;
   p.anc = l.anc;
   p.bad = l.bad;
+  p.parent = a->parent;
+  p.counters = l.counters;
   p.part_o = l.part_o;
   p.part_ml = l.part_ml;
   p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.W = (N + 31) / 32; p.d = d;
@@ -259,10 +267,11 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
     if (!make_map_bf16(&tmK, a->k_cache, 3, dims, strides, box) ||
         !make_map_bf16(&tmV, a->v_cache, 3, dims, strides, box))
       return SPEC_ERR_CUDA;
+    const size_t ncnt = (size_t)B * Hkv * l.plan.n_rg;
+    if (cudaMemsetAsync(l.counters, 0, ncnt * sizeof(int32_t), stream) != cudaSuccess) return SPEC_ERR_CUDA;
     record(a->timing_begin, stream);
     if (launch_attention_bf16(&tmK, &tmV, p, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     record(a->timing_end, stream);
-    launch_attention_merge_bf16(p, stream);
   }
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -281,18 +290,19 @@ spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const VerifyLayout l = layout_verify(a, workspace);
   const int B = a->batch, N = a->n_max, V = a->vocab, Hd = a->hidden;
-  launch_tree_prep(a->parent, a->n_nodes, nullptr, 0, a->tokens, V, B, N, l.depth, l.anc, l.bad, dev_status, stream);
   if (a->rule == SPEC_RULE_REJECTION && a->draft_to_target)
     launch_build_inverse_map(a->draft_to_target, a->draft_vocab, V, l.inv, l.map_bad, dev_status, stream);
   const float inv_tau = (a->rule == SPEC_RULE_GREEDY) ? 1.f : 1.f / a->temperature;
 
   LmParams lp;
   std::memset(&lp, 0, sizeof(lp));
-  lp.R = l.R; lp.V = V; lp.Hd = Hd; lp.n_vt = l.n_vt; lp.n_nc = l.n_nc; lp.BN = l.BN;
+  lp.R = l.R; lp.V = V; lp.Hd = Hd; lp.n_vt = l.n_vt; lp.n_nc = l.n_nc; lp.BN = l.BN; lp.cpc = l.cpc;
   lp.inv_tau = inv_tau;
   lp.part = l.part;
   lp.part_idx = l.part_idx;
   lp.logits = l.logits;
+  lp.counters = l.counters;
+  lp.n_counters = B;
   lp.dev_status = dev_status;
   if (a->dtype == SPEC_DTYPE_BF16) {
     CUtensorMap tmW, tmH;
@@ -309,21 +319,12 @@ spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_
     if (launch_lmhead_bf16(&tmW, &tmH, lp, sms, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     record(a->timing_end, stream);
   } else {
+    if (cudaMemsetAsync(l.counters, 0, (size_t)B * sizeof(int32_t), stream) != cudaSuccess) return SPEC_ERR_CUDA;
     record(a->timing_begin, stream);
     launch_lmhead_f32(static_cast<const float*>(a->hidden_states), static_cast<const float*>(a->lm_head_weight), lp,
                       stream);
     record(a->timing_end, stream);
   }
-
-  ReduceParams rp;
-  std::memset(&rp, 0, sizeof(rp));
-  rp.part = l.part; rp.part_idx = l.part_idx; rp.logits = l.logits;
-  rp.hidden = a->hidden_states; rp.weight = a->lm_head_weight; rp.is_bf16 = a->dtype == SPEC_DTYPE_BF16;
-  rp.tokens = a->tokens; rp.parent = a->parent; rp.n_nodes = a->n_nodes; rp.bad = l.bad;
-  rp.B = B; rp.N = N; rp.R = l.R; rp.V = V; rp.Hd = Hd; rp.n_vt = l.n_vt; rp.inv_tau = inv_tau;
-  rp.rmax = l.rmax; rp.rlse = l.rlse; rp.rent = l.rent; rp.rgap = l.rgap; rp.rarg = l.rarg; rp.clog = l.clog;
-  rp.hook_max = a->row_max; rp.hook_lse = a->row_lse; rp.hook_ent = a->row_entropy; rp.hook_arg = a->row_argmax;
-  launch_row_reduce(rp, stream);
 
   AcceptParams ap;
   std::memset(&ap, 0, sizeof(ap));
@@ -332,13 +333,25 @@ spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_
   ap.log_eps = (a->eps > 0.f) ? logf(a->eps) : -INFINITY;
   ap.log_delta = (a->delta > 0.f) ? logf(a->delta) : -INFINITY;
   ap.seed = a->seed;
-  ap.tokens = a->tokens; ap.parent = a->parent; ap.n_nodes = a->n_nodes; ap.depth = l.depth; ap.bad = l.bad;
+  ap.tokens = a->tokens; ap.parent = a->parent; ap.n_nodes = a->n_nodes;
   ap.rmax = l.rmax; ap.rlse = l.rlse; ap.rent = l.rent; ap.rgap = l.rgap; ap.rarg = l.rarg; ap.clog = l.clog;
   ap.logits = l.logits; ap.draft = a->draft_probs; ap.inv_map = l.inv; ap.map_bad = l.map_bad; ap.rbuf = l.rbuf;
   ap.accept_len = a->accept_len; ap.path = a->path; ap.bonus = a->bonus_token;
   ap.margin_count = a->margin_count; ap.bonus_margin = a->bonus_margin;
   ap.dev_status = dev_status;
-  launch_accept(ap, stream);
+
+  FinalizeParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.part = l.part; fp.part_idx = l.part_idx; fp.n_parts = l.n_parts; fp.logits = l.logits;
+  fp.hidden = a->hidden_states; fp.weight = a->lm_head_weight; fp.is_bf16 = a->dtype == SPEC_DTYPE_BF16;
+  fp.B = B; fp.N = N; fp.R = l.R; fp.V = V; fp.Hd = Hd;
+  fp.rmax = l.rmax; fp.rlse = l.rlse; fp.rent = l.rent; fp.rgap = l.rgap; fp.rarg = l.rarg; fp.clog = l.clog;
+  fp.hook_max = a->row_max; fp.hook_lse = a->row_lse; fp.hook_ent = a->row_entropy; fp.hook_arg = a->row_argmax;
+  fp.fuse_accept = a->rule != SPEC_RULE_REJECTION;
+  fp.counters = l.counters;
+  fp.acc = ap;
+  launch_row_finalize(fp, stream);
+  if (a->rule == SPEC_RULE_REJECTION) launch_accept(ap, stream);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

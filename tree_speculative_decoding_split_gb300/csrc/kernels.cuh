@@ -25,8 +25,10 @@ struct AttnParams {
   const float* v32;
   const int32_t* prefix_len;
   const int32_t* n_nodes;
-  const uint32_t* anc;
-  const int32_t* bad;
+  const uint32_t* anc;      // fp32 path: ancestor bits from the tree-prep kernel
+  const int32_t* bad;       // fp32 path: per-request verdict of the tree-prep kernel
+  const int32_t* parent;    // [B][N]
+  int32_t* counters;        // bf16 path: [B * Hkv * n_rg] arrival counters, zero on entry
   float* part_o;     // [B*N*Hq][n_split][d]
   float2* part_ml;   // [B*N*Hq][n_split] (running max in log2 units, sum)
   int B, N, Hq, Hkv, G, W, d;
@@ -47,7 +49,6 @@ AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_s
 size_t attention_smem_bytes(int d);
 cudaError_t launch_attention_bf16(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
                                   cudaStream_t stream);
-void launch_attention_merge_bf16(const AttnParams& p, cudaStream_t stream);
 void launch_attention_f32(const AttnParams& p, cudaStream_t stream);
 
 // ---- K2: LM head + row statistics -----------------------------------------------------------
@@ -57,10 +58,13 @@ struct LmParams {
   int n_vt;        // vocabulary tiles of 128
   int n_nc;        // node chunks of BN rows
   int BN;
+  int cpc;         // CTAs per node chunk (grid = cpc * n_nc); records per row of the tc kernel
   float inv_tau;
-  float4* part;    // [n_vt][R] {max, sumexp, sumexp*y, second max}
-  int* part_idx;   // [n_vt][R] argmax
+  float4* part;    // [slot][R] {max, sumexp, sumexp*y, second max}
+  int* part_idx;   // [slot][R] argmax
   float* logits;   // [R][V] raw z, or nullptr
+  int32_t* counters;  // zeroed by the kernel (per-request arrival counters of the finalisation)
+  int n_counters;
   int32_t* dev_status;
 };
 int lmhead_pick_bn(int R);
@@ -68,24 +72,6 @@ size_t lmhead_smem_bytes(int BN);
 cudaError_t launch_lmhead_bf16(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p,
                                int num_sms, cudaStream_t stream);
 void launch_lmhead_f32(const float* H, const float* W, const LmParams& p, cudaStream_t stream);
-
-struct ReduceParams {
-  const float4* part;
-  const int* part_idx;
-  const float* logits;     // [R][V] or nullptr
-  const void* hidden;      // [R][Hd]
-  const void* weight;      // [V][Hd]
-  int is_bf16;
-  const int32_t* tokens;
-  const int32_t* parent;
-  const int32_t* n_nodes;
-  const int32_t* bad;
-  int B, N, R, V, Hd, n_vt;
-  float inv_tau;
-  float* rmax;  float* rlse;  float* rent;  float* rgap;  int32_t* rarg;  float* clog;
-  float* hook_max; float* hook_lse; float* hook_ent; int32_t* hook_arg;
-};
-void launch_row_reduce(const ReduceParams& p, cudaStream_t stream);
 
 // ---- K3: acceptance + longest path ----------------------------------------------------------
 struct AcceptParams {
@@ -95,8 +81,6 @@ struct AcceptParams {
   const int32_t* tokens;
   const int32_t* parent;
   const int32_t* n_nodes;
-  const int32_t* depth;
-  const int32_t* bad;
   const float* rmax; const float* rlse; const float* rent; const float* rgap;
   const int32_t* rarg; const float* clog;
   const float* logits;         // [R][V] (rejection)
@@ -107,6 +91,26 @@ struct AcceptParams {
   int32_t* accept_len; int32_t* path; int32_t* bonus; int32_t* margin_count; int32_t* bonus_margin;
   int32_t* dev_status;
 };
+
+// K2r: per-row statistics from the LM-head records, the child logit of each node, and (greedy /
+// typical) the acceptance of a request by the last of its rows to finish.
+struct FinalizeParams {
+  const float4* part;
+  const int* part_idx;
+  int n_parts;             // records per row
+  const float* logits;     // [R][V] or nullptr
+  const void* hidden;      // [R][Hd]
+  const void* weight;      // [V][Hd]
+  int is_bf16;
+  int B, N, R, V, Hd;
+  float* rmax; float* rlse; float* rent; float* rgap; int32_t* rarg; float* clog;
+  float* hook_max; float* hook_lse; float* hook_ent; int32_t* hook_arg;
+  int fuse_accept;         // greedy / typical: accept in the last CTA of each request
+  int32_t* counters;       // [B], zero on entry
+  AcceptParams acc;
+};
+void launch_row_finalize(const FinalizeParams& p, cudaStream_t stream);
+
 void launch_build_inverse_map(const int32_t* map, int Vd, int V, int32_t* inv, int32_t* map_bad,
                               int32_t* dev_status, cudaStream_t stream);
 void launch_accept(const AcceptParams& p, cudaStream_t stream);

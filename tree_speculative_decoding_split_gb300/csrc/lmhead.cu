@@ -1,5 +1,5 @@
 // K2: LM head z = W h for every tree node, fused with per-row softmax statistics.
-// K2f: fp32 variant (SIMT).  K2r: merge of the per-vocabulary-tile statistics, child logits.
+// K2f: fp32 variant (SIMT).
 //
 // The LM head is a linear layer followed by softmax (tech-tldr "多トークン予測（Medusa・EAGLE）",
 // section "Medusa"; jisaku glossary "Medusa", architecture table: hidden_dim x vocab_size).  It
@@ -12,8 +12,11 @@
 // issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulators in tensor memory, double-buffered
 // across units), warps 2..5 drain the accumulators with tcgen05.ld and reduce every node's
 // column over the 128 vocabulary rows with warp shuffles into {max, sum exp, sum exp*y, second
-// max, argmax} at y = z / tau.  Full fp32 logits go to HBM only when the caller needs them
-// (rejection sampling), written once from the same epilogue.
+// max, argmax} at y = z / tau.  Each CTA owns one chunk of rows and a strided set of vocabulary
+// tiles, and keeps one running record per row in shared memory across its tiles, so it writes
+// one record per row at the end (about 150 records per row in total, merged by the row
+// finalisation kernel).  Full fp32 logits go to HBM only when the caller needs them (rejection
+// sampling), written once from the same epilogue.
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -102,7 +105,7 @@ struct LmCfg {
   static constexpr int kStage = kStageA + kStageB;
   static constexpr int kStages = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
   static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
-  static constexpr int kEpiBytes = 4 * BN * (int)sizeof(float4) + 4 * BN * (int)sizeof(int);
+  static constexpr int kEpiBytes = 5 * BN * (int)sizeof(float4) + 5 * BN * (int)sizeof(int);
   static constexpr int kSmem = 1024 + kStages * kStage + kEpiBytes + 256;
 };
 
@@ -117,9 +120,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
   uint8_t* sB = base + C::kStages * C::kStageA;
-  float4* sEpi = reinterpret_cast<float4*>(base + C::kStages * C::kStage);
-  int* sEpiIdx = reinterpret_cast<int*>(sEpi + 4 * BN);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpiIdx + 4 * BN);
+  float4* sEpi = reinterpret_cast<float4*>(base + C::kStages * C::kStage);  // [4][BN] per-warp records
+  float4* sRun = sEpi + 4 * BN;                                               // [BN] running records
+  int* sEpiIdx = reinterpret_cast<int*>(sRun + BN);
+  int* sRunIdx = sEpiIdx + 4 * BN;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRunIdx + BN);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::kStages;
   uint64_t* tfull = empty + C::kStages;
@@ -132,7 +137,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_kb = p.Hd / kBK;
-  const int total = p.n_vt * p.n_nc;
+  // CTA c owns row chunk nc = c % n_nc and vocabulary tiles slot, slot + cpc, ...
+  const int nc = blockIdx.x % p.n_nc, slot = blockIdx.x / p.n_nc;
+  if (blockIdx.x == 0 && threadIdx.x < 32)
+    for (int i = threadIdx.x; i < p.n_counters; i += 32) p.counters[i] = 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -166,8 +174,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       const uint64_t pol_h = l2_policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const int vt = u / p.n_nc, nc = u % p.n_nc;
+      for (int vt = slot; vt < p.n_vt && ok; vt += p.cpc) {
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
           const int st = it % C::kStages;
           if (!mbar_wait_bounded(&empty[st], ((it / C::kStages) & 1) ^ 1, &s_abort)) {
@@ -192,7 +199,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       uint32_t it = 0;
       int lu = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++lu) {
+      for (int vt = slot; vt < p.n_vt && ok; vt += p.cpc, ++lu) {
         const int a = lu & 1;
         if (!mbar_wait_bounded(&tempty[a], ((lu >> 1) & 1) ^ 1, &s_abort)) {
           ok = false;
@@ -230,8 +237,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int q = warp & 3;
     const int etid = (warp - 2) * 32 + lane;
     int lu = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++lu) {
-      const int vt = u / p.n_nc, nc = u % p.n_nc;
+    for (int j = etid; j < BN; j += 128) {
+      sRun[j] = make_float4(-INFINITY, 0.f, 0.f, -INFINITY);
+      sRunIdx[j] = 0x7fffffff;
+    }
+    for (int vt = slot; vt < p.n_vt; vt += p.cpc, ++lu) {
       const int a = lu & 1;
       // The four epilogue warps agree on the outcome of the wait before going on, so that
       // none of them can be left alone at a named barrier.
@@ -277,21 +287,29 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       if (lane == 0) mbar_arrive(&tempty[a]);
       named_bar_sync(1, 128);
       for (int j = etid; j < BN; j += 128) {
-        const int n = nc * BN + j;
-        if (n < p.R) {
-          RowPart acc = rowpart_empty();
+        RowPart acc;
+        const float4 r0 = sRun[j];
+        acc.m = r0.x; acc.s = r0.y; acc.t = r0.z; acc.y2 = r0.w; acc.idx = sRunIdx[j];
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const float4 f = sEpi[qq * BN + j];
-            RowPart o;
-            o.m = f.x; o.s = f.y; o.t = f.z; o.y2 = f.w; o.idx = sEpiIdx[qq * BN + j];
-            acc = rowpart_merge(acc, o);
-          }
-          p.part[(size_t)vt * p.R + n] = make_float4(acc.m, acc.s, acc.t, acc.y2);
-          p.part_idx[(size_t)vt * p.R + n] = acc.idx;
+        for (int qq = 0; qq < 4; ++qq) {
+          const float4 f = sEpi[qq * BN + j];
+          RowPart o;
+          o.m = f.x; o.s = f.y; o.t = f.z; o.y2 = f.w; o.idx = sEpiIdx[qq * BN + j];
+          acc = rowpart_merge(acc, o);
         }
+        sRun[j] = make_float4(acc.m, acc.s, acc.t, acc.y2);
+        sRunIdx[j] = acc.idx;
       }
       named_bar_sync(1, 128);
+    }
+    if (!s_epi_fail) {
+      for (int j = etid; j < BN; j += 128) {
+        const int n = nc * BN + j;
+        if (n < p.R) {
+          p.part[(size_t)slot * p.R + n] = sRun[j];
+          p.part_idx[(size_t)slot * p.R + n] = sRunIdx[j];
+        }
+      }
     }
   }
 
@@ -344,7 +362,8 @@ __global__ void __launch_bounds__(256) lmhead_f32_kernel(const float* __restrict
     }
 }
 
-// Partial statistics of logits[row][vt*128 .. +128): one warp per (tile, row).
+// Partial statistics of logits[row][vt*128 .. +128): one warp per (tile, row).  Records are laid
+// out [tile][row] like the tensor-core kernel's [slot][row], with one slot per tile.
 __global__ void __launch_bounds__(256) stats_from_logits_kernel(const float* __restrict__ logits, int R, int V,
                                                                 int n_vt, float inv_tau, float4* __restrict__ part,
                                                                 int* __restrict__ part_idx) {
@@ -374,86 +393,6 @@ __global__ void __launch_bounds__(256) stats_from_logits_kernel(const float* __r
   }
 }
 
-// ---- K2r: per-row statistics + child logits -------------------------------------------------
-
-__device__ __forceinline__ RowPart shfl_rowpart(const RowPart& a, int o) {
-  RowPart r;
-  r.m = __shfl_xor_sync(0xffffffffu, a.m, o);
-  r.s = __shfl_xor_sync(0xffffffffu, a.s, o);
-  r.t = __shfl_xor_sync(0xffffffffu, a.t, o);
-  r.y2 = __shfl_xor_sync(0xffffffffu, a.y2, o);
-  r.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
-  return r;
-}
-
-__global__ void __launch_bounds__(256) row_reduce_kernel(const ReduceParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = blockIdx.x * 8 + warp;
-  if (n >= p.R) return;
-  const int b = n / p.N, i = n % p.N;
-  const bool real = !p.bad[b] && i < p.n_nodes[b];
-  RowPart acc = rowpart_empty();
-  if (real) {
-    for (int vt = lane; vt < p.n_vt; vt += 32) {
-      const float4 f = p.part[(size_t)vt * p.R + n];
-      RowPart o;
-      o.m = f.x; o.s = f.y; o.t = f.z; o.y2 = f.w; o.idx = p.part_idx[(size_t)vt * p.R + n];
-      acc = rowpart_merge(acc, o);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc = rowpart_merge(acc, shfl_rowpart(acc, o));
-  }
-  float clog = 0.f;
-  if (real && i > 0) {
-    const int pn = p.parent[n];
-    const int x = p.tokens[n];
-    const size_t prow = (size_t)b * p.N + pn;
-    if (p.logits) {
-      clog = p.logits[prow * p.V + x];
-    } else if (p.is_bf16) {
-      const __nv_bfloat16* hw = static_cast<const __nv_bfloat16*>(p.hidden) + prow * p.Hd;
-      const __nv_bfloat16* ww = static_cast<const __nv_bfloat16*>(p.weight) + (size_t)x * p.Hd;
-      float d = 0.f;
-      for (int k = lane * 8; k < p.Hd; k += 256) {
-        const uint4 hv = *reinterpret_cast<const uint4*>(hw + k);
-        const uint4 wv = *reinterpret_cast<const uint4*>(ww + k);
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hv);
-        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 hf = __bfloat1622float2(h2[e]);
-          const float2 wf = __bfloat1622float2(w2[e]);
-          d = fmaf(hf.x, wf.x, d);
-          d = fmaf(hf.y, wf.y, d);
-        }
-      }
-      clog = warp_sum(d);
-    } else {
-      const float* hw = static_cast<const float*>(p.hidden) + prow * p.Hd;
-      const float* ww = static_cast<const float*>(p.weight) + (size_t)x * p.Hd;
-      float d = 0.f;
-      for (int k = lane; k < p.Hd; k += 32) d = fmaf(hw[k], ww[k], d);
-      clog = warp_sum(d);
-    }
-  }
-  if (lane == 0) {
-    float mx = 0.f, lse = 0.f, ent = 0.f, gap = 0.f;
-    int am = -1;
-    if (real) {
-      mx = acc.m;
-      lse = acc.m + logf(acc.s);
-      ent = lse - acc.t / acc.s;
-      am = acc.idx;
-      gap = (acc.y2 == -INFINITY) ? INFINITY : (acc.m - acc.y2) / p.inv_tau;
-    }
-    p.rmax[n] = mx; p.rlse[n] = lse; p.rent[n] = ent; p.rgap[n] = gap; p.rarg[n] = am; p.clog[n] = clog;
-    if (p.hook_max) p.hook_max[n] = mx;
-    if (p.hook_lse) p.hook_lse[n] = lse;
-    if (p.hook_ent) p.hook_ent[n] = ent;
-    if (p.hook_arg) p.hook_arg[n] = am;
-  }
-}
-
 // ---- host side ------------------------------------------------------------------------------
 
 int lmhead_pick_bn(int R) {
@@ -478,9 +417,7 @@ static cudaError_t launch_lm(const CUtensorMap* tmW, const CUtensorMap* tmH, con
   const int smem = LmCfg<BN>::kSmem;
   cudaError_t err = cudaFuncSetAttribute(lmhead_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const int total = p.n_vt * p.n_nc;
-  const int grid = total < num_sms ? total : num_sms;
-  lmhead_tc_kernel<BN><<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
+  lmhead_tc_kernel<BN><<<p.cpc * p.n_nc, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
   return cudaGetLastError();
 }
 
@@ -502,8 +439,5 @@ void launch_lmhead_f32(const float* H, const float* W, const LmParams& p, cudaSt
                                                                             p.part, p.part_idx);
 }
 
-void launch_row_reduce(const ReduceParams& p, cudaStream_t stream) {
-  row_reduce_kernel<<<(p.R + 7) / 8, 256, 0, stream>>>(p);
-}
 
 }  // namespace spectree
