@@ -43,6 +43,8 @@ def _args():
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", type=int, default=WORKLOAD,
+                   help="gen.configs workload id (the headline metric is quoted on the default)")
     return p.parse_args()
 
 
@@ -188,7 +190,7 @@ def run_native(a, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    case = make_config_case(WORKLOAD, seed=a.seed + rank)
+    case = make_config_case(a.workload, seed=a.seed + rank)
     t = _device_tensors(case, dev)
     stream = torch.cuda.current_stream()
     sp = ctypes.c_void_p(stream.cuda_stream)
@@ -275,12 +277,16 @@ def run_native(a, rank, world, dist):
     host["v_tree"] = [t["v"][b, :, Lp[b]:Lp[b] + n_tree].contiguous().cpu().pin_memory() for b in range(case.B)]
     res_host = {k: torch.empty(outs[k].shape, dtype=torch.int32).pin_memory() for k in ("accept_len", "path", "bonus_token")}
     nl_host = torch.empty(new_len.shape, dtype=torch.int32).pin_memory()
-    h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "hidden", "tokens", "parent", "n_nodes", "prefix_len"))
+    step_inputs = ["q", "hidden", "tokens", "parent", "n_nodes", "prefix_len"]
+    if t["draft"] is not None:  # rejection sampling: the draft distributions arrive with every step
+        host["draft"] = t["draft"].cpu().pin_memory()
+        step_inputs.append("draft")
+    h2d = sum(host[k].numel() * host[k].element_size() for k in step_inputs)
     h2d += sum(x.numel() * x.element_size() for x in host["k_tree"] + host["v_tree"])
     d2h = sum(x.numel() * 4 for x in res_host.values()) + nl_host.numel() * 4
 
     def e2e_step():
-        for k in ("q", "hidden", "tokens", "parent", "n_nodes", "prefix_len"):
+        for k in step_inputs:
             t[k].copy_(host[k], non_blocking=True)
         for b in range(case.B):
             t["k"][b, :, Lp[b]:Lp[b] + n_tree].copy_(host["k_tree"][b], non_blocking=True)
@@ -319,6 +325,8 @@ def run_native(a, rank, world, dist):
     lm_avg = statistics.fmean(lm_ms)
     attn_avg = statistics.fmean(attn_ms)
     lm_achieved = w["lm_kernel_bytes"] / (lm_avg * 1e-3) / 1e9
+    lm_tflops = w["lm_flops"] / (lm_avg * 1e-3) / 1e12
+    lm_tc_bound = w["lm_flops"] / (tc * 1e12) > w["lm_kernel_bytes"] / (hbm * 1e9)
     traffic = _traffic_from_profile(os.path.join(ROOT, "tree_speculative_decoding_split_gb300", "csrc", "lmhead.cu"))
     step_bytes = w["kv_bytes"] + w["qo_bytes"] + w["w_bytes"] + w["h_bytes"] + w["logits_bytes"]
     t_hbm = step_bytes / (hbm * 1e9)
@@ -328,25 +336,33 @@ def run_native(a, rank, world, dist):
         "metric": METRIC, "value": world * w["nodes"] / (ms * 1e-3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, a.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": case.name, "batch": case.B, "prefix_len": int(case.prefix_len[0]),
+        "config": {"workload": case.name, "batch": case.B, "prefix_len": [int(x) for x in case.prefix_len][:8],
                    "tree_nodes": int(case.n_nodes[0]), "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d,
                    "hidden": case.Hd, "vocab": case.V, "rule": case.rule, "eps": case.eps, "delta": case.delta,
                    "parallelism": f"replicas x{world}", "l2": "flushed before every step (256 MB write, then read)"},
         "e2e": {"value": world * w["nodes"] / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": K * _launches_per_step(case),
-        "roofline": {"kernel": "lmhead_tc_kernel (LM head GEMM + row statistics)", "bound": "hbm",
-                     "achieved": lm_achieved, "peak": hbm, "unit": "GB/s", "frac": lm_achieved / hbm,
-                     "traffic": traffic, "algorithmic_bytes": w["lm_kernel_bytes"], "ms": lm_avg,
-                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "roofline": ({"kernel": "lmhead_tc_kernel (LM head GEMM + row statistics)", "bound": "tensor",
+                      "achieved": lm_tflops, "peak": tc, "unit": "TFLOP/s", "frac": lm_tflops / tc,
+                      "traffic": traffic, "algorithmic_flops": w["lm_flops"], "ms": lm_avg,
+                      "peak_source": f"{peak_kind} bf16_tflops (burst)"} if lm_tc_bound else
+                     {"kernel": "lmhead_tc_kernel (LM head GEMM + row statistics)", "bound": "hbm",
+                      "achieved": lm_achieved, "peak": hbm, "unit": "GB/s", "frac": lm_achieved / hbm,
+                      "traffic": traffic, "algorithmic_bytes": w["lm_kernel_bytes"], "ms": lm_avg,
+                      "peak_source": f"{peak_kind} hbm_gbs"}),
         "kernels": {"tree_attention_splitkv_ms": attn_avg, "lmhead_ms": lm_avg,
-                    "attention_achieved_gbs": w["attn_kernel_bytes"] / (attn_avg * 1e-3) / 1e9},
+                    "attention_achieved_gbs": w["attn_kernel_bytes"] / (attn_avg * 1e-3) / 1e9,
+                    "attention_achieved_tflops": w["attn_flops"] / (attn_avg * 1e-3) / 1e12,
+                    "attention_roofline_frac": max(w["attn_kernel_bytes"] / (hbm * 1e9),
+                                                   w["attn_flops"] / (tc * 1e12)) / (attn_avg * 1e-3),
+                    "lmhead_achieved_tflops": lm_tflops},
         "roofline_step": {"combined_s": t_ns, "frac_combined": t_ns / (ms * 1e-3),
                           "full_s": max(t_hbm, t_tc), "frac_full": max(t_hbm, t_tc) / (ms * 1e-3),
                           "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 sustained {tc_sus} TFLOP/s"},
         "clocks": clk,
     }
-    if world == 1 and not a.no_cpu_baseline:
+    if world == 1 and not a.no_cpu_baseline and a.workload == WORKLOAD:
         line["cpu_baseline"] = _cpu_baseline(case)
     return line
 
@@ -385,7 +401,7 @@ def _cpu_baseline(case, budget_s=20.0):
 
 def run_reference(a):
     from gen import make_config_case
-    case = make_config_case(WORKLOAD, seed=a.seed)
+    case = make_config_case(a.workload, seed=a.seed)
     x = _oracle_inputs(case)
     for _ in range(a.warmup if a.warmup < 3 else 1):
         _oracle_step(case, x)
@@ -400,7 +416,7 @@ def run_reference(a):
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": a.gpus, "steps": len(times),
             "warmup": a.warmup, "ms_per_step": s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": case.name, "batch": case.B, "prefix_len": int(case.prefix_len[0]),
+            "config": {"workload": case.name, "batch": case.B, "prefix_len": [int(x) for x in case.prefix_len][:8],
                        "tree_nodes": nodes, "rule": case.rule},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": _threads_used(), "kind": "oracle",
                              "sample": f"{len(times)} full steps of the workload (capped at 20 timed steps)"},

@@ -94,7 +94,7 @@ spec_status check_attn(const spec_attn_args* a) {
 }
 
 struct AttnLayout {
-  int32_t* depth; uint32_t* anc; int32_t* bad; float* part_o; float2* part_ml; int32_t* counters;
+  int32_t* depth; uint32_t* anc; int32_t* bad; float* part_o; float2* part_ml;
   AttnPlan plan;
   size_t bytes;
 };
@@ -110,12 +110,10 @@ AttnLayout layout_attn(const spec_attn_args* a, void* ws) {
   l.bad = c.take<int32_t>(B);
   l.part_o = nullptr;
   l.part_ml = nullptr;
-  l.counters = nullptr;
   if (a->dtype == SPEC_DTYPE_BF16) {
     const size_t rows = (size_t)B * N * a->num_q_heads;
     l.part_o = c.take<float>(rows * l.plan.n_split * a->head_dim);
     l.part_ml = c.take<float2>(rows * l.plan.n_split);
-    l.counters = c.take<int32_t>((size_t)B * a->num_kv_heads * l.plan.n_rg);
   }
   l.bytes = c.off;
   return l;
@@ -154,7 +152,7 @@ struct VerifyLayout {
   float4* part; int* part_idx;
   float *rmax, *rlse, *rent, *rgap, *clog; int32_t* rarg;
   float* logits; float* rbuf; int32_t* inv; int32_t* map_bad; int32_t* counters;
-  int R, n_vt, BN, n_nc, cpc, n_parts;
+  int R, n_vt, BN, BNV, n_nc, cpc, n_parts;
   size_t bytes;
 };
 
@@ -166,9 +164,13 @@ VerifyLayout layout_verify(const spec_verify_args* a, void* ws) {
   l.BN = lmhead_pick_bn(l.R);
   l.n_nc = (l.R + l.BN - 1) / l.BN;
   const int sms = num_sms_current();
+  // BN == 128: tree rows on the MMA M side, BNV vocabulary entries per tile; else vocabulary
+  // on M in tiles of 128 and BN tree rows on N
+  l.BNV = (l.BN == 128) ? lmhead_rows_bnv(l.n_nc, sms) : 128;
+  const int tiles = (a->vocab + l.BNV - 1) / l.BNV;
   l.cpc = sms / l.n_nc;
   if (l.cpc < 1) l.cpc = 1;
-  if (l.cpc > l.n_vt) l.cpc = l.n_vt;
+  if (l.cpc > tiles) l.cpc = tiles;
   // statistics records per row: one per CTA of the row's chunk (bf16), one per tile (fp32)
   l.n_parts = (a->dtype == SPEC_DTYPE_BF16) ? l.cpc : l.n_vt;
   Carver c(ws);
@@ -241,7 +243,6 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
   p.anc = l.anc;
   p.bad = l.bad;
   p.parent = a->parent;
-  p.counters = l.counters;
   p.part_o = l.part_o;
   p.part_ml = l.part_ml;
   p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.W = (N + 31) / 32; p.d = d;
@@ -267,11 +268,10 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
     if (!make_map_bf16(&tmK, a->k_cache, 3, dims, strides, box) ||
         !make_map_bf16(&tmV, a->v_cache, 3, dims, strides, box))
       return SPEC_ERR_CUDA;
-    const size_t ncnt = (size_t)B * Hkv * l.plan.n_rg;
-    if (cudaMemsetAsync(l.counters, 0, ncnt * sizeof(int32_t), stream) != cudaSuccess) return SPEC_ERR_CUDA;
     record(a->timing_begin, stream);
     if (launch_attention_bf16(&tmK, &tmV, p, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     record(a->timing_end, stream);
+    launch_attention_merge_bf16(p, stream);
   }
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -296,7 +296,7 @@ spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_
 
   LmParams lp;
   std::memset(&lp, 0, sizeof(lp));
-  lp.R = l.R; lp.V = V; lp.Hd = Hd; lp.n_vt = l.n_vt; lp.n_nc = l.n_nc; lp.BN = l.BN; lp.cpc = l.cpc;
+  lp.R = l.R; lp.V = V; lp.Hd = Hd; lp.n_vt = l.n_vt; lp.n_nc = l.n_nc; lp.BN = l.BN; lp.BNV = l.BNV; lp.cpc = l.cpc;
   lp.inv_tau = inv_tau;
   lp.part = l.part;
   lp.part_idx = l.part_idx;
@@ -309,7 +309,7 @@ spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_
     const cuuint64_t dW[2] = {(cuuint64_t)Hd, (cuuint64_t)V};
     const cuuint64_t dH[2] = {(cuuint64_t)Hd, (cuuint64_t)l.R};
     const cuuint64_t str[1] = {(cuuint64_t)Hd * 2};
-    const cuuint32_t bW[2] = {64, 128};
+    const cuuint32_t bW[2] = {64, (cuuint32_t)l.BNV};
     const cuuint32_t bH[2] = {64, (cuuint32_t)l.BN};
     if (!make_map_bf16(&tmW, a->lm_head_weight, 2, dW, str, bW) ||
         !make_map_bf16(&tmH, a->hidden_states, 2, dH, str, bH))

@@ -1,4 +1,4 @@
-// K1: split-KV tree attention (with the merge of its splits), K1f: fp32 exact variant.
+// K1: split-KV tree attention, K1m: merge of the splits, K1f: fp32 exact variant.
 //
 // Parallel verification scores every candidate in one forward pass over the KV cache (qiita
 // "EAGLE-3とMedusaで実装するSpeculative Decoding実践ガイド", section "並列検証"); each tree node
@@ -14,9 +14,8 @@
 // ragged end; the last split covers the tree slots [L_b, L_b + n_b) and applies the ancestor
 // mask from a bit matrix (one 32-bit word per 32 nodes) that the CTA builds in shared memory by
 // pointer jumping over the parent array.  Every CTA validates the tree itself.  Each split
-// writes a normalised partial (o, running max, sum) and arrives on its row group's counter;
-// the last CTA to arrive (nothing waits) merges the splits per row with warp shuffles and
-// writes O and the natural-log LSE.
+// writes a normalised partial (o, running max, sum); the merge kernel combines the splits per
+// row with warp shuffles and writes O and the natural-log LSE.
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -65,52 +64,6 @@ __device__ __forceinline__ uint32_t sw128(int r, int ch, int rows) {
 
 }  // namespace
 
-// Merge of the splits of one row group by the last CTA to arrive: one warp per row, lane s holds
-// split s; other CTAs' partials are read through L2.
-template <int D>
-__device__ void merge_group(const AttnParams& p, int b, int g, int row0, int rows_total, int n, bool zero) {
-  constexpr int EPL = D / 32;  // elements per lane, contiguous
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < kRows; r += kThreads / 32) {
-    const int row = row0 + r;
-    if (row >= rows_total) break;
-    const int i = row / p.G, h = g * p.G + row % p.G;
-    const size_t orow = ((size_t)b * p.N + i) * p.Hq + h;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D + lane * EPL;
-    if (zero || i >= n) {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) out[e] = __float2bfloat16(0.f);
-      if (p.lse && lane == 0) p.lse[orow] = 0.f;
-      continue;
-    }
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (lane < p.n_split) ml = __ldcg(p.part_ml + orow * p.n_split + lane);
-    const float M = warp_max(ml.y > 0.f ? ml.x : -INFINITY);
-    const float w = (ml.y > 0.f) ? ml.y * exp2f(ml.x - M) : 0.f;
-    const float wsum = warp_sum(w);
-    float acc[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-    for (int s = 0; s < p.n_split; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w, s);
-      if (ws > 0.f) {
-        const float* src = p.part_o + (orow * p.n_split + s) * D + lane * EPL;
-        if constexpr (EPL == 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-          acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-          acc[0] += ws * v.x; acc[1] += ws * v.y;
-        }
-      }
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) out[e] = __float2bfloat16(acc[e] * inv);
-    if (p.lse && lane == 0) p.lse[orow] = (M + log2f(wsum)) * 0.69314718055994531f;
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_splitkv_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -126,7 +79,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sAnc + kRows * kAncWords);
   __shared__ int s_abort;
   __shared__ int s_issued;
-  __shared__ int s_last;
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_jmp[kMaxNodes];
   __shared__ uint32_t s_nanc[kMaxNodes][kAncWords];  // ancestor-or-self words of every node
@@ -398,19 +350,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ---- arrival; the last CTA of this (request, KV head, row group) merges all splits ----
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const int cidx = bg * p.n_rg + rg;
-    s_last = atomicAdd(&p.counters[cidx], 1) == p.n_split - 1;
-    if (s_last) p.counters[cidx] = 0;
+  // the first CTA of each request reports a bad tree; the merge kernel zeroes its outputs
+  if (err && tid == 0 && blockIdx.x == 0 && split == 0 && g == 0) set_status(p.dev_status, err);
+}
+
+// K1m: merge of the splits, one warp per output row (b, i, h); lane s holds split s.  Requests
+// with an invalid tree (checked again here: a handful of loads per warp) get zero outputs.
+template <int D>
+__global__ void __launch_bounds__(256) attn_merge_bf16_kernel(const AttnParams p) {
+  constexpr int EPL = D / 32;  // elements per lane, contiguous
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t orow = (size_t)blockIdx.x * 8 + warp;
+  const size_t total = (size_t)p.B * p.N * p.Hq;
+  if (orow >= total) return;
+  const int b = (int)(orow / ((size_t)p.N * p.Hq));
+  const int i = (int)((orow / p.Hq) % p.N);
+  const int n = p.n_nodes[b];
+  const long long L = p.prefix_len[b];
+  bool zero = n < 1 || n > p.N || i >= n || L < 0 || L + n > p.L_cap;
+  if (!zero) {
+    bool bad = false;
+    for (int c = lane; c < n; c += 32) {
+      const int par = p.parent[(size_t)b * p.N + c];
+      bad |= (c == 0) ? par != -1 : (par < 0 || par >= c);
+    }
+    zero = __any_sync(0xffffffffu, bad);
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (err && tid == 0) set_status(p.dev_status, err);
-  merge_group<D>(p, b, g, row0, rows_total, n, err != 0);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D + lane * EPL;
+  if (zero) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[e] = __float2bfloat16(0.f);
+    if (p.lse && lane == 0) p.lse[orow] = 0.f;
+    return;
+  }
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < p.n_split) ml = p.part_ml[orow * p.n_split + lane];
+  const float M = warp_max(ml.y > 0.f ? ml.x : -INFINITY);
+  const float w = (ml.y > 0.f) ? ml.y * exp2f(ml.x - M) : 0.f;
+  const float wsum = warp_sum(w);
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  for (int s = 0; s < p.n_split; ++s) {
+    const float ws = __shfl_sync(0xffffffffu, w, s);
+    if (ws > 0.f) {
+      const float* src = p.part_o + (orow * p.n_split + s) * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += ws * v.x; acc[1] += ws * v.y;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) out[e] = __float2bfloat16(acc[e] * inv);
+  if (p.lse && lane == 0) p.lse[orow] = (M + log2f(wsum)) * 0.69314718055994531f;
 }
 
 // K1f: fp32 tree attention, one warp per output row; keys visited one by one (prefix, then the
@@ -514,6 +511,15 @@ cudaError_t launch_attention_bf16(const CUtensorMap* tmK, const CUtensorMap* tmV
     attn_splitkv_bf16_kernel<64><<<grid, kThreads, smem, stream>>>(*tmK, *tmV, p);
   }
   return cudaGetLastError();
+}
+
+void launch_attention_merge_bf16(const AttnParams& p, cudaStream_t stream) {
+  const size_t total = (size_t)p.B * p.N * p.Hq;
+  const unsigned blocks = (unsigned)((total + 7) / 8);
+  if (p.d == 128)
+    attn_merge_bf16_kernel<128><<<blocks, 256, 0, stream>>>(p);
+  else
+    attn_merge_bf16_kernel<64><<<blocks, 256, 0, stream>>>(p);
 }
 
 void launch_attention_f32(const AttnParams& p, cudaStream_t stream) {

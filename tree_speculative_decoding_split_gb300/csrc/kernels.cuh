@@ -28,7 +28,6 @@ struct AttnParams {
   const uint32_t* anc;      // fp32 path: ancestor bits from the tree-prep kernel
   const int32_t* bad;       // fp32 path: per-request verdict of the tree-prep kernel
   const int32_t* parent;    // [B][N]
-  int32_t* counters;        // bf16 path: [B * Hkv * n_rg] arrival counters, zero on entry
   float* part_o;     // [B*N*Hq][n_split][d]
   float2* part_ml;   // [B*N*Hq][n_split] (running max in log2 units, sum)
   int B, N, Hq, Hkv, G, W, d;
@@ -49,6 +48,7 @@ AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_s
 size_t attention_smem_bytes(int d);
 cudaError_t launch_attention_bf16(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
                                   cudaStream_t stream);
+void launch_attention_merge_bf16(const AttnParams& p, cudaStream_t stream);
 void launch_attention_f32(const AttnParams& p, cudaStream_t stream);
 
 // ---- K2: LM head + row statistics -----------------------------------------------------------
@@ -59,6 +59,7 @@ struct LmParams {
   int n_nc;        // node chunks of BN rows
   int BN;
   int cpc;         // CTAs per node chunk (grid = cpc * n_nc); records per row of the tc kernel
+  int BNV;         // rows-on-M kernel (BN == 128): vocabulary entries per tile (128 or 256)
   float inv_tau;
   float4* part;    // [slot][R] {max, sumexp, sumexp*y, second max}
   int* part_idx;   // [slot][R] argmax
@@ -68,6 +69,7 @@ struct LmParams {
   int32_t* dev_status;
 };
 int lmhead_pick_bn(int R);
+int lmhead_rows_bnv(int n_nc, int num_sms);
 size_t lmhead_smem_bytes(int BN);
 cudaError_t launch_lmhead_bf16(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p,
                                int num_sms, cudaStream_t stream);

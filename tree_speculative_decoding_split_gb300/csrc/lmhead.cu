@@ -324,6 +324,225 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
+// ---- rows-on-M orientation (128 tree rows per MMA tile, vocabulary on N) --------------------
+// Used when there are at least 128 tree rows: the epilogue thread that owns TMEM lane r owns
+// tree row r of the chunk, so the softmax statistics of a row are a running, per-thread
+// reduction over the vocabulary columns (no cross-lane shuffles), carried in registers across
+// all vocabulary tiles of the CTA.  CTA c owns row chunk rc = c % n_nc and vocabulary tiles
+// slot, slot + cpc, ... of BNV entries each.
+
+template <int BNV>
+struct LmRowsCfg {
+  static constexpr int kStageA = kBM * kBK * 2;   // 128 tree rows x 64 hidden
+  static constexpr int kStageB = BNV * kBK * 2;   // BNV vocabulary rows x 64 hidden
+  static constexpr int kStage = kStageA + kStageB;
+  static constexpr int kStages = (BNV >= 256) ? 4 : 6;
+  static constexpr uint32_t kTmemCols = 2 * BNV;  // double-buffered accumulators
+  static constexpr int kSmem = 1024 + kStages * kStage + 256;
+};
+
+template <int BNV>
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lmhead_tc_rows_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                          const LmParams p) {
+  using C = LmRowsCfg<BNV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + C::kStages * C::kStageA;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kStages * C::kStage);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drained = tempty + 2;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ uint32_t s_issued, s_consumed;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_kb = p.Hd / kBK;
+  const int rc = blockIdx.x % p.n_nc, slot = blockIdx.x / p.n_nc;
+  const int n_vt = (p.V + BNV - 1) / BNV;
+  if (blockIdx.x == 0 && threadIdx.x < 32)
+    for (int i = threadIdx.x; i < p.n_counters; i += 32) p.counters[i] = 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drained, 1);
+    s_abort = 0;
+    s_issued = 0;
+    s_consumed = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer: tree rows (re-read from L2 per tile), vocabulary rows of W ----
+      const uint64_t pol_h = l2_policy_evict_last();
+      const uint64_t pol_w = (p.n_nc > 1) ? l2_policy_evict_last() : l2_policy_evict_first();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int vt = slot; vt < n_vt && ok; vt += p.cpc) {
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % C::kStages;
+          if (!mbar_wait_bounded(&empty[st], ((it / C::kStages) & 1) ^ 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], C::kStage);
+          tma_load_2d(sA + st * C::kStageA, &tmH, &full[st], kb * kBK, rc * kBM, pol_h);
+          tma_load_2d(sB + st * C::kStageB, &tmW, &full[st], kb * kBK, vt * BNV, pol_w);
+          s_issued = it + 1;
+        }
+      }
+      if (!ok) {
+        s_abort = 1;
+        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      constexpr uint32_t idesc = idesc_bf16(kBM, BNV);
+      uint32_t it = 0;
+      int lu = 0;
+      bool ok = true;
+      for (int vt = slot; vt < n_vt && ok; vt += p.cpc, ++lu) {
+        const int a = lu & 1;
+        if (!mbar_wait_bounded(&tempty[a], ((lu >> 1) & 1) ^ 1, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(a * BNV);
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % C::kStages;
+          if (!mbar_wait_bounded(&full[st], (it / C::kStages) & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_sw128(smem_u32(sA + st * C::kStageA));
+          const uint64_t bd = sdesc_sw128(smem_u32(sB + st * C::kStageB));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+          umma_commit(&empty[st]);
+          s_consumed = it + 1;
+        }
+        if (ok) umma_commit(&tfull[a]);
+      }
+      if (!ok) {
+        s_abort = 1;
+        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+      }
+      umma_commit(drained);
+      mbar_wait_bounded(drained, 0, nullptr);
+    }
+  } else {
+    // ---- epilogue: warps 2..5; thread (q, lane) owns tree row rc*128 + 32q + lane ----
+    const int q = warp & 3;
+    const int n = rc * kBM + q * 32 + lane;
+    const bool nvalid = n < p.R;
+    constexpr float kLog2e = 1.4426950408889634f;
+    float m1 = -INFINITY, m2 = -INFINITY, s = 0.f, t = 0.f;
+    int i1 = 0x7fffffff;
+    bool failed = false;
+    int lu = 0;
+    for (int vt = slot; vt < n_vt; vt += p.cpc, ++lu) {
+      const int a = lu & 1;
+      // every lane waits on the barrier itself; a timeout is the same verdict in all four warps
+      if (!mbar_wait_bounded(&tfull[a], (lu >> 1) & 1, &s_abort)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < BNV / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BNV + cc * 32), r);
+        tmem_ld_wait();
+        const int vbase = vt * BNV + cc * 32;
+        if (p.logits && nvalid) {
+          float* dst = p.logits + (size_t)n * p.V + vbase;
+          if (vbase + 32 <= p.V && ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(dst + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+          } else {
+            for (int j = 0; j < 32; ++j)
+              if (vbase + j < p.V) dst[j] = __uint_as_float(r[j]);
+          }
+        }
+        const float m_prev = m1;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float y = (vbase + j < p.V) ? __uint_as_float(r[j]) * p.inv_tau : -INFINITY;
+          if (y > m1) {
+            m2 = m1;
+            m1 = y;
+            i1 = vbase + j;
+          } else if (y > m2) {
+            m2 = y;
+          }
+        }
+        if (m1 > -INFINITY) {
+          const float scale = (m_prev > -INFINITY) ? exp2f((m_prev - m1) * kLog2e) : 0.f;
+          s *= scale;
+          t *= scale;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (vbase + j < p.V) {  // entries past the vocabulary contribute nothing (0 * -inf is NaN)
+              const float y = __uint_as_float(r[j]) * p.inv_tau;
+              const float e = exp2f((y - m1) * kLog2e);
+              s += e;
+              t = fmaf(e, y, t);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+    }
+    if (failed) {
+      if (lane == 0) {
+        s_abort = 1;
+        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+      }
+    } else if (nvalid) {
+      p.part[(size_t)slot * p.R + n] = make_float4(m1, s, t, m2);
+      p.part_idx[(size_t)slot * p.R + n] = i1;
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort) {
+    for (uint32_t it = s_consumed; it < s_issued; ++it)
+      mbar_wait_bounded(&full[it % C::kStages], (it / C::kStages) & 1, nullptr);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
 // ---- fp32 path ------------------------------------------------------------------------------
 
 // logits[R][V] = H[R][Hd] . W[V][Hd]^T, 64 x 64 output tile per CTA, 4 x 4 per thread.
@@ -398,17 +617,20 @@ __global__ void __launch_bounds__(256) stats_from_logits_kernel(const float* __r
 int lmhead_pick_bn(int R) {
   if (R <= 32) return 32;
   if (R <= 64) return 64;
-  if (R <= 128) return 128;
-  return 256;
+  return 128;  // 128 tree rows per chunk: the rows-on-M kernel
 }
 
 size_t lmhead_smem_bytes(int BN) {
   switch (BN) {
     case 32: return LmCfg<32>::kSmem;
     case 64: return LmCfg<64>::kSmem;
-    case 128: return LmCfg<128>::kSmem;
-    default: return LmCfg<256>::kSmem;
+    default: return LmRowsCfg<256>::kSmem;
   }
+}
+
+int lmhead_rows_bnv(int n_nc, int num_sms) {
+  // vocabulary entries per tile: 256 once every SM has a row chunk's worth of tiles to stream
+  return (n_nc >= 4 || num_sms <= 0) ? 256 : 128;
 }
 
 template <int BN>
@@ -421,13 +643,24 @@ static cudaError_t launch_lm(const CUtensorMap* tmW, const CUtensorMap* tmH, con
   return cudaGetLastError();
 }
 
+template <int BNV>
+static cudaError_t launch_lm_rows(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p,
+                                  cudaStream_t stream) {
+  const int smem = LmRowsCfg<BNV>::kSmem;
+  cudaError_t err =
+      cudaFuncSetAttribute(lmhead_tc_rows_kernel<BNV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  lmhead_tc_rows_kernel<BNV><<<p.cpc * p.n_nc, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lmhead_bf16(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p, int num_sms,
                                cudaStream_t stream) {
   switch (p.BN) {
     case 32: return launch_lm<32>(tmW, tmH, p, num_sms, stream);
     case 64: return launch_lm<64>(tmW, tmH, p, num_sms, stream);
-    case 128: return launch_lm<128>(tmW, tmH, p, num_sms, stream);
-    default: return launch_lm<256>(tmW, tmH, p, num_sms, stream);
+    default:
+      return (p.BNV == 256) ? launch_lm_rows<256>(tmW, tmH, p, stream) : launch_lm_rows<128>(tmW, tmH, p, stream);
   }
 }
 
