@@ -269,7 +269,7 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
         !make_map_bf16(&tmV, a->v_cache, 3, dims, strides, box))
       return SPEC_ERR_CUDA;
     record(a->timing_begin, stream);
-    if (launch_attention_bf16(&tmK, &tmV, p, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (launch_attention_tc(&tmK, &tmV, p, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     record(a->timing_end, stream);
     launch_attention_merge_bf16(p, stream);
   }

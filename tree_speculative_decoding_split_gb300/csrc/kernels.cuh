@@ -45,10 +45,10 @@ struct AttnPlan {
   int n_rg, n_prefix, chunk, n_split;
 };
 AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_sms);
-size_t attention_smem_bytes(int d);
-cudaError_t launch_attention_bf16(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
-                                  cudaStream_t stream);
 void launch_attention_merge_bf16(const AttnParams& p, cudaStream_t stream);
+size_t attention_tc_smem_bytes(int d);
+cudaError_t launch_attention_tc(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
+                                cudaStream_t stream);
 void launch_attention_f32(const AttnParams& p, cudaStream_t stream);
 
 // ---- K2: LM head + row statistics -----------------------------------------------------------
