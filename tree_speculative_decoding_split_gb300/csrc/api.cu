@@ -251,6 +251,7 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
   p.chunk = l.plan.chunk;
   p.n_split = l.plan.n_split;
   p.n_rg = l.plan.n_rg;
+  p.groups = l.plan.groups;
   p.scale = a->scale > 0.f ? a->scale : 1.f / std::sqrt((float)d);
   p.scale_log2 = p.scale * 1.4426950408889634f;
   p.dev_status = dev_status;

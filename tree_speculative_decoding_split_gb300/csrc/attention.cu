@@ -16,7 +16,6 @@ namespace spectree {
 namespace {
 
 constexpr int kKT = 64;    // keys per tile of the bf16 kernel (split sizes are multiples of it)
-constexpr int kRows = 128; // rows (node x GQA head) per CTA of the bf16 kernel
 
 }  // namespace
 
@@ -137,7 +136,12 @@ __global__ void __launch_bounds__(128) attn_rows_f32_kernel(const AttnParams p) 
 
 AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_sms) {
   AttnPlan pl;
-  pl.n_rg = (N * G + kRows - 1) / kRows;
+  // Two 128-row groups per CTA (ping-pong) when that still gives every SM work before any key
+  // splitting; small problems keep one group so that there are more, shorter CTAs.
+  const long long units2 = (long long)B * Hkv * ((N * G + attention_tc_rows_per_cta(2) - 1) / attention_tc_rows_per_cta(2));
+  pl.groups = (units2 * 2 >= num_sms) ? 2 : 1;
+  const int rows_cta = attention_tc_rows_per_cta(pl.groups);  // (node, GQA head) rows per bf16 CTA
+  pl.n_rg = (N * G + rows_cta - 1) / rows_cta;
   const long long base = (long long)B * Hkv * pl.n_rg;
   long long want = (4LL * num_sms + base - 1) / base;  // about four CTAs per SM
   if (want < 1) want = 1;

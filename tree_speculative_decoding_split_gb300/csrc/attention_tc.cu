@@ -5,18 +5,21 @@
 // attends only to its ancestors and itself (tech-tldr "多トークン予測（Medusa・EAGLE）", section
 // "ツリー検証"; qiita, section "Tree Attention").
 //
-// One CTA owns (request b, KV head g, key split, group of 128 rows); a row is a (tree node i,
-// GQA head j) pair r = i * G + j, so the 128 rows fill the M = 128 side of every MMA and all query
-// heads sharing KV head g and all tree nodes read each K/V tile once.  Roles (192 threads):
+// One CTA owns (request b, KV head g, key split, NG x 128 rows); a row is a (tree node i, GQA head
+// j) pair r = i * G + j, so every K/V tile is read once for all query heads sharing KV head g and
+// all tree nodes.  With NG = 2 the two 128-row groups (the M of one MMA each) run in ping-pong:
+// while one group's softmax works on its scores, the tensor core computes the other group's P V
+// and next Q K^T; small problems use NG = 1 for more, shorter CTAs.  Roles (64 + 128 NG threads):
 //   warp 0     TMA producer: 64-key K and V tiles (128-byte swizzle) into a 3-stage ring;
-//   warp 1     MMA issuer: S = Q K^T into one of two TMEM buffers, then O += P V into a TMEM
-//              accumulator once the softmax has written P; V is consumed MN-major, so no
-//              transpose is needed;
-//   warps 2-5  softmax: the thread owning TMEM lane r owns row r -- it loads its S row, applies
-//              the tree mask (ancestor bits, tail split only) and the online softmax in the log2
-//              domain, and writes the bf16 P row to shared memory.  O is rescaled in TMEM only
-//              when a row's running maximum grows by more than 2^8 (exact: P and the running sum
-//              use the same stale maximum).
+//   warp 1     MMA issuer: per group, S = Q K^T into the group's TMEM score buffer as soon as
+//              the softmax has read the previous S, and O += P V into the group's TMEM
+//              accumulator as soon as P is written; V is consumed MN-major straight from its TMA
+//              tiles;
+//   warps 2-   softmax, four warps per group: the thread owning TMEM lane r of a group owns that
+//              row -- it loads its S row, applies the tree mask (ancestor bits, tail split only)
+//              and the online softmax in the log2 domain, and writes the bf16 P row to shared
+//              memory.  O is rescaled in TMEM only when a row's running maximum grows by more than
+//              2^8 (exact: P and the running sum use the same stale maximum).
 // Every CTA validates the tree; the tail CTA builds the ancestor bits by pointer jumping.  Each
 // split writes a normalised partial (o, running max, sum), merged by the merge kernel.
 
@@ -28,20 +31,31 @@ namespace spectree {
 
 namespace {
 
-constexpr int kKT = 64;         // keys per tile (MMA N of S, K of P V)
-constexpr int kStages = 3;      // K/V ring depth
-constexpr int kRows = 128;      // rows per CTA (MMA M)
-constexpr int kTcThreads = 192;
+constexpr int kKT = 64;          // keys per tile (MMA N of S, K of P V)
+constexpr int kStages = 3;       // K/V ring depth
+constexpr int kGR = 128;         // rows per group (MMA M)
 constexpr float kRescaleLog2 = 8.f;
 
-template <int D>
+template <int D, int NG>
 struct AttnTcCfg {
-  static constexpr int kQ = kRows * D * 2;      // Q tile bytes
+  static constexpr int kGroups = NG;            // 128-row groups per CTA
+  static constexpr int kRowsCta = kGR * NG;
+  static constexpr int kThreads = 64 + 128 * NG;  // producer warp, MMA warp, 4 softmax warps per group
+  static constexpr int kQ = kGR * D * 2;        // Q bytes per group
   static constexpr int kTile = kKT * D * 2;     // K (or V) tile bytes
-  static constexpr int kP = kRows * kKT * 2;    // P tile bytes
-  static constexpr int kSmem = 1024 + kQ + 2 * kStages * kTile + 2 * kP + kRows * kAncWords * 4 + 32 * 8;
-  static constexpr uint32_t kTmemCols = (2 * kKT + D <= 256) ? 256 : 512;  // S x 2 + O
+  static constexpr int kP = kGR * kKT * 2;      // P bytes per group
+  static constexpr int kSmem =
+      1024 + NG * kQ + 2 * kStages * kTile + NG * kP + kRowsCta * kAncWords * 4 + 32 * 8;
+  static constexpr uint32_t kTmemCols = (NG * (kKT + D) <= 256) ? 256 : 512;  // S and O per group
 };
+
+// 2^x with the special-function unit's approximation (PTX ex2.approx.ftz: about 2 ulp; results
+// below the normal range flush to 0).  P is rounded to bf16 right after, so this is ample.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t sw128_off(int r, int ch, int rows) {
   return (uint32_t)((ch >> 3) * rows * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
@@ -58,27 +72,29 @@ __device__ __forceinline__ void tma_load_3d_plain(void* dst, const CUtensorMap* 
 
 }  // namespace
 
-template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int D, int NG>
+__global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const AttnParams p) {
-  using C = AttnTcCfg<D>;
+  using C = AttnTcCfg<D, NG>;
+  constexpr int kGroups = C::kGroups;
+  constexpr int kRowsCta = C::kRowsCta;
+  constexpr int kTcThreads = C::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;
-  uint8_t* sK = sQ + C::kQ;
+  uint8_t* sQ = base;                                  // [group][128 rows][D], K-major swizzled
+  uint8_t* sK = sQ + kGroups * C::kQ;
   uint8_t* sV = sK + kStages * C::kTile;
-  uint8_t* sP = sV + kStages * C::kTile;
-  uint32_t* sAnc = reinterpret_cast<uint32_t*>(sP + 2 * C::kP);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sAnc + kRows * kAncWords);
+  uint8_t* sP = sV + kStages * C::kTile;              // [group][128 rows][64 keys]
+  uint32_t* sAnc = reinterpret_cast<uint32_t*>(sP + kGroups * C::kP);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sAnc + kRowsCta * kAncWords);
   uint64_t* full = bars;                 // [3] K/V landed
-  uint64_t* empty = full + kStages;      // [3] K/V consumed
-  uint64_t* sfull = empty + kStages;     // [2] S computed
-  uint64_t* sfree = sfull + 2;           // [2] S read by the softmax
-  uint64_t* pfull = sfree + 2;           // [2] P written
-  uint64_t* pfree = pfull + 2;           // [2] P consumed
-  uint64_t* ofull = pfree + 2;           // O updated (one phase per tile)
-  uint64_t* drained = ofull + 1;
+  uint64_t* empty = full + kStages;      // [3] K/V consumed by both groups
+  uint64_t* sfull = empty + kStages;     // [group] S computed
+  uint64_t* sfree = sfull + kGroups;     // [group] S read by the softmax
+  uint64_t* pfull = sfree + kGroups;     // [group] P written
+  uint64_t* ofull = pfull + kGroups;     // [group] P V done (O updated, P buffer free)
+  uint64_t* drained = ofull + kGroups;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_issued, s_consumed;
@@ -93,7 +109,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n = p.n_nodes[b];
   const bool tail = (split == p.n_prefix);
   const int rows_total = p.N * p.G;
-  const int row0 = rg * kRows;
+  const int row0 = rg * kRowsCta;
 
   // ---- tree checks, done by every CTA of the request (same verdict everywhere) ----
   int bad_tree = (n < 1 || n > p.N) ? 1 : 0, bad_cap = 0;
@@ -122,8 +138,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const int T = ke > kb ? (int)((ke - kb + kKT - 1) / kKT) : 0;
   if (T == 0) {  // no keys here: the merge skips this split
-    if (tid < kRows && row0 + tid < rows_total) {
-      const int row = row0 + tid, i = row / p.G, h = g * p.G + row % p.G;
+    for (int rr = tid; rr < kRowsCta; rr += kTcThreads) {
+      if (row0 + rr >= rows_total) break;
+      const int row = row0 + rr, i = row / p.G, h = g * p.G + row % p.G;
       const size_t orow = ((size_t)b * p.N + i) * p.Hq + h;
       p.part_ml[orow * p.n_split + split] = make_float2(-INFINITY, 0.f);
     }
@@ -140,7 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       s_jmp[c] = (c == 0) ? -1 : s_par[c];
     }
     __syncthreads();
-    for (int round = 0; round < 8; ++round) {
+    for (int round = 0; round < 8; ++round) {  // 2^8 >= 255 levels; up to two nodes per thread
       int jj[2] = {-1, -1}, nj[2] = {-1, -1};
       uint32_t up[2][kAncWords];
 #pragma unroll
@@ -167,7 +184,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       __syncthreads();
     }
-    for (int c = tid; c < kRows * kAncWords; c += kTcThreads) {
+    for (int c = tid; c < kRowsCta * kAncWords; c += kTcThreads) {
       const int r = c / kAncWords, w = c % kAncWords, row = row0 + r;
       uint32_t word = 0;
       if (row < rows_total) {
@@ -181,27 +198,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---- Q rows -> shared memory in the K-major 128-byte-swizzle layout of the MMA A operand ----
   constexpr int NCH = D / 8;
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-  for (int c = tid; c < kRows * NCH; c += kTcThreads) {
-    const int r = c / NCH, ch = c % NCH, row = row0 + r;
+  for (int c = tid; c < kRowsCta * NCH; c += kTcThreads) {
+    const int rr = c / NCH, ch = c % NCH, row = row0 + rr;
     uint4 val = make_uint4(0, 0, 0, 0);
     if (row < rows_total) {
       const int i = row / p.G, j = row % p.G;
       val = *reinterpret_cast<const uint4*>(q + (((size_t)b * p.N + i) * p.Hq + g * p.G + j) * D + ch * 8);
     }
-    *reinterpret_cast<uint4*>(sQ + sw128_off(r, ch, kRows)) = val;
+    const int grp = rr / kGR;
+    *reinterpret_cast<uint4*>(sQ + grp * C::kQ + sw128_off(rr % kGR, ch, kGR)) = val;
   }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kGroups; ++a) {
       mbar_init(&sfull[a], 1);
       mbar_init(&sfree[a], 4);
       mbar_init(&pfull[a], 4);
-      mbar_init(&pfree[a], 1);
+      mbar_init(&ofull[a], 1);
     }
-    mbar_init(ofull, 1);
     mbar_init(drained, 1);
     s_abort = 0;
     s_issued = 0;
@@ -217,7 +234,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t tmem_o = tmem + 2 * kKT;
+  // TMEM columns: S of group a at [a * 64, a * 64 + 64), O of group a at [NG * 64 + a * D, ...)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -245,47 +262,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer ----
-      constexpr uint32_t idS = idesc_bf16_f32(kRows, kKT, 0);
-      constexpr uint32_t idP = idesc_bf16_f32(kRows, D, 1);
+      // ---- MMA issuer: S_A(0) S_B(0), then per tile t: [P V]_A(t) S_A(t+1) [P V]_B(t) S_B(t+1) ----
+      constexpr uint32_t idS = idesc_bf16_f32(kGR, kKT, 0);
+      constexpr uint32_t idP = idesc_bf16_f32(kGR, D, 1);
       bool ok = true;
-      auto issue_s = [&](int t) -> bool {
-        const int st = t % kStages, sb = t & 1;
-        if (!mbar_wait_bounded(&full[st], (t / kStages) & 1, &s_abort)) return false;
-        if (!mbar_wait_bounded(&sfree[sb], ((t >> 1) & 1) ^ 1, &s_abort)) return false;
+      // Issue order: S_a(0) for every group, then per tile t: S_a(t + 1) for every group as soon as
+      // that group's softmax has read S_a(t) (early in its work on tile t, so the next scores are
+      // ready when it finishes), then P V_a(t) for every group as soon as P_a(t) is written.  K/V
+      // stage t is released after the last group's P V(t).  Waits suspend in the barrier.
+      auto issue_s = [&](int a, int t) -> bool {
+        const int st = t % kStages;
+        if (a == 0 && !mbar_wait_bounded(&full[st], (t / kStages) & 1, &s_abort)) return false;
+        if (t > 0 && !mbar_wait_bounded(&sfree[a], (t - 1) & 1, &s_abort)) return false;
         tc_fence_after();
-        const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK + st * C::kTile);
+        const uint32_t qa = smem_u32(sQ + a * C::kQ), ka = smem_u32(sK + st * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 0, 1024);
+          const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * (kGR * 128) + (kk & 3) * 32, 0, 1024);
           const uint64_t bd = sdesc_sw128(ka + (kk >> 2) * (kKT * 128) + (kk & 3) * 32, 0, 1024);
-          umma_bf16(tmem + sb * kKT, ad, bd, idS, kk > 0);
+          umma_bf16(tmem + a * kKT, ad, bd, idS, kk > 0);
         }
-        umma_commit(&sfull[sb]);
+        umma_commit(&sfull[a]);
         return true;
       };
-      ok = issue_s(0);
-      for (int t = 0; t < T && ok; ++t) {
-        if (t + 1 < T && !issue_s(t + 1)) {
-          ok = false;
-          break;
-        }
-        const int pb = t & 1, st = t % kStages;
-        if (!mbar_wait_bounded(&pfull[pb], (t >> 1) & 1, &s_abort)) {
-          ok = false;
-          break;
-        }
+      auto issue_pv = [&](int a, int t) -> bool {
+        if (!mbar_wait_bounded(&pfull[a], t & 1, &s_abort)) return false;
         tc_fence_after();
-        const uint32_t pa = smem_u32(sP + pb * C::kP), va = smem_u32(sV + st * C::kTile);
+        const uint32_t pa = smem_u32(sP + a * C::kP), va = smem_u32(sV + (t % kStages) * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < kKT / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(pa + kk * 32, 0, 1024);
           const uint64_t bd = sdesc_sw128(va + kk * 16 * 128, kKT * 128, 1024);
-          umma_bf16(tmem_o, ad, bd, idP, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16(tmem + kGroups * kKT + a * D, ad, bd, idP, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&empty[st]);
-        umma_commit(&pfree[pb]);
-        umma_commit(ofull);
+        umma_commit(&ofull[a]);
+        return true;
+      };
+#pragma unroll
+      for (int a = 0; a < kGroups; ++a) ok = ok && issue_s(a, 0);
+      for (int t = 0; t < T && ok; ++t) {
+        if (t + 1 < T) {
+#pragma unroll
+          for (int a = 0; a < kGroups; ++a) ok = ok && issue_s(a, t + 1);
+        }
+#pragma unroll
+        for (int a = 0; a < kGroups; ++a) ok = ok && issue_pv(a, t);
+        if (!ok) break;
+        umma_commit(&empty[t % kStages]);  // every group is done with K/V tile t
         s_consumed = t + 1;
       }
       if (!ok) {
@@ -296,35 +319,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait_bounded(drained, 0, nullptr);
     }
   } else {
-    // ---- softmax: warps 2..5, TMEM lane quarter q, row r = 32 q + lane ----
-    const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;
+    // ---- softmax: warps 2..9; group a = (warp - 2) / 4, TMEM lane quarter q4 = warp % 4 ----
+    const int a = (warp - 2) >> 2, q4 = warp & 3;
+    const int rl = q4 * 32 + lane;            // row within the group (TMEM lane)
+    const int rr = a * kGR + rl;              // row within the CTA
+    const int row = row0 + rr;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int row = row0 + r;
+    const uint32_t tS = tmem + a * kKT + lane_off;
+    const uint32_t tO = tmem + kGroups * kKT + a * D + lane_off;
+    uint8_t* prow = sP + a * C::kP;
     float m_run = -INFINITY, l_run = 0.f;
     uint32_t anc[kAncWords];
 #pragma unroll
-    for (int w = 0; w < kAncWords; ++w) anc[w] = tail ? sAnc[r * kAncWords + w] : 0u;
+    for (int w = 0; w < kAncWords; ++w) anc[w] = tail ? sAnc[rr * kAncWords + w] : 0u;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
-      const int sb = t & 1;
-      if (!mbar_wait_bounded(&sfull[sb], (t >> 1) & 1, &s_abort)) {
+      if (!mbar_wait_bounded(&sfull[a], t & 1, &s_abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t s0[32], s1[32];
-      tmem_ld_x32(tmem + lane_off + sb * kKT, s0);
-      tmem_ld_x32(tmem + lane_off + sb * kKT + 32, s1);
+      tmem_ld_x32(tS, s0);
+      tmem_ld_x32(tS + 32, s1);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sfree[sb]);
-      float v[kKT];
+      if (lane == 0) mbar_arrive(&sfree[a]);
+      float v[kKT];  // raw scores; the softmax scale (log2 units) is applied in the exponent
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        v[j] = __uint_as_float(s0[j]) * p.scale_log2;
-        v[j + 32] = __uint_as_float(s1[j]) * p.scale_log2;
+        v[j] = __uint_as_float(s0[j]);
+        v[j + 32] = __uint_as_float(s1[j]);
       }
       const long long kbase = kb + (long long)t * kKT;
       if (tail || kbase + kKT > ke) {
@@ -339,28 +365,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!keep) v[j] = -INFINITY;
         }
       }
-      float tmax = v[0];
+      float mx[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-      for (int j = 1; j < kKT; ++j) tmax = fmaxf(tmax, v[j]);
+      for (int j = 4; j < kKT; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
       const float m_new = fmaxf(m_run, tmax);
       const bool need = m_new > m_run + kRescaleLog2;  // includes the first finite maximum
+      // P V of the previous tile must be done before P is overwritten or O is rescaled
+      if (t > 0 && !mbar_wait_bounded(&ofull[a], (t - 1) & 1, &s_abort)) {
+        ok = false;
+        break;
+      }
       if (__any_sync(0xffffffffu, need)) {
         const float f = need ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run is -inf
         if (t > 0) {
-          // O holds the previous tiles: wait for their last P V, then rescale in place
-          if (!mbar_wait_bounded(ofull, (t - 1) & 1, &s_abort)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
-            tmem_ld_x32(tmem_o + lane_off + c * 32, o);
+            tmem_ld_x32(tO + c * 32, o);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-            tmem_st_x32(tmem_o + lane_off + c * 32, o);
+            tmem_st_x32(tO + c * 32, o);
           }
           tmem_st_wait();
         }
@@ -370,43 +397,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-      float psum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[kKT / 2];
 #pragma unroll
       for (int j = 0; j < kKT; j += 2) {
-        const float p0 = exp2f(v[j] - mu), p1 = exp2f(v[j + 1] - mu);
-        psum += p0 + p1;
+        const float p0 = ex2_approx(fmaf(v[j], p.scale_log2, -mu)), p1 = ex2_approx(fmaf(v[j + 1], p.scale_log2, -mu));
+        ps[(j >> 1) & 3] += p0 + p1;
         pk[j / 2] = pack_bf16x2(p0, p1);
       }
-      l_run += psum;
-      if (!mbar_wait_bounded(&pfree[sb], ((t >> 1) & 1) ^ 1, &s_abort)) {
-        ok = false;
-        break;
-      }
-      uint8_t* prow = sP + sb * C::kP;
+      l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
 #pragma unroll
       for (int ch = 0; ch < kKT / 8; ++ch)
-        *reinterpret_cast<uint4*>(prow + sw128_off(r, ch, kRows)) =
+        *reinterpret_cast<uint4*>(prow + sw128_off(rl, ch, kGR)) =
             make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&pfull[sb]);
+      if (lane == 0) mbar_arrive(&pfull[a]);
     }
-    if (ok && mbar_wait_bounded(ofull, (T - 1) & 1, &s_abort)) {
+    if (ok && mbar_wait_bounded(&ofull[a], (T - 1) & 1, &s_abort)) {
       tc_fence_after();
       const bool valid = row < rows_total;
       size_t orow = 0;
       if (valid) {
-        const int i = row / p.G, h = g * p.G + row % p.G;
-        orow = ((size_t)b * p.N + i) * p.Hq + h;
+        const int i = row / p.G, hq = g * p.G + row % p.G;
+        orow = ((size_t)b * p.N + i) * p.Hq + hq;
         p.part_ml[orow * p.n_split + split] = make_float2(m_run, l_run);
       }
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld_x32(tmem_o + lane_off + c * 32, o);
+        tmem_ld_x32(tO + c * 32, o);
         tmem_ld_wait();
         if (valid) {
           float* dst = p.part_o + (orow * p.n_split + split) * D + c * 32;
@@ -423,8 +445,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         set_status(p.dev_status, SPEC_ERR_TIMEOUT);
       }
       if (row < rows_total) {  // the merge skips this split
-        const int i = row / p.G, h = g * p.G + row % p.G;
-        p.part_ml[(((size_t)b * p.N + i) * p.Hq + h) * p.n_split + split] = make_float2(-INFINITY, 0.f);
+        const int i = row / p.G, hq = g * p.G + row % p.G;
+        p.part_ml[(((size_t)b * p.N + i) * p.Hq + hq) * p.n_split + split] = make_float2(-INFINITY, 0.f);
       }
     }
   }
@@ -440,24 +462,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-size_t attention_tc_smem_bytes(int d) { return d == 128 ? AttnTcCfg<128>::kSmem : AttnTcCfg<64>::kSmem; }
+int attention_tc_rows_per_cta(int groups) { return kGR * groups; }
+
+template <int D, int NG>
+static cudaError_t launch_tc(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p, cudaStream_t stream) {
+  using C = AttnTcCfg<D, NG>;
+  const dim3 grid(p.n_rg, p.n_split, p.B * p.Hkv);
+  cudaError_t err = cudaFuncSetAttribute(attn_tc_kernel<D, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (err != cudaSuccess) return err;
+  attn_tc_kernel<D, NG><<<grid, C::kThreads, C::kSmem, stream>>>(*tmK, *tmV, p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attention_tc(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
                                 cudaStream_t stream) {
-  const dim3 grid(p.n_rg, p.n_split, p.B * p.Hkv);
-  cudaError_t err;
-  if (p.d == 128) {
-    const int smem = AttnTcCfg<128>::kSmem;
-    err = cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    attn_tc_kernel<128><<<grid, kTcThreads, smem, stream>>>(*tmK, *tmV, p);
-  } else {
-    const int smem = AttnTcCfg<64>::kSmem;
-    err = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    attn_tc_kernel<64><<<grid, kTcThreads, smem, stream>>>(*tmK, *tmV, p);
-  }
-  return cudaGetLastError();
+  if (p.d == 128) return p.groups == 2 ? launch_tc<128, 2>(tmK, tmV, p, stream) : launch_tc<128, 1>(tmK, tmV, p, stream);
+  return p.groups == 2 ? launch_tc<64, 2>(tmK, tmV, p, stream) : launch_tc<64, 1>(tmK, tmV, p, stream);
 }
 
 }  // namespace spectree

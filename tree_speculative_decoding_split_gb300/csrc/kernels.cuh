@@ -35,18 +35,19 @@ struct AttnParams {
   int n_prefix;      // prefix splits
   int chunk;         // keys per prefix split
   int n_split;       // n_prefix + 1 (the last split holds the tree tail)
-  int n_rg;          // row groups of 128 (node, head) rows per KV head
+  int n_rg;          // row groups of (node, head) rows per KV head (one bf16 CTA each)
+  int groups;        // 128-row groups per bf16 CTA (1 or 2)
   float scale;
   float scale_log2;
   int32_t* dev_status;
 };
 
 struct AttnPlan {
-  int n_rg, n_prefix, chunk, n_split;
+  int n_rg, n_prefix, chunk, n_split, groups;
 };
 AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_sms);
 void launch_attention_merge_bf16(const AttnParams& p, cudaStream_t stream);
-size_t attention_tc_smem_bytes(int d);
+int attention_tc_rows_per_cta(int groups);
 cudaError_t launch_attention_tc(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
                                 cudaStream_t stream);
 void launch_attention_f32(const AttnParams& p, cudaStream_t stream);
