@@ -150,6 +150,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# ---- replicas ------------------------------------------------------------------------------------
+
+def aggregate_ranks(times_ms, dist=None, device=None):
+    """Slowest rank's times: every rank runs an independent replica of the workload, so the job's
+    rate is (ranks x work per rank) / the maximum time.  Without a process group, identity."""
+    if dist is None:
+        return list(times_ms)
+    import torch
+    buf = torch.tensor(list(times_ms), dtype=torch.float64, device=device)
+    dist.all_reduce(buf, op=dist.ReduceOp.MAX)
+    return [float(x) for x in buf]
+
+
+def job_rate(world, units_per_rank, ms):
+    """Whole-job throughput in units/s from the slowest rank's per-step time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ---- native arm ---------------------------------------------------------------------------------
 
 def _device_tensors(case, dev):
@@ -313,10 +331,7 @@ def run_native(a, rank, world, dist):
     torch.cuda.synchronize()
     e2e_ms = statistics.fmean(es[i].elapsed_time(ee[i]) for i in range(KE))
 
-    if dist:
-        buf = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(buf, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(buf[0]), float(buf[1])
+    ms, e2e_ms = aggregate_ranks([ms, e2e_ms], dist, dev)
     if rank != 0:
         return None
 
@@ -333,14 +348,14 @@ def run_native(a, rank, world, dist):
     t_tc = (w["lm_flops"] + w["attn_flops"]) / (tc_sus * 1e12)
     t_ns = max((w["kv_bytes"] + w["w_bytes"]) / (hbm * 1e9), w["lm_flops"] / (tc_sus * 1e12))
     line = {
-        "metric": METRIC, "value": world * w["nodes"] / (ms * 1e-3), "unit": UNIT, "n_gpus": world, "steps": K,
+        "metric": METRIC, "value": job_rate(world, w["nodes"], ms), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, a.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": case.name, "batch": case.B, "prefix_len": [int(x) for x in case.prefix_len][:8],
                    "tree_nodes": int(case.n_nodes[0]), "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d,
                    "hidden": case.Hd, "vocab": case.V, "rule": case.rule, "eps": case.eps, "delta": case.delta,
                    "parallelism": f"replicas x{world}", "l2": "flushed before every step (256 MB write, then read)"},
-        "e2e": {"value": world * w["nodes"] / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+        "e2e": {"value": job_rate(world, w["nodes"], e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": K * _launches_per_step(case),
         "roofline": ({"kernel": "lmhead_tc_kernel (LM head GEMM + row statistics)", "bound": "tensor",
