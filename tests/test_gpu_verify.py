@@ -104,3 +104,24 @@ def test_llama70b_greedy_subset():
     ref = H.oracle_verify(case, requests=req)
     H.check_verify(case, got, ref, requests=req)
     H.check_row_stats(case, got, _rows(case, req, limit=8))
+
+
+@pytest.mark.parametrize("V", [2500, 5000, 20000, 300001])
+def test_rejection_vocabulary_slices(V):
+    """Vocabulary sizes that split each request's rejection walk over clusters of 2, 4 and 8 CTAs
+    with ragged slices (V = 1000 above runs on one CTA), and one above 8 x 32768 entries that
+    takes the single-CTA walk with the residual in global memory."""
+    d = H.dev()
+    rng = np.random.default_rng(V)
+    n_tree = 24 if V > 100000 else 48
+    parents = [T.random_bfs_tree(rng, n_tree, 5)[0], T.chain_tree(12), T.random_bfs_tree(rng, n_tree, 3)[0]]
+    case = make_case(dtype="bf16", Hq=4, Hkv=1, d=64, Hd=128, V=V, prefix_len=[4] * 3, parents=parents,
+                     rule="rejection", tau=0.9, seed=V + 1, tokens=("iid", 0.8, 0.4), rng=rng)
+    got = H.gpu_verify(case, H.to_device(case, d))
+    assert got["status"] == 0
+    ref = H.oracle_verify(case)
+    exact, excluded = H.check_verify(case, got, ref)
+    assert exact + excluded == case.B
+    # at large V the bonus draw always lands within the margin band of its neighbours; the path
+    # itself must still have been compared exactly for some request
+    assert sum(not ref[b]["path_margins"] for b in range(case.B)) >= 1

@@ -17,8 +17,17 @@
 // and depth come from pointer jumping over the parent array (8 rounds for 255 nodes), and the
 // deepest reachable node with the lowest index wins.
 // Rejection: the walk is sequential over siblings; each rejected sibling costs one pass over the
-// vocabulary (R <- relu(R - D_e) and its sum) by all 1024 threads of the request's CTA, and the
-// bonus token is an inverse-CDF search (per-thread chunk sums, a block scan, then one chunk).
+// vocabulary (R <- relu(R - D_e) and its sum).  A request runs on a thread-block cluster of up
+// to 8 CTAs that split the vocabulary: each thread keeps its slice of R in registers and of D_e
+// in shared memory, so a rejected sibling costs one on-chip pass and one cluster barrier (the
+// partial sums are exchanged through distributed shared memory).  The bonus token is an
+// inverse-CDF search: per-warp segment sums, a prefix over CTAs, then one warp scans its segment.
+// Vocabularies above 8 x 32768 entries use a single CTA per request with R in global memory.
+
+#include <cooperative_groups.h>
+
+#include <climits>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -300,7 +309,7 @@ namespace {
 constexpr int kRejThreads = 1024;
 }
 
-__global__ void __launch_bounds__(kRejThreads) accept_rejection_kernel(const AcceptParams p) {
+__global__ void __launch_bounds__(kRejThreads) accept_rejection_block_kernel(const AcceptParams p) {
   __shared__ int s_parent[kMaxNodes];
   __shared__ int s_tok[kMaxNodes];
   __shared__ int s_kids[kMaxNodes];
@@ -455,6 +464,379 @@ __global__ void __launch_bounds__(kRejThreads) accept_rejection_kernel(const Acc
   }
 }
 
+// ---- rejection sampling on a thread-block cluster ---------------------------------------------
+
+namespace {
+
+constexpr int kRcThreads = 512;    // threads per CTA
+constexpr int kRcEpt = 64;         // vocabulary entries per thread (registers)
+constexpr int kRcMaxCluster = 8;   // CTAs per request at most (portable cluster size)
+constexpr int kRcSlice = kRcThreads * kRcEpt;  // vocabulary entries per CTA at most
+constexpr int kRcSmem = kRcSlice * (int)sizeof(float);
+
+// T(v) = softmax(z / tau)[v], and one residual step relu(R / S - D): written with explicit fused
+// operations so that every CTA of a cluster evaluates them bit for bit alike.
+__device__ __forceinline__ float target_prob(float z, float inv_tau, float lse) {
+  return expf(fmaf(z, inv_tau, -lse));
+}
+__device__ __forceinline__ float residual_step(float r, float inv_s, float d) {
+  return fmaxf(fmaf(r, inv_s, -d), 0.f);
+}
+
+__device__ __forceinline__ float draft_prob(const AcceptParams& p, const float* row, int v) {
+  if (p.inv_map) {
+    const int j = p.inv_map[v];
+    return j >= 0 ? row[j] : 0.f;
+  }
+  return row[v];
+}
+
+}  // namespace
+
+// One request per cluster of kc CTAs; CTA `rank` holds vocabulary entries [rank*C, rank*C + C),
+// C = ceil(V / kc), entry base + j*512 + tid in register r[j] of thread tid.  Every control
+// decision (accept, adopt a residual, which CTA owns the bonus) is taken by every CTA from the
+// same shared values in the same order, so all CTAs pass the same sequence of cluster barriers.
+// Exchanged values (partial sums, the next sibling's R and D entries) are double-buffered by
+// barrier parity: a slot is rewritten only two barriers after it was read.
+__global__ void __launch_bounds__(kRcThreads, 1)
+    accept_rejection_cluster_kernel(const AcceptParams p) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  extern __shared__ float4 s_dyn4[];
+  float* s_D = reinterpret_cast<float*>(s_dyn4);  // D_e of this slice; R of the slice at the end
+  __shared__ int s_parent[kMaxNodes];
+  __shared__ int s_tok[kMaxNodes];
+  __shared__ int s_first[kMaxNodes];
+  __shared__ int s_next[kMaxNodes];
+  __shared__ float s_slot[2][3];                 // next sibling's R before / after, and D
+  __shared__ float s_part[2][kRcMaxCluster];     // per-CTA residual sums
+  __shared__ double s_tot[kRcMaxCluster];        // per-CTA mass of the final distribution
+  __shared__ float s_red[kRcThreads / 32];
+  __shared__ double s_wsum[kRcThreads / 32];
+
+  const int kc = (int)cl.num_blocks(), rank = (int)cl.block_rank();
+  const int b = blockIdx.x / kc;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  cl.sync();  // every CTA of the cluster is running before any remote shared-memory access
+
+  const int err = load_and_validate(p, b, s_parent, s_tok);
+  if (err || (p.map_bad && *p.map_bad)) {
+    if (rank == 0) {
+      if (tid == 0 && err) set_status(p.dev_status, err);
+      zero_outputs(p, b, tid, blockDim.x);
+    }
+    return;
+  }
+  const int n = p.n_nodes[b];
+  // children of each node in increasing index order: first child and next sibling
+  for (int c = tid; c < n; c += kRcThreads) s_first[c] = INT_MAX;
+  __syncthreads();
+  for (int c = 1 + tid; c < n; c += kRcThreads) atomicMin(&s_first[s_parent[c]], c);
+  for (int c = tid; c < n; c += kRcThreads) {
+    int nx = -1;
+    if (c > 0) {
+      const int pc = s_parent[c];
+      for (int q = c + 1; q < n; ++q)
+        if (s_parent[q] == pc) { nx = q; break; }
+    }
+    s_next[c] = nx;
+  }
+  __syncthreads();
+
+  const int V = p.V;
+  const int C = (V + kc - 1) / kc;
+  const int base = rank * C;
+  const int Lc = max(0, min(C, V - base));
+  const size_t rb = (size_t)b * p.N;
+  float r[kRcEpt];
+  float S = 1.f;  // sum of the residual held in r (1 while r holds T_e itself)
+  int e = 0, dep = 0, margins = 0, sp = 0;
+
+  auto load_node = [&](int node) {
+    const float* lg = p.logits + (rb + node) * (size_t)V + base;
+    const float lse = p.rlse[rb + node];
+    const float* drow = p.draft + (rb + node) * (size_t)p.Vd;
+#pragma unroll
+    for (int j = 0; j < kRcEpt; ++j) {
+      const int li = j * kRcThreads + tid;
+      float t = 0.f;
+      if (li < Lc) {
+        t = target_prob(__ldg(lg + li), p.inv_tau, lse);
+        s_D[li] = draft_prob(p, drow, base + li);
+      }
+      r[j] = t;
+    }
+    S = 1.f;
+  };
+
+  load_node(0);
+  while (true) {
+    int c = s_first[e];
+    if (c == INT_MAX) break;  // a leaf: the bonus is drawn from T_e
+    // first child: R = T_e, so every CTA evaluates R[x] and D[x] itself
+    const size_t erow = rb + e;
+    int x = s_tok[c];
+    float rx = target_prob(__ldg(p.logits + erow * (size_t)V + x), p.inv_tau, p.rlse[erow]);
+    float dx = draft_prob(p, p.draft + erow * (size_t)p.Vd, x);
+    bool moved = false;
+    while (true) {
+      const float u = accept_uniform(p.seed, (uint32_t)b, (uint32_t)c, 0u);
+      const float Rx = rx / S;
+      const float a = (dx > 0.f) ? fminf(1.f, Rx / dx) : (Rx > 0.f ? 1.f : 0.f);
+      if (fabsf(u - a) < kMargin) ++margins;
+      if (u * dx < Rx) {
+        e = c;
+        ++dep;
+        load_node(e);
+        moved = true;
+        break;
+      }
+      // rejected: residual sum of this slice (R is replaced only if the total is positive)
+      const int nc = s_next[c];
+      const float inv_s = 1.f / S;
+      float part = 0.f;
+#pragma unroll
+      for (int j = 0; j < kRcEpt; ++j) {
+        const int li = j * kRcThreads + tid;
+        if (li < Lc) part += residual_step(r[j], inv_s, s_D[li]);
+      }
+      part = warp_sum(part);
+      if (lane == 0) s_red[warp] = part;
+      if (nc >= 0) {  // the owner of the next sibling's token publishes R[x] before and after
+        const int xo = s_tok[nc];
+        const int owner = xo / C, li = xo - owner * C;
+        if (owner == rank && li % kRcThreads == tid) {
+          const int jj = li / kRcThreads;
+          float ro = 0.f;
+#pragma unroll
+          for (int j = 0; j < kRcEpt; ++j)
+            if (j == jj) ro = r[j];
+          const float dd = s_D[li];
+          const float rn = residual_step(ro, inv_s, dd);
+          for (int q = 0; q < kc; ++q) {
+            float* dst = cl.map_shared_rank(&s_slot[sp][0], q);
+            dst[0] = ro;
+            dst[1] = rn;
+            dst[2] = dd;
+          }
+        }
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float cta = 0.f;
+        for (int w = 0; w < kRcThreads / 32; ++w) cta += s_red[w];
+        for (int q = 0; q < kc; ++q) cl.map_shared_rank(&s_part[sp][0], q)[rank] = cta;
+      }
+      cl.sync();
+      float s_new = 0.f;
+      for (int q = 0; q < kc; ++q) s_new += s_part[sp][q];
+      if (s_new > 0.f) {
+#pragma unroll
+        for (int j = 0; j < kRcEpt; ++j) {
+          const int li = j * kRcThreads + tid;
+          if (li < Lc) r[j] = residual_step(r[j], inv_s, s_D[li]);
+        }
+        S = s_new;
+      }
+      if (nc >= 0) {
+        rx = (s_new > 0.f) ? s_slot[sp][1] : s_slot[sp][0];
+        dx = s_slot[sp][2];
+      }
+      sp ^= 1;
+      if (nc < 0) break;
+      c = nc;
+    }
+    if (!moved) break;
+  }
+
+  if (dep + 1 > p.path_cap) {
+    if (rank == 0) {
+      if (tid == 0) set_status(p.dev_status, SPEC_ERR_CAPACITY);
+      zero_outputs(p, b, tid, blockDim.x);
+    }
+    return;
+  }
+
+  // ---- bonus token: inverse CDF of R at u' = U(seed, b, e, 1) ----
+  // R (unnormalised; T_e when no residual was adopted at e) goes to shared memory in vocabulary
+  // order.  Warp w owns the contiguous segment [w*Ws, w*Ws + Ws) of the slice.
+#pragma unroll
+  for (int j = 0; j < kRcEpt; ++j) {
+    const int li = j * kRcThreads + tid;
+    if (li < Lc) s_D[li] = r[j];
+  }
+  __syncthreads();
+  constexpr int kWarps = kRcThreads / 32;
+  const int Ws = (Lc + kWarps - 1) / kWarps;
+  const int w0 = min(Lc, warp * Ws), w1 = min(Lc, w0 + Ws);
+  float lsum = 0.f;
+  for (int v = w0 + lane; v < w1; v += 32) lsum += s_D[v];
+  const double wsum = warp_sum_d((double)lsum);
+  if (lane == 0) s_wsum[warp] = wsum;
+  __syncthreads();
+  if (tid == 0) {
+    double cta = 0.0;
+    for (int w = 0; w < kWarps; ++w) cta += s_wsum[w];
+    for (int q = 0; q < kc; ++q) cl.map_shared_rank(&s_tot[0], q)[rank] = cta;
+  }
+  cl.sync();
+  double total = 0.0, pre = 0.0;
+  int owner_cta = -1;
+  const float u2 = accept_uniform(p.seed, (uint32_t)b, (uint32_t)e, 1u);
+  {
+    double run = 0.0;
+    for (int q = 0; q < kc; ++q) run += s_tot[q];
+    total = run;
+    const double target = (double)u2 * total;
+    run = 0.0;
+    for (int q = 0; q < kc; ++q) {  // last CTA with mass that starts at or below the target
+      if (q == rank) pre = run;
+      if (s_tot[q] > 0.0 && run <= target) owner_cta = q;
+      run += s_tot[q];
+    }
+  }
+  const double target = (double)u2 * total;
+  const double band = (double)kMargin * total;
+  if (owner_cta == rank) {
+    int owner_warp = -1;
+    double wstart = 0.0, run = pre;
+    for (int w = 0; w < kWarps; ++w) {
+      if (s_wsum[w] > 0.0 && run <= target) { owner_warp = w; wstart = run; }
+      run += s_wsum[w];
+    }
+    if (warp == owner_warp) {
+      double acc = wstart, prev = wstart;
+      int found = -1, last_nz = -1;
+      for (int v0 = w0; v0 < w1; v0 += 32) {
+        const int v = v0 + lane;
+        const float val = (v < w1) ? s_D[v] : 0.f;
+        float incl = val;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const double accl = acc + (double)incl;
+        const unsigned hit = __ballot_sync(0xffffffffu, v < w1 && accl > target);
+        const unsigned nz = __ballot_sync(0xffffffffu, val > 0.f);
+        if (hit) {
+          const int h = __ffs(hit) - 1;
+          found = base + v0 + h;
+          const double ah = __shfl_sync(0xffffffffu, accl, h);
+          const float vh = __shfl_sync(0xffffffffu, val, h);
+          prev = ah - (double)vh;
+          acc = ah;
+          break;
+        }
+        if (nz) last_nz = base + v0 + 31 - __clz(nz);
+        acc += (double)__shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (found < 0) {
+        found = last_nz >= 0 ? last_nz : V - 1;
+        prev = acc;
+      }
+      if (lane == 0) {
+        const bool near = (target - prev < band) || (acc - target < band) || (target < band);
+        p.bonus[b] = found;
+        if (p.bonus_margin) p.bonus_margin[b] = near ? 1 : 0;
+      }
+    }
+  }
+  if (rank == 0) {
+    write_path(p, b, e, dep, s_parent);
+    if (tid == 0) {
+      p.accept_len[b] = dep;
+      if (owner_cta < 0) {  // no mass at all (cannot happen for a softmax row)
+        p.bonus[b] = V - 1;
+        if (p.bonus_margin) p.bonus_margin[b] = 0;
+      }
+      if (p.margin_count) p.margin_count[b] = margins;
+    }
+  }
+}
+
+bool rejection_uses_cluster(int V) { return V >= 1 && V <= kRcMaxCluster * kRcSlice; }
+
+namespace {
+
+// Largest number of co-resident clusters of 1, 2, 4 and 8 CTAs, per device, measured once.
+struct ClusterOccupancy {
+  bool ready = false;
+  bool ok = false;
+  int max_clusters[4] = {0, 0, 0, 0};
+};
+std::mutex g_rc_mutex;
+ClusterOccupancy g_rc_occ[64];
+
+const ClusterOccupancy& cluster_occupancy() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_rc_mutex);
+  ClusterOccupancy& o = g_rc_occ[dev & 63];
+  if (o.ready) return o;
+  o.ready = true;
+  if (cudaFuncSetAttribute(accept_rejection_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kRcSmem) != cudaSuccess)
+    return o;
+  o.ok = true;
+  for (int i = 0; i < 4; ++i) {
+    const int kc = 1 << i;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kc, 1, 1);
+    cfg.blockDim = dim3(kRcThreads, 1, 1);
+    cfg.dynamicSmemBytes = kRcSmem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = kc;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int m = 0;
+    if (cudaOccupancyMaxActiveClusters(&m, (void*)accept_rejection_cluster_kernel, &cfg) != cudaSuccess) m = 0;
+    o.max_clusters[i] = m;
+  }
+  cudaGetLastError();
+  return o;
+}
+
+}  // namespace
+
+// Cluster size: the smallest that fits the vocabulary in registers, widened (up to 8) while
+// every request still gets a co-resident cluster and each CTA keeps >= 1024 entries.
+int rejection_cluster_size(int B, int V, const int* max_clusters) {
+  int i0 = 0;
+  while (i0 < 3 && (V + (1 << i0) - 1) / (1 << i0) > kRcSlice) ++i0;
+  int best = i0;
+  for (int i = i0 + 1; i < 4; ++i)
+    if (B <= max_clusters[i] && V >= (1 << i) * 1024) best = i;
+  return 1 << best;
+}
+
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {
+  if (!rejection_uses_cluster(p.V)) {
+    accept_rejection_block_kernel<<<p.B, kRejThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  const ClusterOccupancy& occ = cluster_occupancy();
+  if (!occ.ok) return cudaErrorInvalidConfiguration;
+  const int kc = rejection_cluster_size(p.B, p.V, occ.max_clusters);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * kc), 1, 1);
+  cfg.blockDim = dim3(kRcThreads, 1, 1);
+  cfg.dynamicSmemBytes = kRcSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = kc;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, accept_rejection_cluster_kernel, p);
+}
+
 // ---- draft map inversion --------------------------------------------------------------------
 
 __global__ void __launch_bounds__(256) inverse_map_kernel(const int32_t* __restrict__ map, int Vd, int V,
@@ -476,8 +858,5 @@ void launch_build_inverse_map(const int32_t* map, int Vd, int V, int32_t* inv, i
   inverse_map_kernel<<<(Vd + 255) / 256, 256, 0, stream>>>(map, Vd, V, inv, map_bad, dev_status);
 }
 
-void launch_accept(const AcceptParams& p, cudaStream_t stream) {
-  accept_rejection_kernel<<<p.B, kRejThreads, 0, stream>>>(p);
-}
 
 }  // namespace spectree

@@ -189,7 +189,7 @@ VerifyLayout layout_verify(const spec_verify_args* a, void* ws) {
   l.inv = nullptr;
   l.map_bad = nullptr;
   if (a->rule == SPEC_RULE_REJECTION) {
-    l.rbuf = c.take<float>((size_t)B * 2 * a->vocab);
+    if (!rejection_uses_cluster(a->vocab)) l.rbuf = c.take<float>((size_t)B * 2 * a->vocab);
     if (a->draft_to_target) {
       l.inv = c.take<int32_t>(a->vocab);
       l.map_bad = c.take<int32_t>(1);
@@ -352,7 +352,7 @@ spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_
   fp.counters = l.counters;
   fp.acc = ap;
   launch_row_finalize(fp, stream);
-  if (a->rule == SPEC_RULE_REJECTION) launch_accept(ap, stream);
+  if (a->rule == SPEC_RULE_REJECTION && launch_accept(ap, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -116,7 +116,9 @@ void launch_row_finalize(const FinalizeParams& p, cudaStream_t stream);
 
 void launch_build_inverse_map(const int32_t* map, int Vd, int V, int32_t* inv, int32_t* map_bad,
                               int32_t* dev_status, cudaStream_t stream);
-void launch_accept(const AcceptParams& p, cudaStream_t stream);
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
+// True when the rejection walk runs on a thread-block cluster (R held on chip, no R buffer).
+bool rejection_uses_cluster(int V);
 
 // ---- K4: KV compaction ----------------------------------------------------------------------
 void launch_compact_kv(void* k, void* v, int elem_bytes, const int32_t* prefix_len,
