@@ -483,22 +483,31 @@ __device__ __forceinline__ float residual_step(float r, float inv_s, float d) {
   return fmaxf(fmaf(r, inv_s, -d), 0.f);
 }
 
-__device__ __forceinline__ float draft_prob(const AcceptParams& p, const float* row, int v) {
-  if (p.inv_map) {
-    const int j = p.inv_map[v];
-    return j >= 0 ? row[j] : 0.f;
+__device__ __forceinline__ void cp_async_4(float* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Next child of `node` after child `after` (-1: the first child), from the children bitmask.
+__device__ __forceinline__ int next_child(const uint32_t (*kids)[kAncWords], int node, int after) {
+  const int from = after + 1;
+  for (int w = from >> 5; w < kAncWords; ++w) {
+    uint32_t m = kids[node][w];
+    if (w == (from >> 5)) m &= ~0u << (from & 31);
+    if (m) return w * 32 + __ffs(m) - 1;
   }
-  return row[v];
+  return -1;
 }
 
 }  // namespace
 
 // One request per cluster of kc CTAs; CTA `rank` holds vocabulary entries [rank*C, rank*C + C),
-// C = ceil(V / kc), entry base + j*512 + tid in register r[j] of thread tid.  Every control
-// decision (accept, adopt a residual, which CTA owns the bonus) is taken by every CTA from the
-// same shared values in the same order, so all CTAs pass the same sequence of cluster barriers.
-// Exchanged values (partial sums, the next sibling's R and D entries) are double-buffered by
-// barrier parity: a slot is rewritten only two barriers after it was read.
+// C = ceil(V / kc), entry base + j*512 + tid in register r[j] of thread tid and its draft
+// probability in s_D[j*512 + tid].  Every control decision (accept, adopt a residual, which CTA
+// owns the bonus) is taken by every CTA from the same shared values in the same order, so all
+// CTAs pass the same sequence of cluster barriers.  Exchanged values (partial sums, the next
+// sibling's R and D entries) are double-buffered by barrier parity: a slot is rewritten only two
+// barriers after it was read.
 __global__ void __launch_bounds__(kRcThreads, 1)
     accept_rejection_cluster_kernel(const AcceptParams p) {
   namespace cg = cooperative_groups;
@@ -507,13 +516,13 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   float* s_D = reinterpret_cast<float*>(s_dyn4);  // D_e of this slice; R of the slice at the end
   __shared__ int s_parent[kMaxNodes];
   __shared__ int s_tok[kMaxNodes];
-  __shared__ int s_first[kMaxNodes];
-  __shared__ int s_next[kMaxNodes];
-  __shared__ float s_slot[2][3];                 // next sibling's R before / after, and D
-  __shared__ float s_part[2][kRcMaxCluster];     // per-CTA residual sums
-  __shared__ double s_tot[kRcMaxCluster];        // per-CTA mass of the final distribution
+  __shared__ uint32_t s_kids[kMaxNodes][kAncWords];  // children of each node, as bits
+  __shared__ float s_slot[2][3];                     // next sibling's R before / after, and D
+  __shared__ float s_part[2][kRcMaxCluster];         // per-CTA residual sums
+  __shared__ double s_tot[kRcMaxCluster];            // per-CTA mass of the final distribution
   __shared__ float s_red[kRcThreads / 32];
-  __shared__ double s_wsum[kRcThreads / 32];
+  __shared__ double s_dred[kRcThreads / 32];
+  __shared__ int s_owner;
 
   const int kc = (int)cl.num_blocks(), rank = (int)cl.block_rank();
   const int b = blockIdx.x / kc;
@@ -529,19 +538,9 @@ __global__ void __launch_bounds__(kRcThreads, 1)
     return;
   }
   const int n = p.n_nodes[b];
-  // children of each node in increasing index order: first child and next sibling
-  for (int c = tid; c < n; c += kRcThreads) s_first[c] = INT_MAX;
+  for (int i = tid; i < n * kAncWords; i += kRcThreads) (&s_kids[0][0])[i] = 0u;
   __syncthreads();
-  for (int c = 1 + tid; c < n; c += kRcThreads) atomicMin(&s_first[s_parent[c]], c);
-  for (int c = tid; c < n; c += kRcThreads) {
-    int nx = -1;
-    if (c > 0) {
-      const int pc = s_parent[c];
-      for (int q = c + 1; q < n; ++q)
-        if (s_parent[q] == pc) { nx = q; break; }
-    }
-    s_next[c] = nx;
-  }
+  for (int c = 1 + tid; c < n; c += kRcThreads) atomicOr(&s_kids[s_parent[c]][c >> 5], 1u << (c & 31));
   __syncthreads();
 
   const int V = p.V;
@@ -552,102 +551,156 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   float r[kRcEpt];
   float S = 1.f;  // sum of the residual held in r (1 while r holds T_e itself)
   int e = 0, dep = 0, margins = 0, sp = 0;
+  bool moved = true;
 
-  auto load_node = [&](int node) {
-    const float* lg = p.logits + (rb + node) * (size_t)V + base;
-    const float lse = p.rlse[rb + node];
-    const float* drow = p.draft + (rb + node) * (size_t)p.Vd;
-#pragma unroll
-    for (int j = 0; j < kRcEpt; ++j) {
-      const int li = j * kRcThreads + tid;
-      float t = 0.f;
-      if (li < Lc) {
-        t = target_prob(__ldg(lg + li), p.inv_tau, lse);
-        s_D[li] = draft_prob(p, drow, base + li);
-      }
-      r[j] = t;
-    }
-    S = 1.f;
-  };
-
-  load_node(0);
-  while (true) {
-    int c = s_first[e];
-    if (c == INT_MAX) break;  // a leaf: the bonus is drawn from T_e
-    // first child: R = T_e, so every CTA evaluates R[x] and D[x] itself
-    const size_t erow = rb + e;
-    int x = s_tok[c];
-    float rx = target_prob(__ldg(p.logits + erow * (size_t)V + x), p.inv_tau, p.rlse[erow]);
-    float dx = draft_prob(p, p.draft + erow * (size_t)p.Vd, x);
-    bool moved = false;
-    while (true) {
-      const float u = accept_uniform(p.seed, (uint32_t)b, (uint32_t)c, 0u);
-      const float Rx = rx / S;
-      const float a = (dx > 0.f) ? fminf(1.f, Rx / dx) : (Rx > 0.f ? 1.f : 0.f);
-      if (fabsf(u - a) < kMargin) ++margins;
-      if (u * dx < Rx) {
-        e = c;
-        ++dep;
-        load_node(e);
-        moved = true;
-        break;
-      }
-      // rejected: residual sum of this slice (R is replaced only if the total is positive)
-      const int nc = s_next[c];
-      const float inv_s = 1.f / S;
-      float part = 0.f;
-#pragma unroll
-      for (int j = 0; j < kRcEpt; ++j) {
-        const int li = j * kRcThreads + tid;
-        if (li < Lc) part += residual_step(r[j], inv_s, s_D[li]);
-      }
-      part = warp_sum(part);
-      if (lane == 0) s_red[warp] = part;
-      if (nc >= 0) {  // the owner of the next sibling's token publishes R[x] before and after
-        const int xo = s_tok[nc];
-        const int owner = xo / C, li = xo - owner * C;
-        if (owner == rank && li % kRcThreads == tid) {
-          const int jj = li / kRcThreads;
-          float ro = 0.f;
-#pragma unroll
-          for (int j = 0; j < kRcEpt; ++j)
-            if (j == jj) ro = r[j];
-          const float dd = s_D[li];
-          const float rn = residual_step(ro, inv_s, dd);
-          for (int q = 0; q < kc; ++q) {
-            float* dst = cl.map_shared_rank(&s_slot[sp][0], q);
-            dst[0] = ro;
-            dst[1] = rn;
-            dst[2] = dd;
-          }
-        }
-      }
-      __syncthreads();
-      if (tid == 0) {
-        float cta = 0.f;
-        for (int w = 0; w < kRcThreads / 32; ++w) cta += s_red[w];
-        for (int q = 0; q < kc; ++q) cl.map_shared_rank(&s_part[sp][0], q)[rank] = cta;
-      }
-      cl.sync();
-      float s_new = 0.f;
-      for (int q = 0; q < kc; ++q) s_new += s_part[sp][q];
-      if (s_new > 0.f) {
+  while (moved) {
+    // ---- arrive at node e: r <- T_e, s_D <- D_e (this slice) ----
+    {
+      const size_t erow = rb + e;
+      const float* lg = p.logits + erow * (size_t)V + base;
+      const float* drow = p.draft + erow * (size_t)p.Vd;
+      if (p.inv_map) {  // draft indices first (asynchronously, into s_D), then the gathers
 #pragma unroll
         for (int j = 0; j < kRcEpt; ++j) {
           const int li = j * kRcThreads + tid;
-          if (li < Lc) r[j] = residual_step(r[j], inv_s, s_D[li]);
+          if (li < Lc) cp_async_4(s_D + li, p.inv_map + base + li);
         }
-        S = s_new;
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+      } else {
+#pragma unroll
+        for (int j = 0; j < kRcEpt; ++j) {
+          const int li = j * kRcThreads + tid;
+          if (li < Lc) cp_async_4(s_D + li, drow + base + li);
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
       }
-      if (nc >= 0) {
-        rx = (s_new > 0.f) ? s_slot[sp][1] : s_slot[sp][0];
-        dx = s_slot[sp][2];
+#pragma unroll
+      for (int j = 0; j < kRcEpt; ++j) {
+        const int li = j * kRcThreads + tid;
+        r[j] = (li < Lc) ? __ldg(lg + li) : 0.f;
       }
-      sp ^= 1;
-      if (nc < 0) break;
-      c = nc;
+      if (p.inv_map) {
+        cp_async_wait_all();
+#pragma unroll
+        for (int j = 0; j < kRcEpt; ++j) {
+          const int li = j * kRcThreads + tid;
+          if (li < Lc) {
+            const int m = __float_as_int(s_D[li]);
+            if (m >= 0)
+              cp_async_4(s_D + li, drow + m);
+            else
+              s_D[li] = 0.f;
+          }
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+      }
+      const float lse = p.rlse[erow];
+#pragma unroll
+      for (int j = 0; j < kRcEpt; ++j) {
+        const int li = j * kRcThreads + tid;
+        r[j] = (li < Lc) ? target_prob(r[j], p.inv_tau, lse) : 0.f;
+      }
+      S = 1.f;
+      cp_async_wait_all();  // each thread reads back only the entries it copied
     }
-    if (!moved) break;
+    moved = false;
+    int c = next_child(s_kids, e, -1);
+    if (c < 0) break;  // a leaf: the bonus is drawn from T_e
+    // the first child sees R = T_e: every CTA evaluates R[x] and D[x] itself
+    const size_t erow = rb + e;
+    {
+      const int x = s_tok[c];
+      const float* drow = p.draft + erow * (size_t)p.Vd;
+      float rx = target_prob(__ldg(p.logits + erow * (size_t)V + x), p.inv_tau, p.rlse[erow]);
+      float dx;
+      if (p.inv_map) {
+        const int m = __ldg(p.inv_map + x);
+        dx = m >= 0 ? __ldg(drow + m) : 0.f;
+      } else {
+        dx = __ldg(drow + x);
+      }
+      float pend_inv = 0.f;  // > 0: the residual step with this 1/S is still to be applied to r
+      while (true) {
+        const float u = accept_uniform(p.seed, (uint32_t)b, (uint32_t)c, 0u);
+        const float Rx = rx / S;
+        const float a = (dx > 0.f) ? fminf(1.f, Rx / dx) : (Rx > 0.f ? 1.f : 0.f);
+        if (fabsf(u - a) < kMargin) ++margins;
+        if (u * dx < Rx) {
+          e = c;
+          ++dep;
+          moved = true;
+          break;
+        }
+        // rejected: apply a pending residual step, then this slice's sum of relu(R / S - D)
+        const int nc = next_child(s_kids, e, c);
+        const float inv_s = 1.f / S;
+        float part = 0.f;
+        if (pend_inv > 0.f) {
+#pragma unroll
+          for (int j = 0; j < kRcEpt; ++j) {
+            const int li = j * kRcThreads + tid;
+            if (li < Lc) {
+              const float d = s_D[li];
+              r[j] = residual_step(r[j], pend_inv, d);
+              part += residual_step(r[j], inv_s, d);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kRcEpt; ++j) {
+            const int li = j * kRcThreads + tid;
+            if (li < Lc) part += residual_step(r[j], inv_s, s_D[li]);
+          }
+        }
+        part = warp_sum(part);
+        if (lane == 0) s_red[warp] = part;
+        if (nc >= 0) {  // the owner of the next sibling's token publishes R[x] before and after
+          const int xo = s_tok[nc];
+          const int owner = xo / C, li = xo - owner * C;
+          if (owner == rank && li % kRcThreads == tid) {
+            const int jj = li / kRcThreads;
+            float ro = 0.f;
+#pragma unroll
+            for (int j = 0; j < kRcEpt; ++j)
+              if (j == jj) ro = r[j];
+            const float dd = s_D[li];
+            const float rn = residual_step(ro, inv_s, dd);
+            for (int q = 0; q < kc; ++q) {
+              float* dst = cl.map_shared_rank(&s_slot[sp][0], q);
+              dst[0] = ro;
+              dst[1] = rn;
+              dst[2] = dd;
+            }
+          }
+        }
+        __syncthreads();
+        if (tid == 0) {
+          float cta = 0.f;
+          for (int w = 0; w < kRcThreads / 32; ++w) cta += s_red[w];
+          for (int q = 0; q < kc; ++q) cl.map_shared_rank(&s_part[sp][0], q)[rank] = cta;
+        }
+        cl.sync();
+        float s_new = 0.f;
+        for (int q = 0; q < kc; ++q) s_new += s_part[sp][q];
+        const bool adopt = s_new > 0.f;  // otherwise R stays as it is
+        pend_inv = adopt ? inv_s : 0.f;
+        if (adopt) S = s_new;
+        if (nc >= 0) {
+          rx = adopt ? s_slot[sp][1] : s_slot[sp][0];
+          dx = s_slot[sp][2];
+        }
+        sp ^= 1;
+        if (nc < 0) break;
+        c = nc;
+      }
+      if (!moved && pend_inv > 0.f) {
+#pragma unroll
+        for (int j = 0; j < kRcEpt; ++j) {
+          const int li = j * kRcThreads + tid;
+          if (li < Lc) r[j] = residual_step(r[j], pend_inv, s_D[li]);
+        }
+      }
+    }
   }
 
   if (dep + 1 > p.path_cap) {
@@ -660,87 +713,74 @@ __global__ void __launch_bounds__(kRcThreads, 1)
 
   // ---- bonus token: inverse CDF of R at u' = U(seed, b, e, 1) ----
   // R (unnormalised; T_e when no residual was adopted at e) goes to shared memory in vocabulary
-  // order.  Warp w owns the contiguous segment [w*Ws, w*Ws + Ws) of the slice.
+  // order; thread t owns the contiguous chunk [t*CH, t*CH + CH) with CH odd, so that a warp's
+  // chunk reads fall in distinct banks.
+  __syncthreads();
 #pragma unroll
   for (int j = 0; j < kRcEpt; ++j) {
     const int li = j * kRcThreads + tid;
     if (li < Lc) s_D[li] = r[j];
   }
   __syncthreads();
-  constexpr int kWarps = kRcThreads / 32;
-  const int Ws = (Lc + kWarps - 1) / kWarps;
-  const int w0 = min(Lc, warp * Ws), w1 = min(Lc, w0 + Ws);
-  float lsum = 0.f;
-  for (int v = w0 + lane; v < w1; v += 32) lsum += s_D[v];
-  const double wsum = warp_sum_d((double)lsum);
-  if (lane == 0) s_wsum[warp] = wsum;
-  __syncthreads();
-  if (tid == 0) {
-    double cta = 0.0;
-    for (int w = 0; w < kWarps; ++w) cta += s_wsum[w];
-    for (int q = 0; q < kc; ++q) cl.map_shared_rank(&s_tot[0], q)[rank] = cta;
+  const int CH = ((Lc + kRcThreads - 1) / kRcThreads) | 1;
+  const int v0 = min(Lc, tid * CH), v1 = min(Lc, v0 + CH);
+  float csum = 0.f;
+  for (int v = v0; v < v1; ++v) csum += s_D[v];
+  double incl = (double)csum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
   }
+  if (lane == 31) s_dred[warp] = incl;
+  if (tid == 0) s_owner = -1;
+  __syncthreads();
+  double wpre = 0.0, cta = 0.0;
+  for (int w = 0; w < kRcThreads / 32; ++w) {
+    if (w < warp) wpre += s_dred[w];
+    cta += s_dred[w];
+  }
+  const double excl = wpre + incl - (double)csum;  // mass of this slice before the chunk
+  if (tid == 0)
+    for (int q = 0; q < kc; ++q) cl.map_shared_rank(&s_tot[0], q)[rank] = cta;
   cl.sync();
   double total = 0.0, pre = 0.0;
-  int owner_cta = -1;
+  for (int q = 0; q < kc; ++q) {
+    if (q == rank) pre = total;
+    total += s_tot[q];
+  }
   const float u2 = accept_uniform(p.seed, (uint32_t)b, (uint32_t)e, 1u);
+  const double target = (double)u2 * total;
+  const double band = (double)kMargin * total;
+  int owner_cta = -1;
   {
     double run = 0.0;
-    for (int q = 0; q < kc; ++q) run += s_tot[q];
-    total = run;
-    const double target = (double)u2 * total;
-    run = 0.0;
     for (int q = 0; q < kc; ++q) {  // last CTA with mass that starts at or below the target
-      if (q == rank) pre = run;
       if (s_tot[q] > 0.0 && run <= target) owner_cta = q;
       run += s_tot[q];
     }
   }
-  const double target = (double)u2 * total;
-  const double band = (double)kMargin * total;
   if (owner_cta == rank) {
-    int owner_warp = -1;
-    double wstart = 0.0, run = pre;
-    for (int w = 0; w < kWarps; ++w) {
-      if (s_wsum[w] > 0.0 && run <= target) { owner_warp = w; wstart = run; }
-      run += s_wsum[w];
-    }
-    if (warp == owner_warp) {
-      double acc = wstart, prev = wstart;
+    // owner: the last chunk with mass that starts at or below the target
+    if (csum > 0.f && pre + excl <= target) atomicMax(&s_owner, tid);
+    __syncthreads();
+    if (tid == s_owner) {
+      double acc = pre + excl, prev = acc;
       int found = -1, last_nz = -1;
-      for (int v0 = w0; v0 < w1; v0 += 32) {
-        const int v = v0 + lane;
-        const float val = (v < w1) ? s_D[v] : 0.f;
-        float incl = val;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
-        }
-        const double accl = acc + (double)incl;
-        const unsigned hit = __ballot_sync(0xffffffffu, v < w1 && accl > target);
-        const unsigned nz = __ballot_sync(0xffffffffu, val > 0.f);
-        if (hit) {
-          const int h = __ffs(hit) - 1;
-          found = base + v0 + h;
-          const double ah = __shfl_sync(0xffffffffu, accl, h);
-          const float vh = __shfl_sync(0xffffffffu, val, h);
-          prev = ah - (double)vh;
-          acc = ah;
-          break;
-        }
-        if (nz) last_nz = base + v0 + 31 - __clz(nz);
-        acc += (double)__shfl_sync(0xffffffffu, incl, 31);
+      for (int v = v0; v < v1; ++v) {
+        const float rv = s_D[v];
+        if (rv > 0.f) last_nz = v;
+        prev = acc;
+        acc += (double)rv;
+        if (acc > target) { found = v; break; }
       }
       if (found < 0) {
-        found = last_nz >= 0 ? last_nz : V - 1;
+        found = last_nz;
         prev = acc;
       }
-      if (lane == 0) {
-        const bool near = (target - prev < band) || (acc - target < band) || (target < band);
-        p.bonus[b] = found;
-        if (p.bonus_margin) p.bonus_margin[b] = near ? 1 : 0;
-      }
+      const bool near = (target - prev < band) || (acc - target < band) || (target < band);
+      p.bonus[b] = found >= 0 ? base + found : V - 1;
+      if (p.bonus_margin) p.bonus_margin[b] = near ? 1 : 0;
     }
   }
   if (rank == 0) {
