@@ -43,6 +43,9 @@ def _args():
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--mode", default="graph", choices=["graph", "direct"],
+                   help="graph: each step is one spec_round_launch of the captured round (default); "
+                        "direct: the three C-ABI calls per step")
     p.add_argument("--workload", type=int, default=WORKLOAD,
                    help="gen.configs workload id (the headline metric is quoted on the default)")
     return p.parse_args()
@@ -253,31 +256,61 @@ def run_native(a, rank, world, dist):
         raise RuntimeError("device status " + st.status_string(int(status.item())))
 
     K = a.steps
-    ev_s, ev_e = events(K), events(K)
-    ev_ab, ev_ae, ev_lb, ev_le = events(K), events(K), events(K), events(K)
+
+    def timed_direct(n):
+        """n steps of the three direct calls; per-step and per-kernel device times (ms)."""
+        ev_s, ev_e = events(n), events(n)
+        ev_ab, ev_ae, ev_lb, ev_le = events(n), events(n), events(n), events(n)
+        torch.cuda.synchronize()
+        for i in range(n):
+            l2_flush()
+            aa.timing_begin, aa.timing_end = ev_ab[i].cuda_event, ev_ae[i].cuda_event
+            va.timing_begin, va.timing_end = ev_lb[i].cuda_event, ev_le[i].cuda_event
+            ev_s[i].record(stream)
+            step()
+            ev_e[i].record(stream)
+        torch.cuda.synchronize()
+        aa.timing_begin = aa.timing_end = va.timing_begin = va.timing_end = None
+        return ([ev_s[i].elapsed_time(ev_e[i]) for i in range(n)], [ev_ab[i].elapsed_time(ev_ae[i]) for i in range(n)],
+                [ev_lb[i].elapsed_time(ev_le[i]) for i in range(n)])
+
+    def timed_graph(rnd, n):
+        """n steps, each one launch of the captured round."""
+        ev_s, ev_e = events(n), events(n)
+        torch.cuda.synchronize()
+        for i in range(n):
+            l2_flush()
+            ev_s[i].record(stream)
+            rnd.launch(stream)
+            ev_e[i].record(stream)
+        torch.cuda.synchronize()
+        return [ev_s[i].elapsed_time(ev_e[i]) for i in range(n)]
+
+    rnd = None
+    if a.mode == "graph":
+        rnd = st.Round(aa, va, ca, dev_status=status)
+        for _ in range(max(3, a.warmup)):
+            l2_flush()
+            rnd.launch(stream)
+        torch.cuda.synchronize()
+
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    for i in range(K):
-        l2_flush()
-        aa.timing_begin, aa.timing_end = ev_ab[i].cuda_event, ev_ae[i].cuda_event
-        va.timing_begin, va.timing_end = ev_lb[i].cuda_event, ev_le[i].cuda_event
-        ev_s[i].record(stream)
-        step()
-        ev_e[i].record(stream)
-    torch.cuda.synchronize()
+    # Per-kernel device times (the roofline's inputs) come from the direct calls, whose
+    # library-recorded events bracket the attention and LM-head kernels; events recorded inside
+    # a CUDA graph are not timable.  In graph mode the step time comes from the round's launches.
+    direct_ms, attn_ms, lm_ms = timed_direct(K)
+    step_ms = timed_graph(rnd, K) if rnd is not None else direct_ms
     clk = clocks.stop()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    aa.timing_begin = aa.timing_end = va.timing_begin = va.timing_end = None
-    step_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K)]
-    attn_ms = [ev_ab[i].elapsed_time(ev_ae[i]) for i in range(K)]
-    lm_ms = [ev_lb[i].elapsed_time(ev_le[i]) for i in range(K)]
     ms = statistics.fmean(step_ms)
+    other_ms = statistics.fmean(direct_ms) if rnd is not None else None
     if int(status.item()) != 0:
         raise RuntimeError("device status " + st.status_string(int(status.item())))
 
@@ -309,7 +342,10 @@ def run_native(a, rank, world, dist):
         for b in range(case.B):
             t["k"][b, :, Lp[b]:Lp[b] + n_tree].copy_(host["k_tree"][b], non_blocking=True)
             t["v"][b, :, Lp[b]:Lp[b] + n_tree].copy_(host["v_tree"][b], non_blocking=True)
-        step()
+        if rnd is not None:
+            rnd.launch(stream)
+        else:
+            step()
         for k in res_host:
             res_host[k].copy_(outs[k], non_blocking=True)
         nl_host.copy_(new_len, non_blocking=True)
@@ -331,7 +367,8 @@ def run_native(a, rank, world, dist):
     torch.cuda.synchronize()
     e2e_ms = statistics.fmean(es[i].elapsed_time(ee[i]) for i in range(KE))
 
-    ms, e2e_ms = aggregate_ranks([ms, e2e_ms], dist, dev)
+    ms, e2e_ms, other_agg = aggregate_ranks([ms, e2e_ms, other_ms or 0.0], dist, dev)
+    other_ms = other_agg if other_ms is not None else None
     if rank != 0:
         return None
 
@@ -354,7 +391,9 @@ def run_native(a, rank, world, dist):
         "config": {"workload": case.name, "batch": case.B, "prefix_len": [int(x) for x in case.prefix_len][:8],
                    "tree_nodes": int(case.n_nodes[0]), "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d,
                    "hidden": case.Hd, "vocab": case.V, "rule": case.rule, "eps": case.eps, "delta": case.delta,
-                   "parallelism": f"replicas x{world}", "l2": "flushed before every step (256 MB write, then read)"},
+                   "parallelism": f"replicas x{world}", "l2": "flushed before every step (256 MB write, then read)",
+                   "launch": ("one CUDA-graph launch of the captured round per step (spec_round_launch)"
+                              if rnd is not None else "three C-ABI calls per step")},
         "e2e": {"value": job_rate(world, w["nodes"], e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": K * _launches_per_step(case),
@@ -377,6 +416,9 @@ def run_native(a, rank, world, dist):
                           "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 sustained {tc_sus} TFLOP/s"},
         "clocks": clk,
     }
+    if other_ms is not None:
+        line["direct_calls"] = {"ms_per_step": other_ms, "value": job_rate(world, w["nodes"], other_ms),
+                                "note": "same workload, the three C-ABI calls per step instead of the graph"}
     if world == 1 and not a.no_cpu_baseline and a.workload == WORKLOAD:
         line["cpu_baseline"] = _cpu_baseline(case)
     return line

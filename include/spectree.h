@@ -23,9 +23,9 @@
  *   - KV cache layout [B][Hkv][L_cap][head_dim]: request b's prefix occupies slots
  *     [0, prefix_len[b]); tree node i occupies slot prefix_len[b] + i.
  *   - All array arguments are caller-owned, contiguous, row-major DEVICE memory with 16-byte
- *     aligned base addresses.  The library never allocates: scratch space is the caller's
- *     `workspace`, sized by the matching *_workspace() query.  It keeps no global state and
- *     every call may be issued from any host thread.
+ *     aligned base addresses.  The three calls never allocate: scratch space is the caller's
+ *     `workspace`, sized by the matching *_workspace() query, and every call may be issued from
+ *     any host thread.  (spec_round_create, below, has the driver build a CUDA graph.)
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
  *   - Errors found on the host (NULL pointer, unsupported size or dtype, short workspace) are
  *     returned before anything is launched.  Errors that depend on device data (a bad parent
@@ -225,6 +225,42 @@ spec_status spec_compact_kv(const spec_compact_args* args, int32_t* dev_status, 
 #define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
 spec_status spec_verify_accept_noalloc(const spec_verify_args* args, int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * One verification round as a single CUDA-graph launch.  (Deployment convenience: the pages
+ * describe the round's steps -- parallel tree verification, acceptance, keeping the accepted
+ * prefix -- not how they are launched.  At batch 1 the round is a handful of short kernels
+ * around the LM head, so per-call host work and launch gaps are a visible share of it.)
+ *
+ * spec_round_create captures, in this order, spec_tree_attention(attn, attn_workspace),
+ * spec_verify_accept(verify, verify_workspace) and spec_compact_kv(compact) into a CUDA graph
+ * and instantiates it.  Any of the three may be NULL to leave that call out; at least one must
+ * be given.
+ *   - Everything in the argument structs is frozen at creation: device pointers, shapes,
+ *     scalars (rule, temperature, eps, delta, seed), dev_status and the optional timing events.
+ *     The CONTENTS of the device buffers are read when the round runs, so a serving loop refills
+ *     q / hidden_states / tokens / parent / n_nodes / prefix_len / draft_probs / the caches in
+ *     place and launches again.  The argument structs themselves may be freed after creation.
+ *   - Host-side validation runs at creation: the status of the first call that rejects its
+ *     arguments is returned, and no round is made (*out = NULL).
+ *   - The workspaces and every buffer named in the arguments must stay allocated until
+ *     spec_round_destroy, and must not be used by other work that overlaps a running round.
+ *   - spec_round_launch enqueues the whole round on `stream` (one cudaGraphLaunch).  Device-side
+ *     errors reach dev_status exactly as for the individual calls.  Rounds of one spec_round
+ *     must not overlap each other on the GPU (they share the workspaces).
+ *   - Creation captures a private stream in thread-local mode; do not call it while the calling
+ *     thread is capturing another stream.
+ * Errors: SPEC_ERR_INVALID_ARGUMENT (no call given, or out == NULL / round == NULL),
+ * SPEC_ERR_CUDA (capture, instantiation or launch failed), or a captured call's host-side
+ * status.  spec_round_destroy(NULL) does nothing. */
+typedef struct spec_round spec_round;
+
+spec_status spec_round_create(const spec_attn_args* attn, void* attn_workspace, size_t attn_workspace_bytes,
+                              const spec_verify_args* verify, void* verify_workspace,
+                              size_t verify_workspace_bytes, const spec_compact_args* compact,
+                              int32_t* dev_status, spec_round** out);
+spec_status spec_round_launch(const spec_round* round, void* stream);
+void spec_round_destroy(spec_round* round);
 
 /* Static English description of a status code (never NULL). */
 const char* spec_status_string(spec_status status);

@@ -125,3 +125,24 @@ def test_rejection_vocabulary_slices(V):
     # at large V the bonus draw always lands within the margin band of its neighbours; the path
     # itself must still have been compared exactly for some request
     assert sum(not ref[b]["path_margins"] for b in range(case.B)) >= 1
+
+
+@pytest.mark.parametrize("rule", ["greedy", "typical", "rejection"])
+def test_up_to_64_rows_vocab_on_m(rule):
+    """At most 64 tree rows (bf16) take the vocabulary-on-M LM-head kernel: ragged trees with
+    padding rows, a root-only request and a vocabulary spread over every SM."""
+    d = H.dev()
+    rng = np.random.default_rng(100 + len(rule))
+    parents = [T.random_bfs_tree(rng, 21, 4)[0], T.chain_tree(7), np.array([-1], dtype=np.int32)]
+    case = make_case(dtype="bf16", Hq=4, Hkv=1, d=64, Hd=256, V=30011, prefix_len=[3] * 3, parents=parents,
+                     rule=rule, tau=0.0 if rule == "greedy" else 0.9, eps=0.09, delta=0.3, seed=5,
+                     tokens=("iid", 0.8, 0.5) if rule == "rejection" else ("rank", 0.95), rng=rng)
+    assert case.B * case.N <= 64
+    got = H.gpu_verify(case, H.to_device(case, d))
+    assert got["status"] == 0
+    ref = H.oracle_verify(case)
+    exact, excluded = H.check_verify(case, got, ref)
+    assert exact + excluded == case.B and exact >= 1
+    H.check_row_stats(case, got, _rows(case))
+    pad = [(b, i) for b in range(case.B) for i in range(case.n_nodes[b], case.N)]
+    assert all(got["row_argmax"][b, i] == -1 for b, i in pad)

@@ -94,6 +94,12 @@ def test_host_argument_errors_return_before_launch(L):
     assert L.spec_verify_accept(ctypes.byref(v), None, 0, None, None) == 1           # tau must be > 0
     c = st.CompactArgs(dtype=0, batch=1, num_kv_heads=1, head_dim=64, kv_capacity=8, path_cap=0)
     assert L.spec_compact_kv(ctypes.byref(c), None, None) == 1                        # path_cap 0
+    handle = ctypes.c_void_p(123)
+    assert L.spec_round_create(None, None, 0, None, None, 0, None, None, ctypes.byref(handle)) == 1
+    assert handle.value is None                                                       # no call given
+    assert L.spec_round_create(None, None, 0, None, None, 0, None, None, None) == 1   # out == NULL
+    assert L.spec_round_launch(None, None) == 1
+    L.spec_round_destroy(None)
 
 
 def test_workspace_queries_are_host_only(L):

@@ -80,6 +80,14 @@ def lib():
         L.spec_verify_accept_workspace.restype = ctypes.c_size_t
         L.spec_status_string.argtypes = [ctypes.c_int32]
         L.spec_status_string.restype = ctypes.c_char_p
+        L.spec_round_create.argtypes = [ctypes.POINTER(AttnArgs), _vp, ctypes.c_size_t, ctypes.POINTER(VerifyArgs),
+                                        _vp, ctypes.c_size_t, ctypes.POINTER(CompactArgs), _vp,
+                                        ctypes.POINTER(_vp)]
+        L.spec_round_create.restype = ctypes.c_int32
+        L.spec_round_launch.argtypes = [_vp, _vp]
+        L.spec_round_launch.restype = ctypes.c_int32
+        L.spec_round_destroy.argtypes = [_vp]
+        L.spec_round_destroy.restype = None
         _lib_handle = L
     return _lib_handle
 
@@ -313,3 +321,51 @@ def verify_accept_noalloc(hidden, weight, tokens, parent, n_nodes, rule, tempera
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+class Round:
+    """One verification round (spec_round_create): tree attention, LM head + acceptance and KV
+    compaction captured into a CUDA graph and enqueued with one launch.
+
+    Each of ``attn``, ``verify``, ``compact`` is an argument struct from ``attn_args`` /
+    ``verify_args`` / ``compact_args`` (or None to leave that call out).  Every pointer and scalar
+    in them is frozen into the graph; refill the tensors they point at in place between
+    launches.  The workspaces are allocated here and kept, with the structs' tensors, for the
+    round's lifetime.
+    """
+
+    def __init__(self, attn=None, verify=None, compact=None, dev_status=None, keep=()):
+        torch = _torch()
+        L = lib()
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self._keep = list(keep)
+        need_a = L.spec_tree_attention_workspace(ctypes.byref(attn)) if attn is not None else 0
+        need_v = L.spec_verify_accept_workspace(ctypes.byref(verify)) if verify is not None else 0
+        self.ws_attn = torch.empty(max(need_a, 1), dtype=torch.uint8, device=dev)
+        self.ws_verify = torch.empty(max(need_v, 1), dtype=torch.uint8, device=dev)
+        self.status = _status_buffer(dev_status, dev)
+        self._args = (attn, verify, compact)
+        handle = _vp()
+        code = L.spec_round_create(ctypes.byref(attn) if attn is not None else None, _ptr(self.ws_attn), need_a,
+                                   ctypes.byref(verify) if verify is not None else None, _ptr(self.ws_verify),
+                                   need_v, ctypes.byref(compact) if compact is not None else None,
+                                   _ptr(self.status), ctypes.byref(handle))
+        _check(code, "spec_round_create")
+        self._handle = handle
+
+    def launch(self, stream=None):
+        """Enqueue the whole round on ``stream`` (default: the current torch stream)."""
+        if self._handle is None:
+            raise RuntimeError("round destroyed")
+        _check(lib().spec_round_launch(self._handle, _stream(stream)), "spec_round_launch")
+
+    def close(self):
+        if getattr(self, "_handle", None) is not None:
+            lib().spec_round_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

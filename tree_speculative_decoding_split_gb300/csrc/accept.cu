@@ -843,6 +843,8 @@ const ClusterOccupancy& cluster_occupancy() {
 
 }  // namespace
 
+void prepare_rejection_launch() { cluster_occupancy(); }
+
 // Cluster size: the smallest that fits the vocabulary in registers, widened (up to 8) while
 // every request still gets a co-resident cluster and each CTA keeps >= 1024 entries.
 int rejection_cluster_size(int B, int V, const int* max_clusters) {

@@ -56,18 +56,37 @@ __global__ void __launch_bounds__(256) attn_merge_bf16_kernel(const AttnParams p
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  for (int s = 0; s < p.n_split; ++s) {
-    const float ws = __shfl_sync(0xffffffffu, w, s);
-    if (ws > 0.f) {
-      const float* src = p.part_o + (orow * p.n_split + s) * D + lane * EPL;
-      if constexpr (EPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
+  // Partials are loaded in batches of 8 whatever their weight (a split that saw no key of this
+  // row holds stale values, which a zero weight selects away), so the loads overlap.
+  constexpr int kBatch = 8;
+  for (int s0 = 0; s0 < p.n_split; s0 += kBatch) {
+    float v[kBatch][EPL];
+    float ws[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int s = s0 + k;
+      ws[k] = __shfl_sync(0xffffffffu, w, s & 31);
+      if (s < p.n_split) {
+        const float* src = p.part_o + (orow * p.n_split + s) * D + lane * EPL;
+        if constexpr (EPL == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+          v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+        } else {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+          v[k][0] = t.x; v[k][1] = t.y;
+        }
       } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += ws * v.x; acc[1] += ws * v.y;
+        ws[k] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) v[k][e] = 0.f;
       }
     }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      if (ws[k] > 0.f) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(ws[k], v[k][e], acc[e]);
+      }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll

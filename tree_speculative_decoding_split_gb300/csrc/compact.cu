@@ -3,15 +3,18 @@
 // Candidates after a rejection are discarded and the accepted prefix is kept (qiita
 // "EAGLE-3とMedusaで実装するSpeculative Decoding実践ガイド", section "棄却サンプリング").  The
 // accepted path's K/V rows are gathered from their tree slots L + path[j] to L + j, in place.
-// One CTA per (request, KV head); the row copies go in increasing j with a barrier between
-// rows.  That order is hazard-free: path[j] >= j for a root path in topological order, so the
-// only destination slot a later row can read from (L + path[j'] = L + j with j > j') belongs
-// to a row that is written after row j' has been read.
+// One CTA per (request, KV head); rows are copied in batches of up to 64 that are read whole
+// into shared memory before any of them is written, batches in increasing j.  That order is
+// hazard-free: path[j] >= j for a root path in topological order, so a row's source slot
+// L + path[j'] can only be the destination L + j of a row j >= j', i.e. of a row in the same
+// batch (written after the whole batch was read) or in a later batch.
 
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace spectree {
+
+constexpr int kCompactBufChunks = 2048;  // 32 KB of staged rows (64 bf16 rows of d = 128, K and V)
 
 __global__ void __launch_bounds__(128) compact_kv_kernel(
     uint8_t* __restrict__ k, uint8_t* __restrict__ v, int row_bytes, const int32_t* __restrict__ prefix_len,
@@ -22,6 +25,8 @@ __global__ void __launch_bounds__(128) compact_kv_kernel(
   const int len = accept_len[b];
   const int32_t* pth = path + (size_t)b * path_cap;
   __shared__ int s_err;
+  __shared__ uint4 s_buf[kCompactBufChunks];
+  __shared__ int s_pth[kCompactBufChunks / 8];
   if (tid == 0) {
     int err = 0;
     if (len < 0 || len >= path_cap || L < 0 || pth[0] != 0) {
@@ -45,18 +50,29 @@ __global__ void __launch_bounds__(128) compact_kv_kernel(
     }
     return;
   }
-  const int chunks = row_bytes / 16;
+  const int chunks = row_bytes / 16;       // 16-byte pieces of one K (or V) row
+  const int per_row = 2 * chunks;            // K and V
+  const int batch = kCompactBufChunks / per_row;
   const size_t head_off = ((size_t)b * Hkv + g) * (size_t)L_cap;
-  for (int j = 1; j <= len; ++j) {
-    const size_t src = head_off + (size_t)(L + pth[j]);
-    const size_t dst = head_off + (size_t)(L + j);
-    if (src != dst) {
-      for (int c = tid; c < 2 * chunks; c += blockDim.x) {
-        uint8_t* base = (c < chunks) ? k : v;
-        const int cc = (c < chunks) ? c : c - chunks;
-        const uint4 val = *reinterpret_cast<const uint4*>(base + src * row_bytes + cc * 16);
-        *reinterpret_cast<uint4*>(base + dst * row_bytes + cc * 16) = val;
-      }
+  for (int j0 = 1; j0 <= len; j0 += batch) {
+    const int nb = min(batch, len + 1 - j0);
+    if (tid < nb) s_pth[tid] = pth[j0 + tid];
+    __syncthreads();
+    for (int i = tid; i < nb * per_row; i += blockDim.x) {
+      const int jj = i / per_row, c = i - jj * per_row;
+      const uint8_t* base = (c < chunks) ? k : v;
+      const int cc = (c < chunks) ? c : c - chunks;
+      const size_t src = head_off + (size_t)(L + s_pth[jj]);
+      s_buf[i] = *reinterpret_cast<const uint4*>(base + src * row_bytes + cc * 16);
+    }
+    __syncthreads();
+    for (int i = tid; i < nb * per_row; i += blockDim.x) {
+      const int jj = i / per_row, c = i - jj * per_row;
+      if (s_pth[jj] == j0 + jj) continue;  // already in place
+      uint8_t* base = (c < chunks) ? k : v;
+      const int cc = (c < chunks) ? c : c - chunks;
+      const size_t dst = head_off + (size_t)(L + j0 + jj);
+      *reinterpret_cast<uint4*>(base + dst * row_bytes + cc * 16) = s_buf[i];
     }
     __syncthreads();
   }

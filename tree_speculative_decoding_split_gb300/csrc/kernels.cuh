@@ -119,6 +119,9 @@ void launch_build_inverse_map(const int32_t* map, int Vd, int V, int32_t* inv, i
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
 // True when the rejection walk runs on a thread-block cluster (R held on chip, no R buffer).
 bool rejection_uses_cluster(int V);
+// Sets up the rejection walk's per-device launch state (shared-memory attribute, cluster
+// occupancy) ahead of a stream capture.
+void prepare_rejection_launch();
 
 // ---- K4: KV compaction ----------------------------------------------------------------------
 void launch_compact_kv(void* k, void* v, int elem_bytes, const int32_t* prefix_len,
