@@ -416,12 +416,58 @@ def run_native(a, rank, world, dist):
                           "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 sustained {tc_sus} TFLOP/s"},
         "clocks": clk,
     }
+    if a.workload == WORKLOAD and world == 1:
+        line["next_rows"] = {"medusa_expand": _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm)}
     if other_ms is not None:
         line["direct_calls"] = {"ms_per_step": other_ms, "value": job_rate(world, w["nodes"], other_ms),
                                 "note": "same workload, the three C-ABI calls per step instead of the graph"}
     if world == 1 and not a.no_cpu_baseline and a.workload == WORKLOAD:
         line["cpu_baseline"] = _cpu_baseline(case)
     return line
+
+
+def _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm):
+    """Static Medusa expansion at the workload's shapes: B requests, 5 heads of bf16 logits over
+    the vocabulary, the workload's 63-node topology from per-head top-(3, 3, 2, 2, 1)."""
+    import numpy as np
+    import torch
+    from gen import bf16 as BF
+    topk_heads = (3, 3, 2, 2, 1)
+    parent, rank = st.medusa_topology(topk_heads, int(case.n_nodes.max()))
+    rng = np.random.default_rng(5)
+    x = BF.f32_to_bf16_bits(rng.standard_normal((case.B, len(topk_heads), case.V)).astype(np.float32))
+    logits = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    tp, tr = torch.from_numpy(parent).to(dev), torch.from_numpy(rank).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ma, outs = st.medusa_args(logits, tp, tr, max(topk_heads))
+    need = L.spec_medusa_expand_workspace(ctypes.byref(ma))
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    pw, pst, sp = ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(stream.cuda_stream)
+
+    def call():
+        if L.spec_medusa_expand(ctypes.byref(ma), pw, need, pst, sp):
+            raise RuntimeError("spec_medusa_expand failed")
+
+    for _ in range(3):
+        l2_flush()
+        call()
+    n = min(K, 500)
+    es, ee = events(n), events(n)
+    torch.cuda.synchronize()
+    for i in range(n):
+        l2_flush()
+        es[i].record(stream)
+        call()
+        ee[i].record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status " + st.status_string(int(status.item())))
+    ms = statistics.fmean(es[i].elapsed_time(ee[i]) for i in range(n))
+    nbytes = logits.numel() * 2
+    return {"ms": ms, "steps": n, "bound": "hbm", "bytes": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
+            "frac": nbytes / (ms * 1e-3) / 1e9 / hbm, "launches_per_call": 2,
+            "shape": {"batch": case.B, "heads": len(topk_heads), "vocab": case.V, "topk": list(topk_heads),
+                      "nodes": int(len(parent)), "dtype": "bf16"}}
 
 
 # ---- oracle (CPU baseline / reference arm) ------------------------------------------------------

@@ -15,6 +15,9 @@
  *       section "棄却サンプリング") -- and the longest accepted root path plus a bonus token.
  *   spec_compact_kv      Keeps the accepted path's K/V entries right after the prefix (qiita,
  *       section "棄却サンプリング": everything after a rejection is discarded).
+ *   spec_medusa_expand   Builds the draft tree the verification consumes from the top-k of
+ *       every Medusa head along a static topology (jisaku glossary "Medusa", section
+ *       "ツリー構造の候補構築").
  *
  * Conventions shared by every call
  *   - Node 0 of a tree is its root (the last accepted token); parent[0] = -1 and
@@ -225,6 +228,56 @@ spec_status spec_compact_kv(const spec_compact_args* args, int32_t* dev_status, 
 #define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
 spec_status spec_verify_accept_noalloc(const spec_verify_args* args, int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Static Medusa tree expansion (jisaku glossary "Medusa", section "ツリー構造の候補構築": the
+ * candidate tree combines the top candidates of every Medusa head -- head 0's top-3 x head 1's
+ * top-3 x head 2's top-2 gives 18 paths -- along a predefined topology of 63 / 127 / 255 nodes).
+ *
+ * Head j (0 <= j < K) predicts the token j + 1 steps ahead.  Its candidates are its top-k
+ * logits, best first, equal logits ordered by the lower token id (-0 = +0; NaN ranks below
+ * -inf).  A topology node i >= 1 at depth d(i) (edges from the root) with rank r(i) carries
+ * head d(i) - 1's candidate r(i):
+ *   tokens[b][i] = topk(head_logits[b][d(i) - 1])[r(i)],   tokens[b][0] = root_token[b] (or 0)
+ * and parent_out[b][i] = topo_parent[i], so the outputs feed spec_verify_accept directly.
+ * The topology is shared by every request: topo_parent[0] = -1, 0 <= topo_parent[i] < i,
+ * 1 <= d(i) <= K and 0 <= topo_rank[i] < topk for i >= 1; a topology that breaks this sets
+ * SPEC_ERR_BAD_TREE and writes tokens 0.  (spec_medusa_topology builds the pruned Cartesian
+ * topology on the host.)
+ * Host errors: SPEC_ERR_INVALID_ARGUMENT (sizes < 1, NULL logits / topology / tokens, topk > V,
+ * unaligned logits), SPEC_ERR_UNSUPPORTED (K > 16, topk > 32, N > 255, or
+ * V > 4096 * floor(2048 / topk)), SPEC_ERR_WORKSPACE_TOO_SMALL. */
+typedef struct spec_medusa_args {
+  int32_t dtype;              /* head logits: SPEC_DTYPE_F32 or SPEC_DTYPE_BF16 */
+  int32_t batch;              /* B */
+  int32_t num_heads;          /* K, 1..16 */
+  int32_t vocab;              /* V */
+  int32_t n_nodes;            /* N, topology nodes including the root, 1..255 */
+  int32_t topk;               /* candidates per head, 1..32 */
+  const void* head_logits;    /* [B][K][V] */
+  const int32_t* topo_parent; /* [N] */
+  const int32_t* topo_rank;   /* [N] (entry 0 unused) */
+  const int32_t* root_token;  /* [B] or NULL */
+  int32_t* tokens;            /* out [B][N] */
+  int32_t* parent_out;        /* out [B][N] or NULL */
+  int32_t* n_nodes_out;       /* out [B] (all N) or NULL */
+  int32_t* topk_index;        /* out [B][K][topk] or NULL: every head's candidates, best first */
+} spec_medusa_args;
+
+size_t spec_medusa_expand_workspace(const spec_medusa_args* args);
+spec_status spec_medusa_expand(const spec_medusa_args* args, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream);
+
+/* Host-side helper (no GPU): the Cartesian topology of per-head candidate counts topk[0..K-1],
+ * pruned to n_nodes nodes.  Nodes are rank tuples (r_0, ..., r_{d-1}), r_j < topk[j]; the kept
+ * ones are the first n_nodes - 1 in the order (sum of ranks, depth, tuple), which keeps every
+ * prefix of a kept tuple; they are numbered breadth-first (depth, then tuple) after the root, so
+ * siblings are contiguous and ordered by rank.  Writes HOST arrays parent[n_nodes] and
+ * rank[n_nodes] (rank[0] = 0).  SPEC_ERR_INVALID_ARGUMENT for K < 1, a count < 1, n_nodes < 1 or
+ * beyond 1 + the number of tuples, or NULL outputs; SPEC_ERR_UNSUPPORTED beyond 255 nodes or
+ * 16 heads. */
+spec_status spec_medusa_topology(const int32_t* topk, int32_t num_heads, int32_t n_nodes, int32_t* parent,
+                                 int32_t* rank);
 
 /* ---------------------------------------------------------------------------------------
  * One verification round as a single CUDA-graph launch.  (Deployment convenience: the pages

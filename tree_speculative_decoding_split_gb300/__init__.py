@@ -8,6 +8,9 @@ runs in the library's CUDA kernels; if the library has not been built, every cal
     tree_attention(...)   -> (out, lse)          one attention layer over the draft tree
     verify_accept(...)    -> dict of outputs      LM head, acceptance, longest path, bonus token
     compact_kv(...)       -> (src_slot, new_len)  in-place KV compaction of the accepted path
+    medusa_expand(...)    -> dict of outputs      draft tree tokens from Medusa heads' top-k
+    medusa_topology(...)  -> (parent, rank)       pruned Cartesian topology (host arrays)
+    Round(...)                                    the three verification calls as one graph launch
 """
 
 import ctypes
@@ -57,6 +60,13 @@ class CompactArgs(ctypes.Structure):
                 ("path", _vp), ("accept_len", _vp), ("src_slot", _vp), ("new_len", _vp)]
 
 
+class MedusaArgs(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("n_nodes", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("head_logits", _vp), ("topo_parent", _vp), ("topo_rank", _vp), ("root_token", _vp),
+                ("tokens", _vp), ("parent_out", _vp), ("n_nodes_out", _vp), ("topk_index", _vp)]
+
+
 _lib_handle = None
 
 
@@ -88,6 +98,13 @@ def lib():
         L.spec_round_launch.restype = ctypes.c_int32
         L.spec_round_destroy.argtypes = [_vp]
         L.spec_round_destroy.restype = None
+        L.spec_medusa_expand_workspace.argtypes = [ctypes.POINTER(MedusaArgs)]
+        L.spec_medusa_expand_workspace.restype = ctypes.c_size_t
+        L.spec_medusa_expand.argtypes = [ctypes.POINTER(MedusaArgs), _vp, ctypes.c_size_t, _vp, _vp]
+        L.spec_medusa_expand.restype = ctypes.c_int32
+        _i32p = ctypes.POINTER(ctypes.c_int32)
+        L.spec_medusa_topology.argtypes = [_i32p, ctypes.c_int32, ctypes.c_int32, _i32p, _i32p]
+        L.spec_medusa_topology.restype = ctypes.c_int32
         _lib_handle = L
     return _lib_handle
 
@@ -369,3 +386,56 @@ class Round:
             self.close()
         except Exception:
             pass
+
+
+def medusa_topology(topk, n_nodes):
+    """(parent, rank) numpy int32 arrays of the Cartesian topology of per-head candidate counts
+    ``topk`` pruned to ``n_nodes`` nodes (spec_medusa_topology; host only)."""
+    import numpy as np
+    k = np.ascontiguousarray(np.asarray(topk, dtype=np.int32))
+    parent = np.zeros(int(n_nodes), dtype=np.int32)
+    rank = np.zeros(int(n_nodes), dtype=np.int32)
+    _i32p = ctypes.POINTER(ctypes.c_int32)
+    code = lib().spec_medusa_topology(k.ctypes.data_as(_i32p), len(k), int(n_nodes), parent.ctypes.data_as(_i32p),
+                                      rank.ctypes.data_as(_i32p))
+    _check(code, "spec_medusa_topology")
+    return parent, rank
+
+
+def medusa_args(head_logits, topo_parent, topo_rank, topk, root_token=None, outputs=None):
+    """Argument struct and output tensors of spec_medusa_expand.  head_logits [B][K][V] (fp32 or
+    bf16); topo_parent / topo_rank int32 [N] on the same device."""
+    torch = _torch()
+    _need(head_logits, "head_logits")
+    dev = head_logits.device
+    B, K, V = head_logits.shape
+    _need(topo_parent, "topo_parent", torch.int32, dev)
+    _need(topo_rank, "topo_rank", torch.int32, dev)
+    N = topo_parent.shape[0]
+    if root_token is not None:
+        _need(root_token, "root_token", torch.int32, dev)
+    if outputs is None:
+        outputs = {"tokens": torch.empty((B, N), dtype=torch.int32, device=dev),
+                   "parent": torch.empty((B, N), dtype=torch.int32, device=dev),
+                   "n_nodes": torch.empty(B, dtype=torch.int32, device=dev),
+                   "topk_index": torch.empty((B, K, int(topk)), dtype=torch.int32, device=dev)}
+    a = MedusaArgs(dtype=_dtype_code(head_logits), batch=B, num_heads=K, vocab=V, n_nodes=N, topk=int(topk),
+                   head_logits=_ptr(head_logits), topo_parent=_ptr(topo_parent), topo_rank=_ptr(topo_rank),
+                   root_token=_ptr(root_token), tokens=_ptr(outputs["tokens"]), parent_out=_ptr(outputs.get("parent")),
+                   n_nodes_out=_ptr(outputs.get("n_nodes")), topk_index=_ptr(outputs.get("topk_index")))
+    return a, outputs
+
+
+def medusa_expand(head_logits, topo_parent, topo_rank, topk, root_token=None, workspace=None, dev_status=None,
+                  stream=None, outputs=None):
+    """Static Medusa tree expansion (spec_medusa_expand).  Returns a dict of tensors: tokens
+    [B][N], parent [B][N], n_nodes [B], topk_index [B][K][topk]."""
+    a, outputs = medusa_args(head_logits, topo_parent, topo_rank, topk, root_token, outputs)
+    L = lib()
+    need = L.spec_medusa_expand_workspace(ctypes.byref(a))
+    if need == 0:
+        _check(L.spec_medusa_expand(ctypes.byref(a), None, 0, None, None), "spec_medusa_expand")
+    ws = _workspace(need, head_logits.device, workspace)
+    st = _status_buffer(dev_status, head_logits.device)
+    _check(L.spec_medusa_expand(ctypes.byref(a), _ptr(ws), need, _ptr(st), _stream(stream)), "spec_medusa_expand")
+    return outputs

@@ -123,6 +123,29 @@ bool rejection_uses_cluster(int V);
 // occupancy) ahead of a stream capture.
 void prepare_rejection_launch();
 
+// ---- K5: static Medusa tree expansion -------------------------------------------------------
+constexpr int kMaxHeads = 16;          // Medusa heads
+constexpr int kMaxTopk = 32;           // candidates per head
+constexpr int kMedusaMergeCands = 2048;  // chunk candidates per head the merge holds
+
+struct MedusaParams {
+  int B, K, V, N, k;
+  int is_bf16;
+  int n_chunks, chunk;                 // vocabulary chunks per head and their length
+  const void* logits;                  // [B][K][V]
+  const int32_t* topo_parent;          // [N]
+  const int32_t* topo_rank;            // [N]
+  const int32_t* root_token;           // [B] or nullptr
+  unsigned long long* cand;            // workspace [B*K][n_chunks][k] order keys
+  int32_t* tokens;                     // [B][N]
+  int32_t* parent_out;                 // [B][N] or nullptr
+  int32_t* n_nodes_out;                // [B] or nullptr
+  int32_t* topk_index;                 // [B][K][k] or nullptr
+  int32_t* dev_status;
+};
+int medusa_chunks(int B, int K, int V, int k, int num_sms);
+void launch_medusa(const MedusaParams& p, cudaStream_t stream);
+
 // ---- K4: KV compaction ----------------------------------------------------------------------
 void launch_compact_kv(void* k, void* v, int elem_bytes, const int32_t* prefix_len,
                        const int32_t* path, const int32_t* accept_len, int B, int Hkv, int d,
