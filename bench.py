@@ -416,8 +416,13 @@ def run_native(a, rank, world, dist):
                           "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 sustained {tc_sus} TFLOP/s"},
         "clocks": clk,
     }
-    if a.workload == WORKLOAD and world == 1:
-        line["next_rows"] = {"medusa_expand": _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm)}
+    if world == 1:
+        nxt = {}
+        if a.workload == WORKLOAD:
+            nxt["medusa_expand"] = _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm)
+        nxt["paged_attention"] = {f"block_{bs}": _bench_paged(st, L, dev, stream, l2_flush, events, K, case, t, w, hbm, tc,
+                                                              bs, attn_avg) for bs in (16, 64)}
+        line["next_rows"] = nxt
     if other_ms is not None:
         line["direct_calls"] = {"ms_per_step": other_ms, "value": job_rate(world, w["nodes"], other_ms),
                                 "note": "same workload, the three C-ABI calls per step instead of the graph"}
@@ -468,6 +473,54 @@ def _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm):
             "frac": nbytes / (ms * 1e-3) / 1e9 / hbm, "launches_per_call": 2,
             "shape": {"batch": case.B, "heads": len(topk_heads), "vocab": case.V, "topk": list(topk_heads),
                       "nodes": int(len(parent)), "dtype": "bf16"}}
+
+
+def _bench_paged(st, L, dev, stream, l2_flush, events, K, case, t, w, hbm, tc, bs, contiguous_ms):
+    """Tree attention of the workload with its KV cache scattered over a shuffled block pool."""
+    import torch
+    B, Hkv, L_cap, d = t["k"].shape
+    mb = (L_cap + bs - 1) // bs
+    nb = B * mb
+    g = torch.Generator(device="cpu").manual_seed(bs)
+    table = torch.randperm(nb, generator=g).reshape(B, mb).to(torch.int32).to(dev)
+
+    def pool_of(cache):
+        padded = torch.zeros((B, Hkv, mb * bs, d), dtype=cache.dtype, device=dev)
+        padded[:, :, :L_cap] = cache
+        blocks = padded.view(B, Hkv, mb, bs, d).permute(0, 2, 1, 3, 4).reshape(B * mb, Hkv, bs, d)
+        pool = torch.empty(blocks.shape, dtype=blocks.dtype, device=dev)
+        pool[table.reshape(-1).long()] = blocks
+        return pool
+
+    pk, pv = pool_of(t["k"]), pool_of(t["v"])
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    aa, out, lse = st.attn_args(t["q"], pk, pv, t["prefix_len"], t["n_nodes"], t["parent"], block_table=table)
+    need = L.spec_tree_attention_workspace(ctypes.byref(aa))
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    pw, pst, sp = ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(stream.cuda_stream)
+
+    def call():
+        if L.spec_tree_attention(ctypes.byref(aa), pw, need, pst, sp):
+            raise RuntimeError("spec_tree_attention (paged) failed")
+
+    for _ in range(3):
+        l2_flush()
+        call()
+    n = min(K, 300)
+    eb, ee = events(n), events(n)
+    torch.cuda.synchronize()
+    for i in range(n):
+        l2_flush()
+        aa.timing_begin, aa.timing_end = eb[i].cuda_event, ee[i].cuda_event
+        call()
+    torch.cuda.synchronize()
+    aa.timing_begin = aa.timing_end = None
+    if int(status.item()) != 0:
+        raise RuntimeError("device status " + st.status_string(int(status.item())))
+    ms = statistics.fmean(eb[i].elapsed_time(ee[i]) for i in range(n))
+    frac = max(w["attn_kernel_bytes"] / (hbm * 1e9), w["attn_flops"] / (tc * 1e12)) / (ms * 1e-3)
+    return {"kernel_ms": ms, "contiguous_kernel_ms": contiguous_ms, "roofline_frac": frac, "steps": n,
+            "pool_blocks": nb, "table_entries_per_request": mb}
 
 
 # ---- oracle (CPU baseline / reference arm) ------------------------------------------------------

@@ -101,6 +101,17 @@ typedef struct spec_attn_args {
   void* timing_begin;     /* optional cudaEvent_t recorded on `stream` right before the split-KV
                              attention kernel (bf16) or the fp32 attention kernel; NULL = none */
   void* timing_end;       /* optional cudaEvent_t recorded right after that kernel */
+  /* Paged KV cache (block_table != NULL; bf16 only).  k_cache / v_cache are then pools
+   * [num_blocks][Hkv][block_size][d], and request b's logical slot s (prefix at [0, L_b), tree
+   * node i at L_b + i, as above) is row s % block_size of block block_table[b][s / block_size].
+   * kv_capacity must equal max_blocks * block_size.  A table entry outside [0, num_blocks) among
+   * the blocks covering [0, L_b + n_b) sets SPEC_ERR_CAPACITY and zeroes that request's outputs
+   * (nothing outside the pools is read).  Blocks may be shared between requests (read only). */
+  const int32_t* block_table; /* [B][max_blocks], or NULL for the contiguous layout above */
+  int32_t block_size;     /* 16, 32, 64, 128 or 256 */
+  int32_t max_blocks;     /* table entries per request */
+  int32_t num_blocks;     /* blocks per pool; num_blocks * Hkv < 2^31 */
+  int32_t reserved1;      /* must be 0 */
 } spec_attn_args;
 
 /* Bytes of workspace spec_tree_attention needs for these shapes (0 on invalid args). */
@@ -197,8 +208,17 @@ typedef struct spec_compact_args {
   const int32_t* prefix_len;  /* [B] */
   const int32_t* path;        /* [B][path_cap] */
   const int32_t* accept_len;  /* [B] */
-  int32_t* src_slot;          /* out [B][path_cap] or NULL */
+  int32_t* src_slot;          /* out [B][path_cap] or NULL (logical slots) */
   int32_t* new_len;           /* out [B] or NULL */
+  /* Paged KV cache, as in spec_attn_args (either dtype): slots are logical, moved between the
+   * physical rows the table maps them to; a table entry outside [0, num_blocks) among the
+   * blocks the request's moves touch sets SPEC_ERR_CAPACITY and moves nothing for it.  Requests
+   * must not share the blocks that hold their tree slots. */
+  const int32_t* block_table; /* [B][max_blocks] or NULL */
+  int32_t block_size;         /* 16, 32, 64, 128 or 256 */
+  int32_t max_blocks;
+  int32_t num_blocks;
+  int32_t reserved1;          /* must be 0 */
 } spec_compact_args;
 
 spec_status spec_compact_kv(const spec_compact_args* args, int32_t* dev_status, void* stream);

@@ -38,7 +38,8 @@ class AttnArgs(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("kv_capacity", ctypes.c_int64), ("scale", ctypes.c_float),
                 ("reserved0", ctypes.c_int32), ("q", _vp), ("k_cache", _vp), ("v_cache", _vp),
                 ("prefix_len", _vp), ("n_nodes", _vp), ("parent", _vp), ("out", _vp), ("lse", _vp),
-                ("timing_begin", _vp), ("timing_end", _vp)]
+                ("timing_begin", _vp), ("timing_end", _vp), ("block_table", _vp), ("block_size", ctypes.c_int32),
+                ("max_blocks", ctypes.c_int32), ("num_blocks", ctypes.c_int32), ("reserved1", ctypes.c_int32)]
 
 
 class VerifyArgs(ctypes.Structure):
@@ -57,7 +58,9 @@ class CompactArgs(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("kv_capacity", ctypes.c_int64), ("path_cap", ctypes.c_int32),
                 ("reserved0", ctypes.c_int32), ("k_cache", _vp), ("v_cache", _vp), ("prefix_len", _vp),
-                ("path", _vp), ("accept_len", _vp), ("src_slot", _vp), ("new_len", _vp)]
+                ("path", _vp), ("accept_len", _vp), ("src_slot", _vp), ("new_len", _vp), ("block_table", _vp),
+                ("block_size", ctypes.c_int32), ("max_blocks", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("reserved1", ctypes.c_int32)]
 
 
 class MedusaArgs(ctypes.Structure):
@@ -181,8 +184,19 @@ def _status_buffer(dev_status, device):
     return dev_status
 
 
-def attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=None, scale=0.0):
-    """Build the C argument struct for tree attention (tensors are validated here)."""
+def _paged(k_cache, block_table, B, dev):
+    """(block_size, max_blocks, num_blocks, Hkv) of a paged pool [num_blocks][Hkv][block_size][d]."""
+    torch = _torch()
+    _need(block_table, "block_table", torch.int32, dev)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B][max_blocks]")
+    nb, Hkv, bs, _ = k_cache.shape
+    return bs, block_table.shape[1], nb, Hkv
+
+
+def attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=None, scale=0.0, block_table=None):
+    """Build the C argument struct for tree attention (tensors are validated here).  With
+    ``block_table`` [B][max_blocks] the caches are paged pools [num_blocks][Hkv][block_size][d]."""
     torch = _torch()
     _need(q, "q")
     dev = q.device
@@ -191,9 +205,17 @@ def attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=No
     for name, t in (("prefix_len", prefix_len), ("n_nodes", n_nodes), ("parent", parent)):
         _need(t, name, torch.int32, dev)
     B, N, Hq, d = q.shape
-    Hkv, L_cap = k_cache.shape[1], k_cache.shape[2]
-    if k_cache.shape != (B, Hkv, L_cap, d) or v_cache.shape != k_cache.shape:
-        raise ValueError("cache shape must be [B][Hkv][L_cap][d]")
+    paged = (0, 0, 0)
+    if block_table is not None:
+        bs, mb, nb, Hkv = _paged(k_cache, block_table, B, dev)
+        L_cap = mb * bs
+        paged = (bs, mb, nb)
+        if v_cache.shape != k_cache.shape or k_cache.shape[3] != d:
+            raise ValueError("pools must be [num_blocks][Hkv][block_size][d]")
+    else:
+        Hkv, L_cap = k_cache.shape[1], k_cache.shape[2]
+        if k_cache.shape != (B, Hkv, L_cap, d) or v_cache.shape != k_cache.shape:
+            raise ValueError("cache shape must be [B][Hkv][L_cap][d]")
     if tuple(parent.shape) != (B, N) or prefix_len.numel() != B or n_nodes.numel() != B:
         raise ValueError("parent must be [B][N], prefix_len and n_nodes [B]")
     if out is None:
@@ -205,14 +227,15 @@ def attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=No
     a = AttnArgs(dtype=_dtype_code(q), batch=B, n_max=N, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
                  kv_capacity=L_cap, scale=float(scale), reserved0=0, q=_ptr(q), k_cache=_ptr(k_cache),
                  v_cache=_ptr(v_cache), prefix_len=_ptr(prefix_len), n_nodes=_ptr(n_nodes), parent=_ptr(parent),
-                 out=_ptr(out), lse=_ptr(lse))
+                 out=_ptr(out), lse=_ptr(lse), block_table=_ptr(block_table), block_size=paged[0],
+                 max_blocks=paged[1], num_blocks=paged[2], reserved1=0)
     return a, out, lse
 
 
 def tree_attention(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=None, scale=0.0,
-                   workspace=None, dev_status=None, stream=None):
+                   workspace=None, dev_status=None, stream=None, block_table=None):
     """Tree attention (see spec_tree_attention).  Returns (out, lse)."""
-    a, out, lse = attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out, lse, scale)
+    a, out, lse = attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out, lse, scale, block_table)
     L = lib()
     need = L.spec_tree_attention_workspace(ctypes.byref(a))
     if need == 0:
@@ -287,14 +310,22 @@ def verify_accept(hidden, weight, tokens, parent, n_nodes, rule, temperature=0.0
     return outputs
 
 
-def compact_args(k_cache, v_cache, prefix_len, path, accept_len, src_slot=None, new_len=None):
+def compact_args(k_cache, v_cache, prefix_len, path, accept_len, src_slot=None, new_len=None, block_table=None):
     torch = _torch()
     _need(k_cache, "k_cache")
     dev = k_cache.device
     _need(v_cache, "v_cache", k_cache.dtype, dev)
     for name, t in (("prefix_len", prefix_len), ("path", path), ("accept_len", accept_len)):
         _need(t, name, torch.int32, dev)
-    B, Hkv, L_cap, d = k_cache.shape
+    B = prefix_len.numel()
+    paged = (0, 0, 0)
+    if block_table is not None:
+        bs, mb, nb, Hkv = _paged(k_cache, block_table, B, dev)
+        d = k_cache.shape[3]
+        L_cap = mb * bs
+        paged = (bs, mb, nb)
+    else:
+        B, Hkv, L_cap, d = k_cache.shape
     path_cap = path.shape[1]
     if src_slot is None:
         src_slot = torch.empty((B, path_cap), dtype=torch.int32, device=dev)
@@ -303,14 +334,16 @@ def compact_args(k_cache, v_cache, prefix_len, path, accept_len, src_slot=None, 
     a = CompactArgs(dtype=_dtype_code(k_cache), batch=B, num_kv_heads=Hkv, head_dim=d, kv_capacity=L_cap,
                     path_cap=path_cap, reserved0=0, k_cache=_ptr(k_cache), v_cache=_ptr(v_cache),
                     prefix_len=_ptr(prefix_len), path=_ptr(path), accept_len=_ptr(accept_len),
-                    src_slot=_ptr(src_slot), new_len=_ptr(new_len))
+                    src_slot=_ptr(src_slot), new_len=_ptr(new_len), block_table=_ptr(block_table),
+                    block_size=paged[0], max_blocks=paged[1], num_blocks=paged[2], reserved1=0)
     return a, src_slot, new_len
 
 
 def compact_kv(k_cache, v_cache, prefix_len, path, accept_len, src_slot=None, new_len=None, dev_status=None,
-               stream=None):
+               stream=None, block_table=None):
     """In-place KV compaction (see spec_compact_kv).  Returns (src_slot, new_len)."""
-    a, src_slot, new_len = compact_args(k_cache, v_cache, prefix_len, path, accept_len, src_slot, new_len)
+    a, src_slot, new_len = compact_args(k_cache, v_cache, prefix_len, path, accept_len, src_slot, new_len,
+                                        block_table)
     st = _status_buffer(dev_status, k_cache.device)
     _check(lib().spec_compact_kv(ctypes.byref(a), _ptr(st), _stream(stream)), "spec_compact_kv")
     return src_slot, new_len

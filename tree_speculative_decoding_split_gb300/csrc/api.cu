@@ -75,6 +75,22 @@ void record(void* event, cudaStream_t stream) {
 
 // ---- attention ------------------------------------------------------------------------------
 
+// Paged KV: block size a power of two in [16, 256], kv_capacity = max_blocks * block_size, and
+// pool coordinates that fit the tensor map.
+spec_status check_paged(int bs, int max_blocks, int num_blocks, int Hkv, long long L_cap) {
+  if (bs != 16 && bs != 32 && bs != 64 && bs != 128 && bs != 256) return SPEC_ERR_UNSUPPORTED;
+  if (max_blocks < 1 || num_blocks < 1) return SPEC_ERR_INVALID_ARGUMENT;
+  if ((long long)max_blocks * bs != L_cap) return SPEC_ERR_INVALID_ARGUMENT;
+  if ((long long)num_blocks * Hkv >= 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+  return SPEC_OK;
+}
+
+int log2_of(int x) {
+  int s = 0;
+  while ((1 << s) < x) ++s;
+  return s;
+}
+
 spec_status check_attn(const spec_attn_args* a) {
   if (!a) return SPEC_ERR_INVALID_ARGUMENT;
   if (a->dtype != SPEC_DTYPE_F32 && a->dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
@@ -90,6 +106,12 @@ spec_status check_attn(const spec_attn_args* a) {
     return SPEC_ERR_INVALID_ARGUMENT;
   if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->out))
     return SPEC_ERR_INVALID_ARGUMENT;
+  if (a->reserved1 != 0) return SPEC_ERR_INVALID_ARGUMENT;
+  if (a->block_table) {
+    if (a->dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
+    const spec_status ps = check_paged(a->block_size, a->max_blocks, a->num_blocks, a->num_kv_heads, a->kv_capacity);
+    if (ps != SPEC_OK) return ps;
+  }
   return SPEC_OK;
 }
 
@@ -208,6 +230,11 @@ spec_status check_compact(const spec_compact_args* a) {
   if (!a->k_cache || !a->v_cache || !a->prefix_len || !a->path || !a->accept_len) return SPEC_ERR_INVALID_ARGUMENT;
   if (!aligned16(a->k_cache) || !aligned16(a->v_cache)) return SPEC_ERR_INVALID_ARGUMENT;
   if ((long long)a->batch * a->num_kv_heads > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+  if (a->reserved1 != 0) return SPEC_ERR_INVALID_ARGUMENT;
+  if (a->block_table) {
+    const spec_status ps = check_paged(a->block_size, a->max_blocks, a->num_blocks, a->num_kv_heads, a->kv_capacity);
+    if (ps != SPEC_OK) return ps;
+  }
   return SPEC_OK;
 }
 
@@ -255,6 +282,14 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
   p.scale = a->scale > 0.f ? a->scale : 1.f / std::sqrt((float)d);
   p.scale_log2 = p.scale * 1.4426950408889634f;
   p.dev_status = dev_status;
+  if (a->block_table) {
+    p.table = a->block_table;
+    p.bs = a->block_size;
+    p.bs_shift = log2_of(a->block_size);
+    p.max_blocks = a->max_blocks;
+    p.num_blocks = a->num_blocks;
+    p.req_bad = l.bad;
+  }
   if (a->dtype == SPEC_DTYPE_F32) {
     p.k32 = static_cast<const float*>(a->k_cache);
     p.v32 = static_cast<const float*>(a->v_cache);
@@ -263,9 +298,14 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
     record(a->timing_end, stream);
   } else {
     CUtensorMap tmK, tmV;
-    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)a->kv_capacity, (cuuint64_t)B * Hkv};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)a->kv_capacity * d * 2};
-    const cuuint32_t box[3] = {64, 64, 1};
+    // contiguous: (d, L_cap, B*Hkv), 64-slot boxes; paged pools: (d, block, num_blocks*Hkv),
+    // boxes of min(block, 64) slots
+    const bool paged = a->block_table != nullptr;
+    const long long rows = paged ? a->block_size : a->kv_capacity;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows,
+                                paged ? (cuuint64_t)a->num_blocks * Hkv : (cuuint64_t)B * Hkv};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)(paged && a->block_size < 64 ? a->block_size : 64), 1};
     if (!make_map_bf16(&tmK, a->k_cache, 3, dims, strides, box) ||
         !make_map_bf16(&tmV, a->v_cache, 3, dims, strides, box))
       return SPEC_ERR_CUDA;
@@ -360,9 +400,17 @@ spec_status spec_compact_kv(const spec_compact_args* a, int32_t* dev_status, voi
   spec_status st = check_compact(a);
   if (st != SPEC_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  PagedKV pg = {};
+  if (a->block_table) {
+    pg.table = a->block_table;
+    pg.bs = a->block_size;
+    pg.bs_shift = log2_of(a->block_size);
+    pg.max_blocks = a->max_blocks;
+    pg.num_blocks = a->num_blocks;
+  }
   launch_compact_kv(a->k_cache, a->v_cache, a->dtype == SPEC_DTYPE_BF16 ? 2 : 4, a->prefix_len, a->path,
                     a->accept_len, a->batch, a->num_kv_heads, a->head_dim, a->kv_capacity, a->path_cap, a->src_slot,
-                    a->new_len, dev_status, stream);
+                    a->new_len, dev_status, pg, stream);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(256) attn_merge_bf16_kernel(const AttnParams p
   const int i = (int)((orow / p.Hq) % p.N);
   const int n = p.n_nodes[b];
   const long long L = p.prefix_len[b];
-  bool zero = n < 1 || n > p.N || i >= n || L < 0 || L + n > p.L_cap;
+  bool zero = n < 1 || n > p.N || i >= n || L < 0 || L + n > p.L_cap || (p.table && p.req_bad[b]);
   if (!zero) {
     bool bad = false;
     for (int c = lane; c < n; c += 32) {

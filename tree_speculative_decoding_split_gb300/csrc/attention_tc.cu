@@ -35,6 +35,7 @@ constexpr int kKT = 64;          // keys per tile (MMA N of S, K of P V)
 constexpr int kStages = 3;       // K/V ring depth
 constexpr int kGR = 128;         // rows per group (MMA M)
 constexpr float kRescaleLog2 = 8.f;
+constexpr int kMaxBlkCta = 1040;  // paged KV: block-table entries a CTA stages in shared memory
 
 template <int D, int NG>
 struct AttnTcCfg {
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_jmp[kMaxNodes];
   __shared__ uint32_t s_nanc[kMaxNodes][kAncWords];
+  __shared__ int s_blk[kMaxBlkCta];
 
   const int rg = blockIdx.x, split = blockIdx.y, bg = blockIdx.z;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
@@ -136,7 +138,25 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     kb = L;
     ke = L + n;
   }
-  const int T = ke > kb ? (int)((ke - kb + kKT - 1) / kKT) : 0;
+  // Paged KV: tiles start on 64-key boundaries of the logical slots (so that a tile never
+  // straddles a block of >= 64 slots, and a block of fewer slots fills whole 16-row groups of
+  // the swizzled tile); keys below kb are masked.  Contiguous: tiles start at kb.
+  const bool paged = p.table != nullptr;
+  const long long t0 = paged ? (kb & ~(long long)(kKT - 1)) : kb;
+  if (paged && tail) {  // every tail CTA of the request checks its whole table (same verdict)
+    const long long used = (L + n + p.bs - 1) >> p.bs_shift;
+    int badt = 0;
+    for (long long j = tid; j < used; j += kTcThreads) {
+      const int blk = p.table[(size_t)b * p.max_blocks + j];
+      if (blk < 0 || blk >= p.num_blocks) badt = 1;
+    }
+    badt = __syncthreads_or(badt);
+    if (tid == 0) {
+      p.req_bad[b] = badt;
+      if (badt && rg == 0 && g == 0) set_status(p.dev_status, SPEC_ERR_CAPACITY);
+    }
+  }
+  const int T = ke > kb ? (int)((ke - t0 + kKT - 1) / kKT) : 0;
   if (T == 0) {  // no keys here: the merge skips this split
     for (int rr = tid; rr < kRowsCta; rr += kTcThreads) {
       if (row0 + rr >= rows_total) break;
@@ -208,6 +228,15 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     const int grp = rr / kGR;
     *reinterpret_cast<uint4*>(sQ + grp * C::kQ + sw128_off(rr % kGR, ch, kGR)) = val;
   }
+  // paged: this CTA's block-table entries (-1 beyond the table), staged for the producer
+  const int blk0 = paged ? (int)(t0 >> p.bs_shift) : 0;
+  const int nblk = paged ? (int)(((t0 + (long long)T * kKT - 1) >> p.bs_shift) - blk0 + 1) : 0;
+  const bool tbl_staged = nblk <= kMaxBlkCta;
+  if (paged && tbl_staged)
+    for (int j = tid; j < nblk; j += kTcThreads) {
+      const int lb = blk0 + j;
+      s_blk[j] = lb < p.max_blocks ? p.table[(size_t)b * p.max_blocks + lb] : -1;
+    }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -246,12 +275,37 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
           ok = false;
           break;
         }
-        const int key = (int)(kb + (long long)t * kKT);
+        const long long key = t0 + (long long)t * kKT;
         mbar_arrive_expect_tx(&full[st], 2 * C::kTile);
+        if (!paged) {
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128, &tmK, &full[st], c * 64, key, bg);
-          tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128, &tmV, &full[st], c * 64, key, bg);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128, &tmK, &full[st], c * 64, (int)key, bg);
+            tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128, &tmV, &full[st], c * 64, (int)key, bg);
+          }
+        } else {
+          // boxes of min(bs, 64) rows; a slot beyond the table, or an entry out of range, reads
+          // from outside the pool map (zero fill)
+          const int rows = p.bs < kKT ? p.bs : kKT;
+          const long long zlim = (long long)p.num_blocks * p.Hkv;
+          for (int i = 0; i < kKT / rows; ++i) {
+            const long long pos = key + (long long)i * rows;
+            int y = 0, z = (int)zlim;
+            if (pos < p.L_cap) {
+              const int lb = (int)(pos >> p.bs_shift);
+              const int blk = tbl_staged ? s_blk[lb - blk0] : p.table[(size_t)b * p.max_blocks + lb];
+              const long long zz = (long long)blk * p.Hkv + g;
+              if (blk >= 0 && zz < zlim) {
+                y = (int)(pos & (p.bs - 1));
+                z = (int)zz;
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmK, &full[st], c * 64, y, z);
+              tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmV, &full[st], c * 64, y, z);
+            }
+          }
         }
         s_issued = t + 1;
       }
@@ -352,12 +406,12 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         v[j] = __uint_as_float(s0[j]);
         v[j + 32] = __uint_as_float(s1[j]);
       }
-      const long long kbase = kb + (long long)t * kKT;
-      if (tail || kbase + kKT > ke) {
+      const long long kbase = t0 + (long long)t * kKT;
+      if (tail || kbase + kKT > ke || kbase < kb) {
 #pragma unroll
         for (int j = 0; j < kKT; ++j) {
           const long long kidx = kbase + j;
-          bool keep = kidx < ke;
+          bool keep = kidx >= kb && kidx < ke;
           if (tail && keep) {
             const int jj = (int)(kidx - kb);
             keep = (anc[jj >> 5] >> (jj & 31)) & 1u;

@@ -3,6 +3,8 @@
 // Candidates after a rejection are discarded and the accepted prefix is kept (qiita
 // "EAGLE-3とMedusaで実装するSpeculative Decoding実践ガイド", section "棄却サンプリング").  The
 // accepted path's K/V rows are gathered from their tree slots L + path[j] to L + j, in place.
+// Paged caches map each logical slot through the request's block table (the moves are the
+// same, between physical rows).
 // One CTA per (request, KV head); rows are copied in batches of up to 64 that are read whole
 // into shared memory before any of them is written, batches in increasing j.  That order is
 // hazard-free: path[j] >= j for a root path in topological order, so a row's source slot
@@ -19,7 +21,8 @@ constexpr int kCompactBufChunks = 2048;  // 32 KB of staged rows (64 bf16 rows o
 __global__ void __launch_bounds__(128) compact_kv_kernel(
     uint8_t* __restrict__ k, uint8_t* __restrict__ v, int row_bytes, const int32_t* __restrict__ prefix_len,
     const int32_t* __restrict__ path, const int32_t* __restrict__ accept_len, int Hkv, long long L_cap,
-    int path_cap, int32_t* __restrict__ src_slot, int32_t* __restrict__ new_len, int32_t* dev_status) {
+    int path_cap, int32_t* __restrict__ src_slot, int32_t* __restrict__ new_len, int32_t* dev_status,
+    const PagedKV pg) {
   const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv, tid = threadIdx.x;
   const long long L = prefix_len[b];
   const int len = accept_len[b];
@@ -35,6 +38,11 @@ __global__ void __launch_bounds__(128) compact_kv_kernel(
       for (int j = 1; j <= len; ++j)
         if (pth[j] <= pth[j - 1]) { err = SPEC_ERR_BAD_TREE; break; }
       if (!err && L + pth[len] >= L_cap) err = SPEC_ERR_CAPACITY;
+      if (!err && pg.table)  // every block the moves touch: slots [L, L + path[len]]
+        for (long long lb = L >> pg.bs_shift; lb <= (L + pth[len]) >> pg.bs_shift; ++lb) {
+          const int blk = pg.table[(size_t)b * pg.max_blocks + lb];
+          if (blk < 0 || blk >= pg.num_blocks) { err = SPEC_ERR_CAPACITY; break; }
+        }
     }
     s_err = err;
   }
@@ -54,6 +62,12 @@ __global__ void __launch_bounds__(128) compact_kv_kernel(
   const int per_row = 2 * chunks;            // K and V
   const int batch = kCompactBufChunks / per_row;
   const size_t head_off = ((size_t)b * Hkv + g) * (size_t)L_cap;
+  // row index of logical slot s of this (request, KV head) in the cache, or in the paged pool
+  auto phys = [&](long long s) -> size_t {
+    if (!pg.table) return head_off + (size_t)s;
+    const int blk = pg.table[(size_t)b * pg.max_blocks + (s >> pg.bs_shift)];
+    return ((size_t)blk * Hkv + g) * (size_t)pg.bs + (size_t)(s & (pg.bs - 1));
+  };
   for (int j0 = 1; j0 <= len; j0 += batch) {
     const int nb = min(batch, len + 1 - j0);
     if (tid < nb) s_pth[tid] = pth[j0 + tid];
@@ -62,7 +76,7 @@ __global__ void __launch_bounds__(128) compact_kv_kernel(
       const int jj = i / per_row, c = i - jj * per_row;
       const uint8_t* base = (c < chunks) ? k : v;
       const int cc = (c < chunks) ? c : c - chunks;
-      const size_t src = head_off + (size_t)(L + s_pth[jj]);
+      const size_t src = phys(L + s_pth[jj]);
       s_buf[i] = *reinterpret_cast<const uint4*>(base + src * row_bytes + cc * 16);
     }
     __syncthreads();
@@ -71,7 +85,7 @@ __global__ void __launch_bounds__(128) compact_kv_kernel(
       if (s_pth[jj] == j0 + jj) continue;  // already in place
       uint8_t* base = (c < chunks) ? k : v;
       const int cc = (c < chunks) ? c : c - chunks;
-      const size_t dst = head_off + (size_t)(L + j0 + jj);
+      const size_t dst = phys(L + j0 + jj);
       *reinterpret_cast<uint4*>(base + dst * row_bytes + cc * 16) = s_buf[i];
     }
     __syncthreads();
@@ -87,10 +101,10 @@ __global__ void __launch_bounds__(128) compact_kv_kernel(
 void launch_compact_kv(void* k, void* v, int elem_bytes, const int32_t* prefix_len,
                        const int32_t* path, const int32_t* accept_len, int B, int Hkv, int d,
                        long long L_cap, int path_cap, int32_t* src_slot, int32_t* new_len,
-                       int32_t* dev_status, cudaStream_t stream) {
+                       int32_t* dev_status, const PagedKV& pg, cudaStream_t stream) {
   compact_kv_kernel<<<B * Hkv, 128, 0, stream>>>(static_cast<uint8_t*>(k), static_cast<uint8_t*>(v),
                                                 d * elem_bytes, prefix_len, path, accept_len, Hkv,
-                                                L_cap, path_cap, src_slot, new_len, dev_status);
+                                                L_cap, path_cap, src_slot, new_len, dev_status, pg);
 }
 
 }  // namespace spectree

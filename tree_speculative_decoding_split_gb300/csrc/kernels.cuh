@@ -40,6 +40,10 @@ struct AttnParams {
   float scale;
   float scale_log2;
   int32_t* dev_status;
+  // paged KV (bf16): pools [num_blocks][Hkv][bs][d]; table [B][max_blocks]; nullptr = contiguous
+  const int32_t* table;
+  int bs, bs_shift, max_blocks, num_blocks;
+  int32_t* req_bad;  // [B] written by the tail CTAs: the request's table has an entry out of range
 };
 
 struct AttnPlan {
@@ -147,9 +151,13 @@ int medusa_chunks(int B, int K, int V, int k, int num_sms);
 void launch_medusa(const MedusaParams& p, cudaStream_t stream);
 
 // ---- K4: KV compaction ----------------------------------------------------------------------
+struct PagedKV {
+  const int32_t* table;  // [B][max_blocks], nullptr = contiguous caches
+  int bs, bs_shift, max_blocks, num_blocks;
+};
 void launch_compact_kv(void* k, void* v, int elem_bytes, const int32_t* prefix_len,
                        const int32_t* path, const int32_t* accept_len, int B, int Hkv, int d,
                        long long L_cap, int path_cap, int32_t* src_slot, int32_t* new_len,
-                       int32_t* dev_status, cudaStream_t stream);
+                       int32_t* dev_status, const PagedKV& pg, cudaStream_t stream);
 
 }  // namespace spectree
