@@ -31,3 +31,4 @@ from .accept import verify_request, verify_accept, MARGIN  # noqa: F401
 from .compact import compact_kv  # noqa: F401
 from .medusa import head_topk, cartesian_tuples, pruned_topology, medusa_expand  # noqa: F401
 from .paged import gather_paged, scatter_paged  # noqa: F401
+from .eagle import expand_layer, select_tree  # noqa: F401
