@@ -420,6 +420,7 @@ def run_native(a, rank, world, dist):
         nxt = {}
         if a.workload == WORKLOAD:
             nxt["medusa_expand"] = _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm)
+        nxt["eagle_dynamic_tree"] = _bench_eagle(st, L, dev, stream, l2_flush, events, K, case)
         nxt["paged_attention"] = {f"block_{bs}": _bench_paged(st, L, dev, stream, l2_flush, events, K, case, t, w, hbm, tc,
                                                               bs, attn_avg) for bs in (16, 64)}
         line["next_rows"] = nxt
@@ -473,6 +474,55 @@ def _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm):
             "frac": nbytes / (ms * 1e-3) / 1e9 / hbm, "launches_per_call": 2,
             "shape": {"batch": case.B, "heads": len(topk_heads), "vocab": case.V, "topk": list(topk_heads),
                       "nodes": int(len(parent)), "dtype": "bf16"}}
+
+
+def _bench_eagle(st, L, dev, stream, l2_flush, events, K, case):
+    """Dynamic draft tree at the workload's batch: one expansion layer (frontier 8, top-8 over a
+    32000-entry draft vocabulary) and the selection of an N-node tree from 8 stacked layers."""
+    import numpy as np
+    import torch
+    B, F, k, Vd, D = case.B, 8, 8, 32000, 8
+    N = int(min(case.N, 255))
+    rng = np.random.default_rng(9)
+    z = rng.standard_normal((B, F, Vd)).astype(np.float32)
+    lp = torch.from_numpy(z - np.log(np.exp(z.astype(np.float64)).sum(-1, keepdims=True)).astype(np.float32)).to(dev)
+    fs = torch.from_numpy((-rng.exponential(2.0, (B, F))).astype(np.float32)).to(dev)
+    C = F * k
+    # stacked candidates as the expansion produces them: a child scores its parent's score plus
+    # a log-probability (<= 0)
+    Pn = rng.integers(0, C, (B, D, C)).astype(np.int32)
+    Sn = np.zeros((B, D, C), dtype=np.float32)
+    Sn[:, 0] = -rng.exponential(1.0, (B, C))
+    for l in range(1, D):
+        Sn[:, l] = np.take_along_axis(Sn[:, l - 1], Pn[:, l], axis=1) - rng.exponential(1.0, (B, C))
+    S = torch.from_numpy(Sn).to(dev)
+    Tk = torch.from_numpy(rng.integers(0, Vd, (B, D, C)).astype(np.int32)).to(dev)
+    P = torch.from_numpy(Pn).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def timed(call, n):
+        for _ in range(3):
+            l2_flush()
+            call()
+        es, ee = events(n), events(n)
+        torch.cuda.synchronize()
+        for i in range(n):
+            l2_flush()
+            es[i].record(stream)
+            call()
+            ee[i].record(stream)
+        torch.cuda.synchronize()
+        return statistics.fmean(es[i].elapsed_time(ee[i]) for i in range(n))
+
+    n = min(K, 300)
+    layer_ms = timed(lambda: st.eagle_expand(lp, fs, k, F, dev_status=status, stream=stream), n)
+    tree_ms = timed(lambda: st.eagle_tree(S, Tk, P, N, dev_status=status, stream=stream), n)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status " + st.status_string(int(status.item())))
+    return {"expand_layer_ms": layer_ms, "select_tree_ms": tree_ms, "steps": n,
+            "shape": {"batch": B, "frontier": F, "topk": k, "draft_vocab": Vd, "layers": D, "nodes": N},
+            "note": "timed through the Python binding (argument marshalling included)"}
 
 
 def _bench_paged(st, L, dev, stream, l2_flush, events, K, case, t, w, hbm, tc, bs, contiguous_ms):

@@ -18,6 +18,8 @@
  *   spec_medusa_expand   Builds the draft tree the verification consumes from the top-k of
  *       every Medusa head along a static topology (jisaku glossary "Medusa", section
  *       "ツリー構造の候補構築").
+ *   spec_eagle_expand / spec_eagle_tree  Build a dynamic draft tree layer by layer from the
+ *       draft model's log-probabilities, EAGLE-2 style (tech-tldr, section "ツリー検証").
  *
  * Conventions shared by every call
  *   - Node 0 of a tree is its root (the last accepted token); parent[0] = -1 and
@@ -298,6 +300,79 @@ spec_status spec_medusa_expand(const spec_medusa_args* args, void* workspace, si
  * 16 heads. */
 spec_status spec_medusa_topology(const int32_t* topk, int32_t num_heads, int32_t n_nodes, int32_t* parent,
                                  int32_t* rank);
+
+/* ---------------------------------------------------------------------------------------
+ * Dynamic (context-aware) draft tree, layer by layer, in the EAGLE-2 manner (tech-tldr
+ * "多トークン予測（Medusa・EAGLE）", section "ツリー検証": EAGLE-2's dynamic tree shapes the tree
+ * by the context's confidence; jisaku glossary "Medusa", section "EAGLE: Medusaの発展形").  A
+ * node's value is the cumulative log-probability of its path under the draft model.  The draft
+ * model itself runs between the layers, outside this library.
+ *
+ * spec_eagle_expand, one layer: frontier node f of request b (F per request) proposes its topk
+ * best draft tokens by logp[b][f][:] (equal log-probabilities by the lower token id).  Candidate
+ * c = f * topk + r gets token = the r-th token, score = frontier_score[b][f] + logp (one float32
+ * addition), parent = frontier_cand[b][f] (-1 when frontier_cand is NULL); a frontier row with
+ * frontier_valid 0 gives token -1, score -inf, parent -1.  The next frontier is the next_k best
+ * candidates (score, then lower c), -1 / -inf padded; candidates with score -inf or NaN are
+ * never chosen.  Candidate rows of request b start at element b * cand_stride (0 = F * topk), so
+ * a caller can write every layer into one [B][layers][cands] array.
+ * Host errors: SPEC_ERR_INVALID_ARGUMENT (sizes, NULL pointers, topk > draft_vocab,
+ * cand_stride < F * topk), SPEC_ERR_UNSUPPORTED (F > 32, topk > 16, F * topk > 256, next_k >
+ * F * topk, draft_vocab > 4096 * floor(256 / topk)), SPEC_ERR_WORKSPACE_TOO_SMALL. */
+typedef struct spec_eagle_expand_args {
+  int32_t batch;                  /* B */
+  int32_t frontier;               /* F */
+  int32_t draft_vocab;            /* Vd */
+  int32_t topk;                   /* children per frontier node */
+  int32_t next_k;                 /* frontier size of the next layer */
+  int32_t reserved0;              /* must be 0 */
+  int64_t cand_stride;            /* elements between requests' candidate rows; 0 = F * topk */
+  const float* logp;              /* [B][F][Vd] draft log-probabilities */
+  const float* frontier_score;    /* [B][F] */
+  const int32_t* frontier_valid;  /* [B][F] or NULL (all valid) */
+  const int32_t* frontier_cand;   /* [B][F] or NULL: each frontier node's candidate index in the previous layer */
+  int32_t* cand_token;            /* out [B][stride] */
+  float* cand_score;              /* out [B][stride] */
+  int32_t* cand_parent;           /* out [B][stride] */
+  int32_t* next_index;            /* out [B][next_k] candidate indices, best first */
+  float* next_score;              /* out [B][next_k] */
+} spec_eagle_expand_args;
+
+size_t spec_eagle_expand_workspace(const spec_eagle_expand_args* args);
+spec_status spec_eagle_expand(const spec_eagle_expand_args* args, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_status, void* stream);
+
+/* spec_eagle_tree: the draft tree of each request from all layers' candidates, stacked as
+ * [B][layers][cands] (candidate (l, j); on layer l > 0, parent = its candidate index on layer
+ * l - 1, -1 = absent; a score of -inf or NaN = absent).  The tree is the root plus the n_max - 1
+ * best present candidates (score, then lower (l, j)), numbered breadth-first by (l, j) after the
+ * root: tree_parent[0] = -1, tree_token[0] = root_token[b] (0 if NULL), tokens mapped through
+ * draft_to_target when given; padding nodes get parent -1, token 0; node_cand = l * cands + j
+ * (-1 for the root and padding).  Outputs feed spec_verify_accept (n_nodes, parent, tokens).
+ * Scores must not increase from a candidate to its child (true for cumulative log-probabilities);
+ * a kept candidate whose parent is not kept sets SPEC_ERR_BAD_TREE, a token outside
+ * [0, draft_vocab) with a map SPEC_ERR_BAD_TOKEN; either leaves the request a lone root.
+ * Host errors: SPEC_ERR_INVALID_ARGUMENT, SPEC_ERR_UNSUPPORTED (layers * cands > 2048,
+ * n_max > 255). */
+typedef struct spec_eagle_tree_args {
+  int32_t batch;
+  int32_t layers;                 /* D */
+  int32_t cands;                  /* C, candidates per layer */
+  int32_t n_max;                  /* N, tree nodes including the root */
+  int32_t draft_vocab;            /* Vd (range of tokens when draft_to_target is given) */
+  int32_t reserved0;              /* must be 0 */
+  const float* score;             /* [B][D][C] */
+  const int32_t* token;           /* [B][D][C] draft-vocabulary ids */
+  const int32_t* parent;          /* [B][D][C] */
+  const int32_t* draft_to_target; /* [Vd] or NULL */
+  const int32_t* root_token;      /* [B] or NULL */
+  int32_t* tree_parent;           /* out [B][N] */
+  int32_t* tree_token;            /* out [B][N] */
+  int32_t* n_nodes;               /* out [B] */
+  int32_t* node_cand;             /* out [B][N] or NULL */
+} spec_eagle_tree_args;
+
+spec_status spec_eagle_tree(const spec_eagle_tree_args* args, int32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------------
  * One verification round as a single CUDA-graph launch.  (Deployment convenience: the pages

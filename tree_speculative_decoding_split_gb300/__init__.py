@@ -10,6 +10,8 @@ runs in the library's CUDA kernels; if the library has not been built, every cal
     compact_kv(...)       -> (src_slot, new_len)  in-place KV compaction of the accepted path
     medusa_expand(...)    -> dict of outputs      draft tree tokens from Medusa heads' top-k
     medusa_topology(...)  -> (parent, rank)       pruned Cartesian topology (host arrays)
+    eagle_expand(...)     -> dict of outputs      one layer of a dynamic (EAGLE-2 style) draft tree
+    eagle_tree(...)       -> dict of outputs      the tree from all layers' candidates
     Round(...)                                    the three verification calls as one graph launch
 """
 
@@ -70,6 +72,21 @@ class MedusaArgs(ctypes.Structure):
                 ("tokens", _vp), ("parent_out", _vp), ("n_nodes_out", _vp), ("topk_index", _vp)]
 
 
+class EagleExpandArgs(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("frontier", ctypes.c_int32), ("draft_vocab", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("next_k", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("cand_stride", ctypes.c_int64), ("logp", _vp), ("frontier_score", _vp), ("frontier_valid", _vp),
+                ("frontier_cand", _vp), ("cand_token", _vp), ("cand_score", _vp), ("cand_parent", _vp),
+                ("next_index", _vp), ("next_score", _vp)]
+
+
+class EagleTreeArgs(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("layers", ctypes.c_int32), ("cands", ctypes.c_int32),
+                ("n_max", ctypes.c_int32), ("draft_vocab", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("score", _vp), ("token", _vp), ("parent", _vp), ("draft_to_target", _vp), ("root_token", _vp),
+                ("tree_parent", _vp), ("tree_token", _vp), ("n_nodes", _vp), ("node_cand", _vp)]
+
+
 _lib_handle = None
 
 
@@ -108,6 +125,12 @@ def lib():
         _i32p = ctypes.POINTER(ctypes.c_int32)
         L.spec_medusa_topology.argtypes = [_i32p, ctypes.c_int32, ctypes.c_int32, _i32p, _i32p]
         L.spec_medusa_topology.restype = ctypes.c_int32
+        L.spec_eagle_expand_workspace.argtypes = [ctypes.POINTER(EagleExpandArgs)]
+        L.spec_eagle_expand_workspace.restype = ctypes.c_size_t
+        L.spec_eagle_expand.argtypes = [ctypes.POINTER(EagleExpandArgs), _vp, ctypes.c_size_t, _vp, _vp]
+        L.spec_eagle_expand.restype = ctypes.c_int32
+        L.spec_eagle_tree.argtypes = [ctypes.POINTER(EagleTreeArgs), _vp, _vp]
+        L.spec_eagle_tree.restype = ctypes.c_int32
         _lib_handle = L
     return _lib_handle
 
@@ -472,3 +495,68 @@ def medusa_expand(head_logits, topo_parent, topo_rank, topk, root_token=None, wo
     st = _status_buffer(dev_status, head_logits.device)
     _check(L.spec_medusa_expand(ctypes.byref(a), _ptr(ws), need, _ptr(st), _stream(stream)), "spec_medusa_expand")
     return outputs
+
+
+def eagle_expand(logp, frontier_score, topk, next_k, frontier_valid=None, frontier_cand=None, outputs=None,
+                 cand_stride=0, workspace=None, dev_status=None, stream=None):
+    """One layer of the dynamic draft tree (spec_eagle_expand).  logp float32 [B][F][Vd];
+    frontier_score float32 [B][F].  ``outputs`` may pass views into stacked [B][layers][C]
+    buffers together with ``cand_stride``.  Returns a dict of tensors."""
+    torch = _torch()
+    _need(logp, "logp", torch.float32)
+    dev = logp.device
+    B, F, Vd = logp.shape
+    _need(frontier_score, "frontier_score", torch.float32, dev)
+    for name, t in (("frontier_valid", frontier_valid), ("frontier_cand", frontier_cand)):
+        if t is not None:
+            _need(t, name, torch.int32, dev)
+    C = F * int(topk)
+    if outputs is None:
+        outputs = {"token": torch.empty((B, C), dtype=torch.int32, device=dev),
+                   "score": torch.empty((B, C), dtype=torch.float32, device=dev),
+                   "parent": torch.empty((B, C), dtype=torch.int32, device=dev)}
+    outputs.setdefault("next_index", torch.empty((B, int(next_k)), dtype=torch.int32, device=dev))
+    outputs.setdefault("next_score", torch.empty((B, int(next_k)), dtype=torch.float32, device=dev))
+    a = EagleExpandArgs(batch=B, frontier=F, draft_vocab=Vd, topk=int(topk), next_k=int(next_k), reserved0=0,
+                        cand_stride=int(cand_stride), logp=_ptr(logp), frontier_score=_ptr(frontier_score),
+                        frontier_valid=_ptr(frontier_valid), frontier_cand=_ptr(frontier_cand),
+                        cand_token=_vp(outputs["token"].data_ptr()), cand_score=_vp(outputs["score"].data_ptr()),
+                        cand_parent=_vp(outputs["parent"].data_ptr()), next_index=_ptr(outputs["next_index"]),
+                        next_score=_ptr(outputs["next_score"]))
+    L = lib()
+    need = L.spec_eagle_expand_workspace(ctypes.byref(a))
+    if need == 0:
+        _check(L.spec_eagle_expand(ctypes.byref(a), None, 0, None, None), "spec_eagle_expand")
+    ws = _workspace(need, dev, workspace)
+    st = _status_buffer(dev_status, dev)
+    _check(L.spec_eagle_expand(ctypes.byref(a), _ptr(ws), need, _ptr(st), _stream(stream)), "spec_eagle_expand")
+    return outputs
+
+
+def eagle_tree(score, token, parent, n_max, draft_to_target=None, root_token=None, dev_status=None, stream=None):
+    """The draft tree from stacked candidates [B][layers][C] (spec_eagle_tree).  Returns a dict:
+    parent [B][N], tokens [B][N], n_nodes [B], node_cand [B][N]."""
+    torch = _torch()
+    _need(score, "score", torch.float32)
+    dev = score.device
+    B, D, C = score.shape
+    _need(token, "token", torch.int32, dev)
+    _need(parent, "parent", torch.int32, dev)
+    Vd = 0
+    if draft_to_target is not None:
+        _need(draft_to_target, "draft_to_target", torch.int32, dev)
+        Vd = draft_to_target.numel()
+    if root_token is not None:
+        _need(root_token, "root_token", torch.int32, dev)
+    N = int(n_max)
+    out = {"parent": torch.empty((B, N), dtype=torch.int32, device=dev),
+           "tokens": torch.empty((B, N), dtype=torch.int32, device=dev),
+           "n_nodes": torch.empty(B, dtype=torch.int32, device=dev),
+           "node_cand": torch.empty((B, N), dtype=torch.int32, device=dev)}
+    a = EagleTreeArgs(batch=B, layers=D, cands=C, n_max=N, draft_vocab=Vd, reserved0=0, score=_ptr(score),
+                      token=_ptr(token), parent=_ptr(parent), draft_to_target=_ptr(draft_to_target),
+                      root_token=_ptr(root_token), tree_parent=_ptr(out["parent"]), tree_token=_ptr(out["tokens"]),
+                      n_nodes=_ptr(out["n_nodes"]), node_cand=_ptr(out["node_cand"]))
+    st = _status_buffer(dev_status, dev)
+    _check(lib().spec_eagle_tree(ctypes.byref(a), _ptr(st), _stream(stream)), "spec_eagle_tree")
+    return out

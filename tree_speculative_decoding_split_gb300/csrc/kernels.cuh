@@ -149,6 +149,33 @@ struct MedusaParams {
 };
 int medusa_chunks(int B, int K, int V, int k, int num_sms);
 void launch_medusa(const MedusaParams& p, cudaStream_t stream);
+// K5a alone: per-row chunk top-k keys of p.logits [p.B * p.K][p.V] into p.cand.
+void launch_row_topk_chunks(const MedusaParams& p, cudaStream_t stream);
+
+// ---- K6: layered dynamic draft tree (EAGLE-2 reading) --------------------------------------
+constexpr int kEagleMaxCands = 2048;   // candidates of all layers per request (tree selection)
+
+struct EagleExpandParams {
+  int B, F, k, next_k, n_chunks;
+  size_t cand_stride;                  // elements between requests' candidate rows
+  const unsigned long long* chunk_keys;  // [B*F][n_chunks][k] from K5a
+  const float* frontier_score;         // [B][F]
+  const int32_t* frontier_valid;       // [B][F] or nullptr
+  const int32_t* frontier_cand;        // [B][F] or nullptr
+  int32_t* cand_token; float* cand_score; int32_t* cand_parent;  // [B][stride], F*k used
+  int32_t* next_index; float* next_score;                        // [B][next_k]
+};
+void launch_eagle_expand(const EagleExpandParams& p, const MedusaParams& chunks, cudaStream_t stream);
+
+struct EagleTreeParams {
+  int B, D, C, N, Vd;
+  const float* score; const int32_t* token; const int32_t* parent;  // [B][D][C]
+  const int32_t* d2t;                  // [Vd] or nullptr
+  const int32_t* root_token;           // [B] or nullptr
+  int32_t* tree_parent; int32_t* tree_token; int32_t* n_nodes; int32_t* node_cand;
+  int32_t* dev_status;
+};
+void launch_eagle_tree(const EagleTreeParams& p, cudaStream_t stream);
 
 // ---- K4: KV compaction ----------------------------------------------------------------------
 struct PagedKV {

@@ -172,6 +172,10 @@ int medusa_chunks(int B, int K, int V, int k, int num_sms) {
   return want < 1 ? 1 : want;
 }
 
+void launch_row_topk_chunks(const MedusaParams& p, cudaStream_t stream) {
+  medusa_chunk_topk_kernel<<<dim3(p.n_chunks, p.B * p.K), kMxThreads, 0, stream>>>(p);
+}
+
 void launch_medusa(const MedusaParams& p, cudaStream_t stream) {
   medusa_chunk_topk_kernel<<<dim3(p.n_chunks, p.B * p.K), kMxThreads, 0, stream>>>(p);
   medusa_expand_kernel<<<p.B, kMxThreads, 0, stream>>>(p);
