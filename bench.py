@@ -379,7 +379,9 @@ def run_native(a, rank, world, dist):
     lm_achieved = w["lm_kernel_bytes"] / (lm_avg * 1e-3) / 1e9
     lm_tflops = w["lm_flops"] / (lm_avg * 1e-3) / 1e12
     lm_tc_bound = w["lm_flops"] / (tc * 1e12) > w["lm_kernel_bytes"] / (hbm * 1e9)
-    traffic = _traffic_from_profile(os.path.join(ROOT, "tree_speculative_decoding_split_gb300", "csrc", "lmhead.cu"))
+    # the committed counters are for the benchmark workload's LM-head kernel only
+    traffic = (_traffic_from_profile(os.path.join(ROOT, "tree_speculative_decoding_split_gb300", "csrc", "lmhead.cu"))
+               if a.workload == WORKLOAD else None)
     step_bytes = w["kv_bytes"] + w["qo_bytes"] + w["w_bytes"] + w["h_bytes"] + w["logits_bytes"]
     t_hbm = step_bytes / (hbm * 1e9)
     t_tc = (w["lm_flops"] + w["attn_flops"]) / (tc_sus * 1e12)

@@ -98,12 +98,18 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Vocabulary-on-M kernel: four 64-element k atoms per pipeline stage, so that every W row is read
+// 512 contiguous bytes at a time (measured on the 63-row, 128256 x 4096 head: 177.4 us with one
+// atom and 8 stages, 174.6 us with two atoms and 4 stages, 173.4 us with four atoms and 2).
 template <int BN>
 struct LmCfg {
-  static constexpr int kStageA = kBM * kBK * 2;
-  static constexpr int kStageB = BN * kBK * 2;
+  static constexpr int kAtoms = 4;
+  static constexpr int kAtomA = kBM * kBK * 2;
+  static constexpr int kAtomB = BN * kBK * 2;
+  static constexpr int kStageA = kAtomA * kAtoms;
+  static constexpr int kStageB = kAtomB * kAtoms;
   static constexpr int kStage = kStageA + kStageB;
-  static constexpr int kStages = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int kStages = 2;
   static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   static constexpr int kEpiBytes = 5 * BN * (int)sizeof(float4) + 5 * BN * (int)sizeof(int);
   static constexpr int kSmem = 1024 + kStages * kStage + kEpiBytes + 256;
@@ -136,7 +142,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   __shared__ int s_epi_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_kb = p.Hd / kBK;
+  const int n_atoms = p.Hd / kBK;
+  const int n_kb = (n_atoms + C::kAtoms - 1) / C::kAtoms;  // stages per tile
   // CTA c owns row chunk nc = c % n_nc and vocabulary tiles slot, slot + cpc, ...
   const int nc = blockIdx.x % p.n_nc, slot = blockIdx.x / p.n_nc;
   if (blockIdx.x == 0 && threadIdx.x < 32)
@@ -181,9 +188,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[st], C::kStage);
-          tma_load_2d(sA + st * C::kStageA, &tmW, &full[st], kb * kBK, vt * kBM, pol_w);
-          tma_load_2d(sB + st * C::kStageB, &tmH, &full[st], kb * kBK, nc * BN, pol_h);
+          const int na = min(C::kAtoms, n_atoms - kb * C::kAtoms);
+          mbar_arrive_expect_tx(&full[st], na * (C::kAtomA + C::kAtomB));
+          for (int at = 0; at < na; ++at) {
+            const int x = (kb * C::kAtoms + at) * kBK;
+            tma_load_2d(sA + st * C::kStageA + at * C::kAtomA, &tmW, &full[st], x, vt * kBM, pol_w);
+            tma_load_2d(sB + st * C::kStageB + at * C::kAtomB, &tmH, &full[st], x, nc * BN, pol_h);
+          }
           s_issued = it + 1;
         }
       }
@@ -214,11 +225,14 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_sw128(smem_u32(sA + st * C::kStageA));
-          const uint64_t bd = sdesc_sw128(smem_u32(sB + st * C::kStageB));
+          const int na = min(C::kAtoms, n_atoms - kb * C::kAtoms);
+          for (int at = 0; at < na; ++at) {
+            const uint64_t ad = sdesc_sw128(smem_u32(sA + st * C::kStageA + at * C::kAtomA));
+            const uint64_t bd = sdesc_sw128(smem_u32(sB + st * C::kStageB + at * C::kAtomB));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | at | kk) != 0);
+          }
           umma_commit(&empty[st]);
           s_consumed = it + 1;
         }
