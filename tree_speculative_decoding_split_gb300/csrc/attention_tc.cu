@@ -214,20 +214,6 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       sAnc[c] = word;
     }
   }
-
-  // ---- Q rows -> shared memory in the K-major 128-byte-swizzle layout of the MMA A operand ----
-  constexpr int NCH = D / 8;
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-  for (int c = tid; c < kRowsCta * NCH; c += kTcThreads) {
-    const int rr = c / NCH, ch = c % NCH, row = row0 + rr;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (row < rows_total) {
-      const int i = row / p.G, j = row % p.G;
-      val = *reinterpret_cast<const uint4*>(q + (((size_t)b * p.N + i) * p.Hq + g * p.G + j) * D + ch * 8);
-    }
-    const int grp = rr / kGR;
-    *reinterpret_cast<uint4*>(sQ + grp * C::kQ + sw128_off(rr % kGR, ch, kGR)) = val;
-  }
   // paged: this CTA's block-table entries (-1 beyond the table), staged for the producer
   const int blk0 = paged ? (int)(t0 >> p.bs_shift) : 0;
   const int nblk = paged ? (int)(((t0 + (long long)T * kKT - 1) >> p.bs_shift) - blk0 + 1) : 0;
@@ -258,6 +244,77 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     tmem_alloc(&s_tmem, C::kTmemCols);
     tmem_relinquish();
   }
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, block-table entries staged
+  tc_fence_after();
+
+  // K/V tile t of this split -> ring stage t % kStages (the caller has made that stage free)
+  auto issue_tile = [&](int t) {
+    const int st = t % kStages;
+    const long long key = t0 + (long long)t * kKT;
+    mbar_arrive_expect_tx(&full[st], 2 * C::kTile);
+    if (!paged) {
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128, &tmK, &full[st], c * 64, (int)key, bg);
+        tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128, &tmV, &full[st], c * 64, (int)key, bg);
+      }
+    } else {
+      // boxes of min(bs, 64) rows; a slot beyond the table, or an entry out of range, reads
+      // from outside the pool map (zero fill)
+      const int rows = p.bs < kKT ? p.bs : kKT;
+      const long long zlim = (long long)p.num_blocks * p.Hkv;
+      for (int i = 0; i < kKT / rows; ++i) {
+        const long long pos = key + (long long)i * rows;
+        int y = 0, z = (int)zlim;
+        if (pos < p.L_cap) {
+          const int lb = (int)(pos >> p.bs_shift);
+          const int blk = tbl_staged ? s_blk[lb - blk0] : p.table[(size_t)b * p.max_blocks + lb];
+          const long long zz = (long long)blk * p.Hkv + g;
+          if (blk >= 0 && zz < zlim) {
+            y = (int)(pos & (p.bs - 1));
+            z = (int)zz;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmK, &full[st], c * 64, y, z);
+          tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmV, &full[st], c * 64, y, z);
+        }
+      }
+    }
+  };
+  // The first kStages tiles go out now (every stage starts free), so they load while Q is staged.
+  const int pre = T < kStages ? T : kStages;
+  if (warp == 0 && lane == 0) {
+    for (int t = 0; t < pre; ++t) issue_tile(t);
+    s_issued = pre;
+  }
+
+  // ---- Q rows -> shared memory in the K-major 128-byte-swizzle layout of the MMA A operand ----
+  // Every load of a thread is issued before its first store, so the loads overlap.
+  constexpr int NCH = D / 8;
+  constexpr int kQPer = (kRowsCta * NCH + kTcThreads - 1) / kTcThreads;
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+  uint4 qv[kQPer];
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int c = tid + k * kTcThreads;
+    const int rr = c / NCH, ch = c % NCH, row = row0 + rr;
+    qv[k] = make_uint4(0, 0, 0, 0);
+    if (c < kRowsCta * NCH && row < rows_total) {
+      const int i = row / p.G, j = row % p.G;
+      qv[k] = *reinterpret_cast<const uint4*>(q + (((size_t)b * p.N + i) * p.Hq + g * p.G + j) * D + ch * 8);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int c = tid + k * kTcThreads;
+    if (c < kRowsCta * NCH) {
+      const int rr = c / NCH, ch = c % NCH;
+      *reinterpret_cast<uint4*>(sQ + (rr / kGR) * C::kQ + sw128_off(rr % kGR, ch, kGR)) = qv[k];
+    }
+  }
   fence_proxy_async_smem();  // Q (generic stores) becomes visible to the tensor cores
   tc_fence_before();
   __syncthreads();
@@ -267,46 +324,15 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---- TMA producer ----
+      // ---- TMA producer (tiles pre .. T-1) ----
       bool ok = true;
-      for (int t = 0; t < T && ok; ++t) {
+      for (int t = pre; t < T && ok; ++t) {
         const int st = t % kStages;
         if (!mbar_wait_bounded(&empty[st], ((t / kStages) & 1) ^ 1, &s_abort)) {
           ok = false;
           break;
         }
-        const long long key = t0 + (long long)t * kKT;
-        mbar_arrive_expect_tx(&full[st], 2 * C::kTile);
-        if (!paged) {
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128, &tmK, &full[st], c * 64, (int)key, bg);
-            tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128, &tmV, &full[st], c * 64, (int)key, bg);
-          }
-        } else {
-          // boxes of min(bs, 64) rows; a slot beyond the table, or an entry out of range, reads
-          // from outside the pool map (zero fill)
-          const int rows = p.bs < kKT ? p.bs : kKT;
-          const long long zlim = (long long)p.num_blocks * p.Hkv;
-          for (int i = 0; i < kKT / rows; ++i) {
-            const long long pos = key + (long long)i * rows;
-            int y = 0, z = (int)zlim;
-            if (pos < p.L_cap) {
-              const int lb = (int)(pos >> p.bs_shift);
-              const int blk = tbl_staged ? s_blk[lb - blk0] : p.table[(size_t)b * p.max_blocks + lb];
-              const long long zz = (long long)blk * p.Hkv + g;
-              if (blk >= 0 && zz < zlim) {
-                y = (int)(pos & (p.bs - 1));
-                z = (int)zz;
-              }
-            }
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-              tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmK, &full[st], c * 64, y, z);
-              tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmV, &full[st], c * 64, y, z);
-            }
-          }
-        }
+        issue_tile(t);
         s_issued = t + 1;
       }
       if (!ok) {
@@ -383,9 +409,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     const uint32_t tO = tmem + kGroups * kKT + a * D + lane_off;
     uint8_t* prow = sP + a * C::kP;
     float m_run = -INFINITY, l_run = 0.f;
-    uint32_t anc[kAncWords];
-#pragma unroll
-    for (int w = 0; w < kAncWords; ++w) anc[w] = tail ? sAnc[rr * kAncWords + w] : 0u;
+    const uint32_t* anc = sAnc + rr * kAncWords;  // this row's ancestor words (tail split)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       if (!mbar_wait_bounded(&sfull[a], t & 1, &s_abort)) {
@@ -407,16 +431,27 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         v[j + 32] = __uint_as_float(s1[j]);
       }
       const long long kbase = t0 + (long long)t * kKT;
-      if (tail || kbase + kKT > ke || kbase < kb) {
+      if (tail) {
+        // key j of the tile is tree node kbase - kb + j; its ancestor bit comes from a 64-bit
+        // window of the row's ancestor words in shared memory (held in registers, the words
+        // would need a runtime index, which puts them in local memory); nodes outside [0, n)
+        // have no bit
+        const int off = (int)(kbase - kb);
+        const int lo = off >> 5;            // floor division (off may be negative when paged)
+        const int r = off - (lo << 5);      // 0..31
+        const uint32_t w0 = (lo >= 0 && lo < kAncWords) ? anc[lo] : 0u;
+        const uint32_t w1 = (lo + 1 >= 0 && lo + 1 < kAncWords) ? anc[lo + 1] : 0u;
+        const uint32_t w2 = (lo + 2 >= 0 && lo + 2 < kAncWords) ? anc[lo + 2] : 0u;
+        const unsigned long long win = ((unsigned long long)w1 << 32) | w0;
+        const unsigned long long mask = (win >> r) | (r ? ((unsigned long long)w2 << (64 - r)) : 0ull);
+#pragma unroll
+        for (int j = 0; j < kKT; ++j)
+          if (!((mask >> j) & 1ull)) v[j] = -INFINITY;
+      } else if (kbase + kKT > ke || kbase < kb) {
 #pragma unroll
         for (int j = 0; j < kKT; ++j) {
           const long long kidx = kbase + j;
-          bool keep = kidx >= kb && kidx < ke;
-          if (tail && keep) {
-            const int jj = (int)(kidx - kb);
-            keep = (anc[jj >> 5] >> (jj & 31)) & 1u;
-          }
-          if (!keep) v[j] = -INFINITY;
+          if (!(kidx >= kb && kidx < ke)) v[j] = -INFINITY;
         }
       }
       float mx[4] = {v[0], v[1], v[2], v[3]};
