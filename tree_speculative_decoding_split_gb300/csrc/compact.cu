@@ -27,30 +27,38 @@ __global__ void __launch_bounds__(128) compact_kv_kernel(
   const long long L = prefix_len[b];
   const int len = accept_len[b];
   const int32_t* pth = path + (size_t)b * path_cap;
-  __shared__ int s_err;
   __shared__ uint4 s_buf[kCompactBufChunks];
   __shared__ int s_pth[kCompactBufChunks / 8];
-  if (tid == 0) {
-    int err = 0;
-    if (len < 0 || len >= path_cap || L < 0 || pth[0] != 0) {
-      err = (len >= path_cap) ? SPEC_ERR_CAPACITY : SPEC_ERR_BAD_TREE;
-    } else {
-      for (int j = 1; j <= len; ++j)
-        if (pth[j] <= pth[j - 1]) { err = SPEC_ERR_BAD_TREE; break; }
-      if (!err && L + pth[len] >= L_cap) err = SPEC_ERR_CAPACITY;
-      if (!err && pg.table)  // every block the moves touch: slots [L, L + path[len]]
-        for (long long lb = L >> pg.bs_shift; lb <= (L + pth[len]) >> pg.bs_shift; ++lb) {
-          const int blk = pg.table[(size_t)b * pg.max_blocks + lb];
-          if (blk < 0 || blk >= pg.num_blocks) { err = SPEC_ERR_CAPACITY; break; }
-        }
+  // path checks, spread over the threads (every branch below depends on block-uniform values)
+  int err = 0;
+  if (len < 0 || len >= path_cap || L < 0) {
+    err = (len >= path_cap) ? SPEC_ERR_CAPACITY : SPEC_ERR_BAD_TREE;
+  } else {
+    int bad = 0;
+    for (int j = tid; j <= len; j += blockDim.x) {
+      const int pj = pth[j];
+      if (j == 0 ? pj != 0 : pj <= pth[j - 1]) bad = 1;
     }
-    s_err = err;
+    if (__syncthreads_or(bad)) {
+      err = SPEC_ERR_BAD_TREE;
+    } else {
+      const long long last = L + pth[len];
+      if (last >= L_cap) {
+        err = SPEC_ERR_CAPACITY;
+      } else if (pg.table) {  // every block the moves touch: slots [L, L + path[len]]
+        int badb = 0;
+        for (long long lb = (L >> pg.bs_shift) + tid; lb <= (last >> pg.bs_shift); lb += blockDim.x) {
+          const int blk = pg.table[(size_t)b * pg.max_blocks + lb];
+          if (blk < 0 || blk >= pg.num_blocks) badb = 1;
+        }
+        if (__syncthreads_or(badb)) err = SPEC_ERR_CAPACITY;
+      }
+    }
   }
-  __syncthreads();
-  if (s_err) {
+  if (err) {
     if (g == 0) {
       if (tid == 0) {
-        set_status(dev_status, s_err);
+        set_status(dev_status, err);
         if (new_len) new_len[b] = (int)L;
       }
       if (src_slot)
