@@ -41,7 +41,9 @@ template <int D, int NG>
 struct AttnTcCfg {
   static constexpr int kGroups = NG;            // 128-row groups per CTA
   static constexpr int kRowsCta = kGR * NG;
-  static constexpr int kThreads = 64 + 128 * NG;  // producer warp, MMA warp, 4 softmax warps per group
+  // producer warp, MMA warp (group 0), 4 softmax warps per group, and with two groups a second
+  // MMA warp that issues group 1's MMAs, so that neither group's issue waits on the other's
+  static constexpr int kThreads = 64 + 128 * NG + (NG > 1 ? 32 * (NG - 1) : 0);
   static constexpr int kQ = kGR * D * 2;        // Q bytes per group
   static constexpr int kTile = kKT * D * 2;     // K (or V) tile bytes
   static constexpr int kP = kGR * kKT * 2;      // P bytes per group
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kGroups);  // one P V commit per group's issuer
     }
     for (int a = 0; a < kGroups; ++a) {
       mbar_init(&sfull[a], 1);
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       mbar_init(&pfull[a], 4);
       mbar_init(&ofull[a], 1);
     }
-    mbar_init(drained, 1);
+    for (int a = 0; a < kGroups; ++a) mbar_init(&drained[a], 1);
     s_abort = 0;
     s_issued = 0;
     s_consumed = 0;
@@ -340,63 +342,60 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         set_status(p.dev_status, SPEC_ERR_TIMEOUT);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp >= 2 + 4 * kGroups) {
+    // ---- MMA issuers: group 0 on warp 1, group g > 0 on warp 1 + 4 * kGroups + g ----
+    const int ga = (warp == 1) ? 0 : warp - (1 + 4 * kGroups);
     if (lane == 0) {
-      // ---- MMA issuer: S_A(0) S_B(0), then per tile t: [P V]_A(t) S_A(t+1) [P V]_B(t) S_B(t+1) ----
       constexpr uint32_t idS = idesc_bf16_f32(kGR, kKT, 0);
       constexpr uint32_t idP = idesc_bf16_f32(kGR, D, 1);
       bool ok = true;
-      // Issue order: S_a(0) for every group, then per tile t: S_a(t + 1) for every group as soon as
-      // that group's softmax has read S_a(t) (early in its work on tile t, so the next scores are
-      // ready when it finishes), then P V_a(t) for every group as soon as P_a(t) is written.  K/V
-      // stage t is released after the last group's P V(t).  Waits suspend in the barrier.
-      auto issue_s = [&](int a, int t) -> bool {
+      // Issue order for the group: S(0), then per tile t: S(t + 1) as soon as the softmax has
+      // read S(t) (early in its work on tile t, so the next scores are ready when it finishes),
+      // then P V(t) as soon as P(t) is written.  K/V stage t is released once every group's
+      // issuer has committed its P V(t).  Waits suspend in the barrier.
+      auto issue_s = [&](int t) -> bool {
         const int st = t % kStages;
-        if (a == 0 && !mbar_wait_bounded(&full[st], (t / kStages) & 1, &s_abort)) return false;
-        if (t > 0 && !mbar_wait_bounded(&sfree[a], (t - 1) & 1, &s_abort)) return false;
+        if (!mbar_wait_bounded(&full[st], (t / kStages) & 1, &s_abort)) return false;
+        if (t > 0 && !mbar_wait_bounded(&sfree[ga], (t - 1) & 1, &s_abort)) return false;
         tc_fence_after();
-        const uint32_t qa = smem_u32(sQ + a * C::kQ), ka = smem_u32(sK + st * C::kTile);
+        const uint32_t qa = smem_u32(sQ + ga * C::kQ), ka = smem_u32(sK + st * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * (kGR * 128) + (kk & 3) * 32, 0, 1024);
           const uint64_t bd = sdesc_sw128(ka + (kk >> 2) * (kKT * 128) + (kk & 3) * 32, 0, 1024);
-          umma_bf16(tmem + a * kKT, ad, bd, idS, kk > 0);
+          umma_bf16(tmem + ga * kKT, ad, bd, idS, kk > 0);
         }
-        umma_commit(&sfull[a]);
+        umma_commit(&sfull[ga]);
         return true;
       };
-      auto issue_pv = [&](int a, int t) -> bool {
-        if (!mbar_wait_bounded(&pfull[a], t & 1, &s_abort)) return false;
+      auto issue_pv = [&](int t) -> bool {
+        if (!mbar_wait_bounded(&pfull[ga], t & 1, &s_abort)) return false;
         tc_fence_after();
-        const uint32_t pa = smem_u32(sP + a * C::kP), va = smem_u32(sV + (t % kStages) * C::kTile);
+        const uint32_t pa = smem_u32(sP + ga * C::kP), va = smem_u32(sV + (t % kStages) * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < kKT / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(pa + kk * 32, 0, 1024);
           const uint64_t bd = sdesc_sw128(va + kk * 16 * 128, kKT * 128, 1024);
-          umma_bf16(tmem + kGroups * kKT + a * D, ad, bd, idP, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16(tmem + kGroups * kKT + ga * D, ad, bd, idP, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&ofull[a]);
+        umma_commit(&ofull[ga]);
         return true;
       };
-#pragma unroll
-      for (int a = 0; a < kGroups; ++a) ok = ok && issue_s(a, 0);
+      ok = issue_s(0);
       for (int t = 0; t < T && ok; ++t) {
-        if (t + 1 < T) {
-#pragma unroll
-          for (int a = 0; a < kGroups; ++a) ok = ok && issue_s(a, t + 1);
-        }
-#pragma unroll
-        for (int a = 0; a < kGroups; ++a) ok = ok && issue_pv(a, t);
+        if (t + 1 < T) ok = issue_s(t + 1);
+        ok = ok && issue_pv(t);
         if (!ok) break;
-        umma_commit(&empty[t % kStages]);  // every group is done with K/V tile t
-        s_consumed = t + 1;
+        umma_commit(&empty[t % kStages]);  // this group is done with K/V tile t
+        if (ga == 0) s_consumed = t + 1;
       }
       if (!ok) {
         s_abort = 1;
         set_status(p.dev_status, SPEC_ERR_TIMEOUT);
       }
-      umma_commit(drained);
-      mbar_wait_bounded(drained, 0, nullptr);
+      // every MMA this thread issued has finished once drained[ga] completes
+      umma_commit(&drained[ga]);
+      mbar_wait_bounded(&drained[ga], 0, nullptr);
     }
   } else {
     // ---- softmax: warps 2..9; group a = (warp - 2) / 4, TMEM lane quarter q4 = warp % 4 ----
