@@ -26,6 +26,8 @@ def test_tiny_fp32_config():
     ([33], [127], 8, 2, 64),       # ragged tile edges
     ([255], [129], 4, 1, 128),     # maximum tree, 1020 rows per KV head
     ([10, 63, 1], [200, 0, 65], 16, 2, 128),  # ragged batch, padded nodes
+    ([40, 7], [70, 300], 12, 4, 128),  # G = 3: Q rows staged through registers (3 does not divide 128)
+    ([5], [100], 128, 1, 64),      # G = 128: one node per 128-row group
 ])
 def test_small_shapes(dtype, shape):
     d = H.dev()

@@ -59,7 +59,8 @@ bool make_map_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* 
                    const cuuint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  if (rank < 1 || rank > 5) return false;
   std::memset(m, 0, sizeof(*m));
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -251,7 +252,7 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
                                 int32_t* dev_status, void* stream_ptr) {
   spec_status st = check_attn(a);
   if (st != SPEC_OK) return st;
-  if (!workspace) return SPEC_ERR_INVALID_ARGUMENT;
+  if (!workspace || !aligned16(workspace)) return SPEC_ERR_INVALID_ARGUMENT;
   const AttnLayout need = layout_attn(a, nullptr);
   if (workspace_bytes < need.bytes) return SPEC_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -309,8 +310,19 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
     if (!make_map_bf16(&tmK, a->k_cache, 3, dims, strides, box) ||
         !make_map_bf16(&tmV, a->v_cache, 3, dims, strides, box))
       return SPEC_ERR_CUDA;
+    // Q as (d, Hq, N, B): one box of (64, G, 128 / G, 1) is a 128-row group of (node, head) rows
+    // of one KV head.  Other G stage Q through registers.
+    CUtensorMap tmQ;
+    std::memset(&tmQ, 0, sizeof(tmQ));
+    if (p.G <= 128 && 128 % p.G == 0) {
+      const cuuint64_t qd[4] = {(cuuint64_t)d, (cuuint64_t)Hq, (cuuint64_t)N, (cuuint64_t)B};
+      const cuuint64_t qs[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hq * d * 2, (cuuint64_t)N * Hq * d * 2};
+      const cuuint32_t qb[4] = {64, (cuuint32_t)p.G, (cuuint32_t)(128 / p.G), 1};
+      if (!make_map_bf16(&tmQ, a->q, 4, qd, qs, qb)) return SPEC_ERR_CUDA;
+      p.q_tma = 1;
+    }
     record(a->timing_begin, stream);
-    if (launch_attention_tc(&tmK, &tmV, p, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (launch_attention_tc(&tmQ, &tmK, &tmV, p, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     record(a->timing_end, stream);
     launch_attention_merge_bf16(p, stream);
   }

@@ -50,6 +50,11 @@ struct AttnTcCfg {
   static constexpr int kSmem =
       1024 + NG * kQ + 2 * kStages * kTile + NG * kP + kRowsCta * kAncWords * 4 + 32 * 8;
   static constexpr uint32_t kTmemCols = (NG * (kKT + D) <= 256) ? 256 : 512;  // S and O per group
+  // epilogue: the normalised O rows staged in shared memory (fp32, rows padded by 16 bytes so
+  // that the quarter-warps' 16-byte stores of consecutive rows hit distinct banks), reusing the
+  // Q / K / V / P region once every MMA of the CTA has completed
+  static constexpr int kORow = D * 4 + 16;
+  static_assert(kRowsCta * kORow <= NG * kQ + 2 * kStages * kTile + NG * kP, "O staging does not fit");
 };
 
 // 2^x with the special-function unit's approximation (PTX ex2.approx.ftz: about 2 ulp; results
@@ -64,6 +69,25 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int ch, int rows) {
   return (uint32_t)((ch >> 3) * rows * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
+__device__ __forceinline__ void tma_load_4d_plain(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                                  int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
+// One row of the output partial (fp32) from shared memory to global memory by the bulk-copy
+// engine; the row stays readable in shared memory until the matching wait below.
+__device__ __forceinline__ void bulk_store_row(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+               "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_load_3d_plain(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                                                   int z) {
   asm volatile(
@@ -77,8 +101,8 @@ __device__ __forceinline__ void tma_load_3d_plain(void* dst, const CUtensorMap* 
 
 template <int D, int NG>
 __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   const AttnParams p) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using C = AttnTcCfg<D, NG>;
   constexpr int kGroups = C::kGroups;
   constexpr int kRowsCta = C::kRowsCta;
@@ -98,6 +122,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   uint64_t* pfull = sfree + kGroups;     // [group] P written
   uint64_t* ofull = pfull + kGroups;     // [group] P V done (O updated, P buffer free)
   uint64_t* drained = ofull + kGroups;
+  uint64_t* qfull = drained + kGroups;   // Q of every group landed (TMA path)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_issued, s_consumed;
@@ -195,6 +220,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         }
       }
       __syncthreads();
+      int more = 0;
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int c = tid + k * kTcThreads;
@@ -202,9 +228,10 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
 #pragma unroll
           for (int w = 0; w < kAncWords; ++w) s_nanc[c][w] |= up[k][w];
           s_jmp[c] = nj[k];
+          more |= nj[k] >= 0;
         }
       }
-      __syncthreads();
+      if (!__syncthreads_or(more)) break;  // every node's set reaches the root
     }
     for (int c = tid; c < kRowsCta * kAncWords; c += kTcThreads) {
       const int r = c / kAncWords, w = c % kAncWords, row = row0 + r;
@@ -237,6 +264,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       mbar_init(&ofull[a], 1);
     }
     for (int a = 0; a < kGroups; ++a) mbar_init(&drained[a], 1);
+    mbar_init(qfull, 1);
     s_abort = 0;
     s_issued = 0;
     s_consumed = 0;
@@ -286,41 +314,54 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       }
     }
   };
-  // The first kStages tiles go out now (every stage starts free), so they load while Q is staged.
+  // Q (TMA path) and the first kStages K/V tiles go out now (every stage starts free).
   const int pre = T < kStages ? T : kStages;
   if (warp == 0 && lane == 0) {
+    if (p.q_tma) {
+      // box (64 dims, G heads, 128 / G nodes) = 128 rows (node, head) in row order, swizzled
+      // like the MMA's A operand; rows past the last node read as zeros
+      mbar_arrive_expect_tx(qfull, kGroups * C::kQ);
+      const int npg = kGR / p.G;  // nodes per group
+#pragma unroll
+      for (int a = 0; a < kGroups; ++a)
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d_plain(sQ + a * C::kQ + c * kGR * 128, &tmQ, qfull, c * 64, g * p.G, (row0 / p.G) + a * npg, b);
+    }
     for (int t = 0; t < pre; ++t) issue_tile(t);
     s_issued = pre;
   }
 
-  // ---- Q rows -> shared memory in the K-major 128-byte-swizzle layout of the MMA A operand ----
-  // Every load of a thread is issued before its first store, so the loads overlap.
-  constexpr int NCH = D / 8;
-  constexpr int kQPer = (kRowsCta * NCH + kTcThreads - 1) / kTcThreads;
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-  uint4 qv[kQPer];
+  if (!p.q_tma) {
+    // ---- Q rows -> shared memory in the K-major 128-byte-swizzle layout of the MMA A operand ----
+    // Every load of a thread is issued before its first store, so the loads overlap.
+    constexpr int NCH = D / 8;
+    constexpr int kQPer = (kRowsCta * NCH + kTcThreads - 1) / kTcThreads;
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+    uint4 qv[kQPer];
 #pragma unroll
-  for (int k = 0; k < kQPer; ++k) {
-    const int c = tid + k * kTcThreads;
-    const int rr = c / NCH, ch = c % NCH, row = row0 + rr;
-    qv[k] = make_uint4(0, 0, 0, 0);
-    if (c < kRowsCta * NCH && row < rows_total) {
-      const int i = row / p.G, j = row % p.G;
-      qv[k] = *reinterpret_cast<const uint4*>(q + (((size_t)b * p.N + i) * p.Hq + g * p.G + j) * D + ch * 8);
+    for (int k = 0; k < kQPer; ++k) {
+      const int c = tid + k * kTcThreads;
+      const int rr = c / NCH, ch = c % NCH, row = row0 + rr;
+      qv[k] = make_uint4(0, 0, 0, 0);
+      if (c < kRowsCta * NCH && row < rows_total) {
+        const int i = row / p.G, j = row % p.G;
+        qv[k] = *reinterpret_cast<const uint4*>(q + (((size_t)b * p.N + i) * p.Hq + g * p.G + j) * D + ch * 8);
+      }
     }
-  }
 #pragma unroll
-  for (int k = 0; k < kQPer; ++k) {
-    const int c = tid + k * kTcThreads;
-    if (c < kRowsCta * NCH) {
-      const int rr = c / NCH, ch = c % NCH;
-      *reinterpret_cast<uint4*>(sQ + (rr / kGR) * C::kQ + sw128_off(rr % kGR, ch, kGR)) = qv[k];
+    for (int k = 0; k < kQPer; ++k) {
+      const int c = tid + k * kTcThreads;
+      if (c < kRowsCta * NCH) {
+        const int rr = c / NCH, ch = c % NCH;
+        *reinterpret_cast<uint4*>(sQ + (rr / kGR) * C::kQ + sw128_off(rr % kGR, ch, kGR)) = qv[k];
+      }
     }
+    fence_proxy_async_smem();  // Q (generic stores) becomes visible to the tensor cores
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
   }
-  fence_proxy_async_smem();  // Q (generic stores) becomes visible to the tensor cores
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   const uint32_t tmem = s_tmem;
   // TMEM columns: S of group a at [a * 64, a * 64 + 64), O of group a at [NG * 64 + a * D, ...)
 
@@ -381,7 +422,8 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         umma_commit(&ofull[ga]);
         return true;
       };
-      ok = issue_s(0);
+      ok = !p.q_tma || mbar_wait_bounded(qfull, 0, &s_abort);
+      ok = ok && issue_s(0);
       for (int t = 0; t < T && ok; ++t) {
         if (t + 1 < T) ok = issue_s(t + 1);
         ok = ok && issue_pv(t);
@@ -503,39 +545,43 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&pfull[a]);
     }
-    if (ok && mbar_wait_bounded(&ofull[a], (T - 1) & 1, &s_abort)) {
+    const bool fin = ok && mbar_wait_bounded(&ofull[a], (T - 1) & 1, &s_abort);
+    // Once every group's last P V has completed, no MMA or copy reads or writes the Q / K / V / P
+    // region any more: the O rows are staged there and leave through the bulk-copy engine.
+    named_bar_sync(1, 128 * kGroups);
+    const bool valid = row < rows_total;
+    size_t orow = 0;
+    if (valid) {
+      const int i = row / p.G, hq = g * p.G + row % p.G;
+      orow = ((size_t)b * p.N + i) * p.Hq + hq;
+    }
+    if (fin) {
       tc_fence_after();
-      const bool valid = row < rows_total;
-      size_t orow = 0;
-      if (valid) {
-        const int i = row / p.G, hq = g * p.G + row % p.G;
-        orow = ((size_t)b * p.N + i) * p.Hq + hq;
-        p.part_ml[orow * p.n_split + split] = make_float2(m_run, l_run);
-      }
+      if (valid) p.part_ml[orow * p.n_split + split] = make_float2(m_run, l_run);
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      uint8_t* srow = base + rr * C::kORow;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld_x32(tO + c * 32, o);
         tmem_ld_wait();
-        if (valid) {
-          float* dst = p.part_o + (orow * p.n_split + split) * D + c * 32;
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(dst + j) =
-                make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
-                            __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
-        }
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(srow + (c * 32 + j) * 4) =
+              make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                          __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+      }
+      if (valid) {
+        fence_proxy_async_smem();  // the staged row (generic stores) becomes visible to the copy
+        bulk_store_row(p.part_o + (orow * p.n_split + split) * D, srow, D * 4);
+        bulk_wait_read();
       }
     } else {
       if (lane == 0) {
         s_abort = 1;
         set_status(p.dev_status, SPEC_ERR_TIMEOUT);
       }
-      if (row < rows_total) {  // the merge skips this split
-        const int i = row / p.G, hq = g * p.G + row % p.G;
-        p.part_ml[(((size_t)b * p.N + i) * p.Hq + hq) * p.n_split + split] = make_float2(-INFINITY, 0.f);
-      }
+      if (valid) p.part_ml[orow * p.n_split + split] = make_float2(-INFINITY, 0.f);  // the merge skips this split
     }
   }
 
@@ -544,6 +590,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     // let the copies still in flight land before shared memory is released
     for (int u = s_consumed; u < s_issued; ++u)
       mbar_wait_bounded(&full[u % kStages], (uint32_t)((u / kStages) & 1), nullptr);
+    if (p.q_tma) mbar_wait_bounded(qfull, 0, nullptr);
   }
   __syncthreads();
   tc_fence_after();
@@ -553,19 +600,21 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
 int attention_tc_rows_per_cta(int groups) { return kGR * groups; }
 
 template <int D, int NG>
-static cudaError_t launch_tc(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p, cudaStream_t stream) {
+static cudaError_t launch_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
+                             cudaStream_t stream) {
   using C = AttnTcCfg<D, NG>;
   const dim3 grid(p.n_rg, p.n_split, p.B * p.Hkv);
   cudaError_t err = cudaFuncSetAttribute(attn_tc_kernel<D, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
-  attn_tc_kernel<D, NG><<<grid, C::kThreads, C::kSmem, stream>>>(*tmK, *tmV, p);
+  attn_tc_kernel<D, NG><<<grid, C::kThreads, C::kSmem, stream>>>(*tmQ, *tmK, *tmV, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attention_tc(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
-                                cudaStream_t stream) {
-  if (p.d == 128) return p.groups == 2 ? launch_tc<128, 2>(tmK, tmV, p, stream) : launch_tc<128, 1>(tmK, tmV, p, stream);
-  return p.groups == 2 ? launch_tc<64, 2>(tmK, tmV, p, stream) : launch_tc<64, 1>(tmK, tmV, p, stream);
+cudaError_t launch_attention_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                const AttnParams& p, cudaStream_t stream) {
+  if (p.d == 128)
+    return p.groups == 2 ? launch_tc<128, 2>(tmQ, tmK, tmV, p, stream) : launch_tc<128, 1>(tmQ, tmK, tmV, p, stream);
+  return p.groups == 2 ? launch_tc<64, 2>(tmQ, tmK, tmV, p, stream) : launch_tc<64, 1>(tmQ, tmK, tmV, p, stream);
 }
 
 }  // namespace spectree

@@ -44,6 +44,7 @@ struct AttnParams {
   const int32_t* table;
   int bs, bs_shift, max_blocks, num_blocks;
   int32_t* req_bad;  // [B] written by the tail CTAs: the request's table has an entry out of range
+  int q_tma;         // bf16: Q rows arrive by TMA through the (d, Hq, N, B) map (128 % G == 0)
 };
 
 struct AttnPlan {
@@ -52,8 +53,8 @@ struct AttnPlan {
 AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_sms);
 void launch_attention_merge_bf16(const AttnParams& p, cudaStream_t stream);
 int attention_tc_rows_per_cta(int groups);
-cudaError_t launch_attention_tc(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
-                                cudaStream_t stream);
+cudaError_t launch_attention_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                const AttnParams& p, cudaStream_t stream);
 void launch_attention_f32(const AttnParams& p, cudaStream_t stream);
 
 // ---- K2: LM head + row statistics -----------------------------------------------------------
