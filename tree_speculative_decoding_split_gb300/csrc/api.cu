@@ -275,7 +275,6 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
   p.part_ml = l.part_ml;
   p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.W = (N + 31) / 32; p.d = d;
   p.L_cap = a->kv_capacity;
-  p.n_prefix = l.plan.n_prefix;
   p.chunk = l.plan.chunk;
   p.n_split = l.plan.n_split;
   p.n_rg = l.plan.n_rg;

@@ -162,22 +162,42 @@ AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_s
   const int rows_cta = attention_tc_rows_per_cta(pl.groups);  // (node, GQA head) rows per bf16 CTA
   pl.n_rg = (N * G + rows_cta - 1) / rows_cta;
   const long long base = (long long)B * Hkv * pl.n_rg;
-  long long want = (4LL * num_sms + base - 1) / base;  // about four CTAs per SM
-  if (want < 1) want = 1;
-  if (want > 31) want = 31;
-  long long chunk = (L_cap + want - 1) / want;
-  chunk = (chunk + kKT - 1) / kKT * kKT;
-  if (chunk < 4 * kKT) chunk = 4 * kKT;      // at least 4 key tiles per CTA
-  if (chunk > 16384) chunk = 16384;          // long prefixes: at most 16K keys per CTA
-  long long np = (L_cap + chunk - 1) / chunk;
-  if (np < 1) np = 1;
-  while (np > 31) {  // keep n_split within a warp for the merge
-    chunk *= 2;
-    np = (L_cap + chunk - 1) / chunk;
+  // Key splits.  A CTA costs about kFixedTiles key tiles of fixed work (tree checks, prologue,
+  // epilogue) plus its key tiles, and the CTAs run one per SM in rounds; prefix lengths are only
+  // known on the device, so the estimate takes every request at L_cap.  Among chunks of 4 or
+  // more key tiles (at most 16K keys, at most 31 splits) take the one with the smallest
+  // estimated time, with at least two CTAs per SM when the prefix allows it (shorter requests
+  // then leave the rounds less unbalanced); ties go to fewer splits (fewer partials to merge).
+  constexpr long long kFixedTiles = 4;
+  const long long min_ctas = 2LL * num_sms;
+  long long best_chunk = -1, best_cost = 0, best_np = 0;
+  bool best_meets = false;
+  for (long long s = 1; s <= 31; ++s) {
+    long long chunk = (L_cap + s - 1) / s;
+    chunk = (chunk + kKT - 1) / kKT * kKT;
+    if (chunk < 4 * kKT) chunk = 4 * kKT;
+    if (chunk > 16384) continue;
+    const long long np = (L_cap + chunk - 1) / chunk;
+    const long long ctas = base * np;
+    const long long cost = ((ctas + num_sms - 1) / num_sms) * (kFixedTiles + chunk / kKT);
+    const bool meets = ctas >= min_ctas;
+    if (best_chunk < 0 || (meets && !best_meets) || (meets == best_meets && cost < best_cost)) {
+      best_chunk = chunk;
+      best_cost = cost;
+      best_np = np;
+      best_meets = meets;
+    }
   }
-  pl.chunk = (int)chunk;
-  pl.n_prefix = (int)np;
-  pl.n_split = pl.n_prefix + 1;
+  if (best_chunk < 0) {  // very long prefixes: 16K-key chunks, doubled until 31 splits cover L_cap
+    best_chunk = 16384;
+    best_np = (L_cap + best_chunk - 1) / best_chunk;
+    while (best_np > 31) {
+      best_chunk *= 2;
+      best_np = (L_cap + best_chunk - 1) / best_chunk;
+    }
+  }
+  pl.chunk = (int)best_chunk;
+  pl.n_split = (int)(best_np < 1 ? 1 : best_np);
   return pl;
 }
 

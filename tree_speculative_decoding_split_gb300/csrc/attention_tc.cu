@@ -9,19 +9,23 @@
 // j) pair r = i * G + j, so every K/V tile is read once for all query heads sharing KV head g and
 // all tree nodes.  With NG = 2 the two 128-row groups (the M of one MMA each) run in ping-pong:
 // while one group's softmax works on its scores, the tensor core computes the other group's P V
-// and next Q K^T; small problems use NG = 1 for more, shorter CTAs.  Roles (64 + 128 NG threads):
-//   warp 0     TMA producer: 64-key K and V tiles (128-byte swizzle) into a 3-stage ring;
-//   warp 1     MMA issuer: per group, S = Q K^T into the group's TMEM score buffer as soon as
-//              the softmax has read the previous S, and O += P V into the group's TMEM
-//              accumulator as soon as P is written; V is consumed MN-major straight from its TMA
-//              tiles;
-//   warps 2-   softmax, four warps per group: the thread owning TMEM lane r of a group owns that
-//              row -- it loads its S row, applies the tree mask (ancestor bits, tail split only)
-//              and the online softmax in the log2 domain, and writes the bf16 P row to shared
-//              memory.  O is rescaled in TMEM only when a row's running maximum grows by more than
-//              2^8 (exact: P and the running sum use the same stale maximum).
-// Every CTA validates the tree; the tail CTA builds the ancestor bits by pointer jumping.  Each
-// split writes a normalised partial (o, running max, sum), merged by the merge kernel.
+// and next Q K^T; small problems use NG = 1 for more, shorter CTAs.  Roles:
+//   warp 0     TMA producer: the CTA's Q rows (when G divides 128), then 64-key K and V tiles
+//              (128-byte swizzle) into a 4-stage ring;
+//   warp 1 (+ one more warp per extra group)  MMA issuer of one group: S = Q K^T into the
+//              group's TMEM score buffer as soon as the softmax has read the previous S, and
+//              O += P V into the group's TMEM accumulator as soon as P is written, with P read
+//              from tensor memory and V consumed MN-major straight from its TMA tiles;
+//   softmax    four warps per group: the thread owning TMEM lane r of a group owns that row --
+//              it loads its S row, applies the tree mask (ancestor bits, tree tiles only) and
+//              the online softmax in the log2 domain, and writes the bf16 P row into one of the
+//              group's two P buffers in tensor memory (so P(t) waits only for P V(t - 2)).  O is
+//              rescaled in TMEM only when a row's running maximum grows by more than 2^8
+//              (exact: P and the running sum use the same stale maximum).
+// Every CTA validates the tree; the CTAs of the split that holds the tree keys (the prefix split
+// containing slot L, which then also covers [L, L + n)) build the ancestor bits by pointer
+// jumping.  Each split writes a normalised partial (o, running max, sum), merged by the merge
+// kernel.
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -32,7 +36,7 @@ namespace spectree {
 namespace {
 
 constexpr int kKT = 64;          // keys per tile (MMA N of S, K of P V)
-constexpr int kStages = 3;       // K/V ring depth
+constexpr int kStages = 4;       // K/V ring depth
 constexpr int kGR = 128;         // rows per group (MMA M)
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxBlkCta = 1040;  // paged KV: block-table entries a CTA stages in shared memory
@@ -46,15 +50,17 @@ struct AttnTcCfg {
   static constexpr int kThreads = 64 + 128 * NG + (NG > 1 ? 32 * (NG - 1) : 0);
   static constexpr int kQ = kGR * D * 2;        // Q bytes per group
   static constexpr int kTile = kKT * D * 2;     // K (or V) tile bytes
-  static constexpr int kP = kGR * kKT * 2;      // P bytes per group
   static constexpr int kSmem =
-      1024 + NG * kQ + 2 * kStages * kTile + NG * kP + kRowsCta * kAncWords * 4 + 32 * 8;
-  static constexpr uint32_t kTmemCols = (NG * (kKT + D) <= 256) ? 256 : 512;  // S and O per group
+      1024 + NG * kQ + 2 * kStages * kTile + kRowsCta * kAncWords * 4 + 32 * 8;
+  // TMEM columns per group: S (kKT fp32), O (D fp32), and two P buffers (kKT bf16 = kKT / 2
+  // columns each)
+  static constexpr int kColS = 0, kColO = NG * kKT, kColP = NG * (kKT + D);
+  static constexpr uint32_t kTmemCols = (NG * (2 * kKT + D) <= 256) ? 256 : 512;
   // epilogue: the normalised O rows staged in shared memory (fp32, rows padded by 16 bytes so
   // that the quarter-warps' 16-byte stores of consecutive rows hit distinct banks), reusing the
   // Q / K / V / P region once every MMA of the CTA has completed
   static constexpr int kORow = D * 4 + 16;
-  static_assert(kRowsCta * kORow <= NG * kQ + 2 * kStages * kTile + NG * kP, "O staging does not fit");
+  static_assert(kRowsCta * kORow <= NG * kQ + 2 * kStages * kTile, "O staging does not fit");
 };
 
 // 2^x with the special-function unit's approximation (PTX ex2.approx.ftz: about 2 ulp; results
@@ -112,16 +118,15 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   uint8_t* sQ = base;                                  // [group][128 rows][D], K-major swizzled
   uint8_t* sK = sQ + kGroups * C::kQ;
   uint8_t* sV = sK + kStages * C::kTile;
-  uint8_t* sP = sV + kStages * C::kTile;              // [group][128 rows][64 keys]
-  uint32_t* sAnc = reinterpret_cast<uint32_t*>(sP + kGroups * C::kP);
+  uint32_t* sAnc = reinterpret_cast<uint32_t*>(sV + kStages * C::kTile);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sAnc + kRowsCta * kAncWords);
-  uint64_t* full = bars;                 // [3] K/V landed
-  uint64_t* empty = full + kStages;      // [3] K/V consumed by both groups
+  uint64_t* full = bars;                 // [stage] K/V landed
+  uint64_t* empty = full + kStages;      // [stage] K/V consumed by every group
   uint64_t* sfull = empty + kStages;     // [group] S computed
   uint64_t* sfree = sfull + kGroups;     // [group] S read by the softmax
   uint64_t* pfull = sfree + kGroups;     // [group] P written
-  uint64_t* ofull = pfull + kGroups;     // [group] P V done (O updated, P buffer free)
-  uint64_t* drained = ofull + kGroups;
+  uint64_t* ofull = pfull + kGroups;     // [group][P buffer] P V done (O updated, buffer free)
+  uint64_t* drained = ofull + 2 * kGroups;
   uint64_t* qfull = drained + kGroups;   // Q of every group landed (TMA path)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -136,7 +141,6 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long L = p.prefix_len[b];
   const int n = p.n_nodes[b];
-  const bool tail = (split == p.n_prefix);
   const int rows_total = p.N * p.G;
   const int row0 = rg * kRowsCta;
 
@@ -157,14 +161,12 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     if (tid == 0 && rg == 0 && split == 0 && g == 0) set_status(p.dev_status, err);
     return;
   }
-  long long kb, ke;
-  if (!tail) {
-    kb = (long long)split * p.chunk;
-    ke = kb + p.chunk < L ? kb + p.chunk : L;
-  } else {
-    kb = L;
-    ke = L + n;
-  }
+  // Split s covers keys [s * chunk, (s + 1) * chunk); the split holding key L (the first tree
+  // slot) also takes every tree key, [L, L + n), and the splits after it have none.
+  const int s_tree = (int)(L / p.chunk) < p.n_split - 1 ? (int)(L / p.chunk) : p.n_split - 1;
+  const bool tail = (split == s_tree);   // this CTA's keys include the tree
+  const long long kb = (long long)split * p.chunk;
+  const long long ke = split < s_tree ? kb + p.chunk : (tail ? L + n : kb);
   // Paged KV: tiles start on 64-key boundaries of the logical slots (so that a tile never
   // straddles a block of >= 64 slots, and a block of fewer slots fills whole 16-row groups of
   // the swizzled tile); keys below kb are masked.  Contiguous: tiles start at kb.
@@ -261,7 +263,8 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       mbar_init(&sfull[a], 1);
       mbar_init(&sfree[a], 4);
       mbar_init(&pfull[a], 4);
-      mbar_init(&ofull[a], 1);
+      mbar_init(&ofull[2 * a], 1);
+      mbar_init(&ofull[2 * a + 1], 1);
     }
     for (int a = 0; a < kGroups; ++a) mbar_init(&drained[a], 1);
     mbar_init(qfull, 1);
@@ -363,7 +366,6 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     tc_fence_after();
   }
   const uint32_t tmem = s_tmem;
-  // TMEM columns: S of group a at [a * 64, a * 64 + 64), O of group a at [NG * 64 + a * D, ...)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * (kGR * 128) + (kk & 3) * 32, 0, 1024);
           const uint64_t bd = sdesc_sw128(ka + (kk >> 2) * (kKT * 128) + (kk & 3) * 32, 0, 1024);
-          umma_bf16(tmem + ga * kKT, ad, bd, idS, kk > 0);
+          umma_bf16(tmem + C::kColS + ga * kKT, ad, bd, idS, kk > 0);
         }
         umma_commit(&sfull[ga]);
         return true;
@@ -412,14 +414,14 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       auto issue_pv = [&](int t) -> bool {
         if (!mbar_wait_bounded(&pfull[ga], t & 1, &s_abort)) return false;
         tc_fence_after();
-        const uint32_t pa = smem_u32(sP + ga * C::kP), va = smem_u32(sV + (t % kStages) * C::kTile);
+        const uint32_t pt = tmem + C::kColP + (2 * ga + (t & 1)) * (kKT / 2);  // P(t) in TMEM
+        const uint32_t va = smem_u32(sV + (t % kStages) * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < kKT / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(pa + kk * 32, 0, 1024);
           const uint64_t bd = sdesc_sw128(va + kk * 16 * 128, kKT * 128, 1024);
-          umma_bf16(tmem + kGroups * kKT + ga * D, ad, bd, idP, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_tmem_a(tmem + C::kColO + ga * D, pt + kk * 8, bd, idP, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&ofull[ga]);
+        umma_commit(&ofull[2 * ga + (t & 1)]);
         return true;
       };
       ok = !p.q_tma || mbar_wait_bounded(qfull, 0, &s_abort);
@@ -446,9 +448,9 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     const int rr = a * kGR + rl;              // row within the CTA
     const int row = row0 + rr;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const uint32_t tS = tmem + a * kKT + lane_off;
-    const uint32_t tO = tmem + kGroups * kKT + a * D + lane_off;
-    uint8_t* prow = sP + a * C::kP;
+    const uint32_t tS = tmem + C::kColS + a * kKT + lane_off;
+    const uint32_t tO = tmem + C::kColO + a * D + lane_off;
+    const uint32_t tP = tmem + C::kColP + 2 * a * (kKT / 2) + lane_off;  // + (t & 1) * kKT / 2
     float m_run = -INFINITY, l_run = 0.f;
     const uint32_t* anc = sAnc + rr * kAncWords;  // this row's ancestor words (tail split)
     bool ok = true;
@@ -472,19 +474,21 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         v[j + 32] = __uint_as_float(s1[j]);
       }
       const long long kbase = t0 + (long long)t * kKT;
-      if (tail) {
-        // key j of the tile is tree node kbase - kb + j; its ancestor bit comes from a 64-bit
-        // window of the row's ancestor words in shared memory (held in registers, the words
-        // would need a runtime index, which puts them in local memory); nodes outside [0, n)
-        // have no bit
-        const int off = (int)(kbase - kb);
-        const int lo = off >> 5;            // floor division (off may be negative when paged)
+      if (tail && kbase + kKT > L) {
+        // key j of the tile is tree node kbase - L + j when that is >= 0, else a prefix key; the
+        // ancestor bits come from a 64-bit window of the row's ancestor words in shared memory
+        // (held in registers, the words would need a runtime index, which puts them in local
+        // memory); nodes outside [0, n) have no bit
+        const int off = (int)(kbase - L);   // >= -63
+        const int lo = off >> 5;            // floor division (off may be negative)
         const int r = off - (lo << 5);      // 0..31
         const uint32_t w0 = (lo >= 0 && lo < kAncWords) ? anc[lo] : 0u;
         const uint32_t w1 = (lo + 1 >= 0 && lo + 1 < kAncWords) ? anc[lo + 1] : 0u;
         const uint32_t w2 = (lo + 2 >= 0 && lo + 2 < kAncWords) ? anc[lo + 2] : 0u;
         const unsigned long long win = ((unsigned long long)w1 << 32) | w0;
-        const unsigned long long mask = (win >> r) | (r ? ((unsigned long long)w2 << (64 - r)) : 0ull);
+        unsigned long long mask = (win >> r) | (r ? ((unsigned long long)w2 << (64 - r)) : 0ull);
+        if (off < 0) mask |= (1ull << -off) - 1ull;  // the tile's first -off keys are prefix keys
+        if (kbase < kb) mask &= ~((1ull << (kb - kbase)) - 1ull);  // paged: keys before the split
 #pragma unroll
         for (int j = 0; j < kKT; ++j)
           if (!((mask >> j) & 1ull)) v[j] = -INFINITY;
@@ -501,14 +505,14 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
       const float m_new = fmaxf(m_run, tmax);
       const bool need = m_new > m_run + kRescaleLog2;  // includes the first finite maximum
-      // P V of the previous tile must be done before P is overwritten or O is rescaled
-      if (t > 0 && !mbar_wait_bounded(&ofull[a], (t - 1) & 1, &s_abort)) {
-        ok = false;
-        break;
-      }
       if (__any_sync(0xffffffffu, need)) {
         const float f = need ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run is -inf
         if (t > 0) {
+          // P V(t - 1) must have landed in O before O is rescaled
+          if (!mbar_wait_bounded(&ofull[2 * a + ((t - 1) & 1)], ((t - 1) >> 1) & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -536,16 +540,18 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         pk[j / 2] = pack_bf16x2(p0, p1);
       }
       l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-#pragma unroll
-      for (int ch = 0; ch < kKT / 8; ++ch)
-        *reinterpret_cast<uint4*>(prow + sw128_off(rl, ch, kGR)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      fence_proxy_async_smem();
+      // P buffer t & 1 was last read by P V(t - 2)
+      if (t >= 2 && !mbar_wait_bounded(&ofull[2 * a + (t & 1)], ((t - 2) >> 1) & 1, &s_abort)) {
+        ok = false;
+        break;
+      }
+      tmem_st_x32(tP + (t & 1) * (kKT / 2), pk);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pfull[a]);
     }
-    const bool fin = ok && mbar_wait_bounded(&ofull[a], (T - 1) & 1, &s_abort);
+    const bool fin = ok && mbar_wait_bounded(&ofull[2 * a + ((T - 1) & 1)], ((T - 1) >> 1) & 1, &s_abort);
     // Once every group's last P V has completed, no MMA or copy reads or writes the Q / K / V / P
     // region any more: the O rows are staged there and leave through the bulk-copy engine.
     named_bar_sync(1, 128 * kGroups);

@@ -32,9 +32,8 @@ struct AttnParams {
   float2* part_ml;   // [B*N*Hq][n_split] (running max in log2 units, sum)
   int B, N, Hq, Hkv, G, W, d;
   long long L_cap;
-  int n_prefix;      // prefix splits
-  int chunk;         // keys per prefix split
-  int n_split;       // n_prefix + 1 (the last split holds the tree tail)
+  int chunk;         // keys per split (a multiple of 64)
+  int n_split;       // key splits; the one holding slot prefix_len also takes the tree keys
   int n_rg;          // row groups of (node, head) rows per KV head (one bf16 CTA each)
   int groups;        // 128-row groups per bf16 CTA (1 or 2)
   float scale;
@@ -48,7 +47,7 @@ struct AttnParams {
 };
 
 struct AttnPlan {
-  int n_rg, n_prefix, chunk, n_split, groups;
+  int n_rg, chunk, n_split, groups;
 };
 AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_sms);
 void launch_attention_merge_bf16(const AttnParams& p, cudaStream_t stream);
