@@ -531,20 +531,22 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         }
       }
       const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      // exponents two at a time (packed fp32 pairs: one FFMA2 per pair, one FADD2 per pair into
+      // two running pair sums)
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nmu2 = make_float2(-mu, -mu);
+      float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       uint32_t pk[kKT / 2];
 #pragma unroll
       for (int j = 0; j < kKT; j += 2) {
-        const float p0 = ex2_approx(fmaf(v[j], p.scale_log2, -mu)), p1 = ex2_approx(fmaf(v[j + 1], p.scale_log2, -mu));
-        ps[(j >> 1) & 3] += p0 + p1;
+        const float2 x = __ffma2_rn(make_float2(v[j], v[j + 1]), sc2, nmu2);
+        const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+        ps2[(j >> 1) & 1] = __fadd2_rn(ps2[(j >> 1) & 1], make_float2(p0, p1));
         pk[j / 2] = pack_bf16x2(p0, p1);
       }
-      l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      // P buffer t & 1 was last read by P V(t - 2)
-      if (t >= 2 && !mbar_wait_bounded(&ofull[2 * a + (t & 1)], ((t - 2) >> 1) & 1, &s_abort)) {
-        ok = false;
-        break;
-      }
+      l_run += (ps2[0].x + ps2[1].x) + (ps2[0].y + ps2[1].y);
+      // P buffer t & 1 was last read by P V(t - 2).  This group's issuer issued that MMA before
+      // S(t), and the commit that completed sfull for S(t) tracks every earlier MMA of that
+      // thread, so the buffer is already free.
       tmem_st_x32(tP + (t & 1) * (kKT / 2), pk);
       tmem_st_wait();
       tc_fence_before();
