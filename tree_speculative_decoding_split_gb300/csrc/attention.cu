@@ -56,8 +56,8 @@ __global__ void __launch_bounds__(256) attn_merge_bf16_kernel(const AttnParams p
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  // Partials are loaded in batches of 8 whatever their weight (a split that saw no key of this
-  // row holds stale values, which a zero weight selects away), so the loads overlap.
+  // Partials are loaded in batches of 8 so that the loads overlap; splits of zero weight (no key
+  // of this row, or past the request's last key) are not read.
   constexpr int kBatch = 8;
   for (int s0 = 0; s0 < p.n_split; s0 += kBatch) {
     float v[kBatch][EPL];
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(256) attn_merge_bf16_kernel(const AttnParams p
     for (int k = 0; k < kBatch; ++k) {
       const int s = s0 + k;
       ws[k] = __shfl_sync(0xffffffffu, w, s & 31);
-      if (s < p.n_split) {
+      if (s < p.n_split && ws[k] > 0.f) {
         const float* src = p.part_o + (orow * p.n_split + s) * D + lane * EPL;
         if constexpr (EPL == 4) {
           const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
@@ -166,12 +166,16 @@ AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_s
   // epilogue) plus its key tiles, and the CTAs run one per SM in rounds; prefix lengths are only
   // known on the device, so the estimate takes every request at L_cap.  Among chunks of 4 or
   // more key tiles (at most 16K keys, at most 31 splits) take the one with the smallest
-  // estimated time, with at least two CTAs per SM when the prefix allows it (shorter requests
-  // then leave the rounds less unbalanced); ties go to fewer splits (fewer partials to merge).
-  constexpr long long kFixedTiles = 4;
-  const long long min_ctas = 2LL * num_sms;
-  long long best_chunk = -1, best_cost = 0, best_np = 0;
-  bool best_meets = false;
+  // estimated time, preferring grids that fill at least one round.  When that fills at most two
+  // rounds, take the most splits (up to twice as many) whose estimate is within 10 %: with few
+  // rounds, requests shorter than L_cap would leave SMs idle unless the work is cut finer.
+  constexpr long long kFixedTiles = 7;
+  struct Cand {
+    long long chunk, np, cost, rounds;
+    bool fills;
+  };
+  Cand cand[32];
+  int nc = 0;
   for (long long s = 1; s <= 31; ++s) {
     long long chunk = (L_cap + s - 1) / s;
     chunk = (chunk + kKT - 1) / kKT * kKT;
@@ -179,16 +183,29 @@ AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_s
     if (chunk > 16384) continue;
     const long long np = (L_cap + chunk - 1) / chunk;
     const long long ctas = base * np;
-    const long long cost = ((ctas + num_sms - 1) / num_sms) * (kFixedTiles + chunk / kKT);
-    const bool meets = ctas >= min_ctas;
-    if (best_chunk < 0 || (meets && !best_meets) || (meets == best_meets && cost < best_cost)) {
-      best_chunk = chunk;
-      best_cost = cost;
-      best_np = np;
-      best_meets = meets;
-    }
+    const long long rounds = (ctas + num_sms - 1) / num_sms;
+    const Cand c = {chunk, np, rounds * (kFixedTiles + chunk / kKT), rounds, ctas >= num_sms};
+    if (nc > 0 && cand[nc - 1].np == np)
+      cand[nc - 1] = c;  // same split count with a smaller chunk
+    else
+      cand[nc++] = c;
   }
-  if (best_chunk < 0) {  // very long prefixes: 16K-key chunks, doubled until 31 splits cover L_cap
+  long long best_chunk = -1, best_np = 0;
+  if (nc > 0) {
+    int bi = 0;
+    for (int i = 1; i < nc; ++i)
+      if ((cand[i].fills && !cand[bi].fills) ||
+          (cand[i].fills == cand[bi].fills && cand[i].cost < cand[bi].cost))
+        bi = i;
+    int pick = bi;
+    if (cand[bi].rounds <= 2)
+      for (int i = 0; i < nc; ++i)
+        if (cand[i].fills == cand[bi].fills && cand[i].np <= 2 * cand[bi].np && cand[i].np > cand[pick].np &&
+            cand[i].cost * 10 <= cand[bi].cost * 11)
+          pick = i;
+    best_chunk = cand[pick].chunk;
+    best_np = cand[pick].np;
+  } else {  // very long prefixes: 16K-key chunks, doubled until 31 splits cover L_cap
     best_chunk = 16384;
     best_np = (L_cap + best_chunk - 1) / best_chunk;
     while (best_np > 31) {

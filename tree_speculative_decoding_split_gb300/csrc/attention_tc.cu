@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   uint64_t* empty = full + kStages;      // [stage] K/V consumed by every group
   uint64_t* sfull = empty + kStages;     // [group] S computed
   uint64_t* sfree = sfull + kGroups;     // [group] S read by the softmax
-  uint64_t* pfull = sfree + kGroups;     // [group] P written
-  uint64_t* ofull = pfull + kGroups;     // [group][P buffer] P V done (O updated, buffer free)
+  uint64_t* pfull = sfree + kGroups;     // [group][P buffer] P written
+  uint64_t* ofull = pfull + 2 * kGroups; // [group][P buffer] P V done (O updated, buffer free)
   uint64_t* drained = ofull + 2 * kGroups;
   uint64_t* qfull = drained + kGroups;   // Q of every group landed (TMA path)
   __shared__ uint32_t s_tmem;
@@ -262,7 +262,8 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     for (int a = 0; a < kGroups; ++a) {
       mbar_init(&sfull[a], 1);
       mbar_init(&sfree[a], 4);
-      mbar_init(&pfull[a], 4);
+      mbar_init(&pfull[2 * a], 4);
+      mbar_init(&pfull[2 * a + 1], 4);
       mbar_init(&ofull[2 * a], 1);
       mbar_init(&ofull[2 * a + 1], 1);
     }
@@ -412,7 +413,9 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         return true;
       };
       auto issue_pv = [&](int t) -> bool {
-        if (!mbar_wait_bounded(&pfull[ga], t & 1, &s_abort)) return false;
+        // one barrier per P buffer: the softmax may finish tile t + 1 before this wait for tile t
+        // begins, but never tile t + 2 (it needs S(t + 2), issued after this P V)
+        if (!mbar_wait_bounded(&pfull[2 * ga + (t & 1)], (t >> 1) & 1, &s_abort)) return false;
         tc_fence_after();
         const uint32_t pt = tmem + C::kColP + (2 * ga + (t & 1)) * (kKT / 2);  // P(t) in TMEM
         const uint32_t va = smem_u32(sV + (t % kStages) * C::kTile);
@@ -551,7 +554,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&pfull[a]);
+      if (lane == 0) mbar_arrive(&pfull[2 * a + (t & 1)]);
     }
     const bool fin = ok && mbar_wait_bounded(&ofull[2 * a + ((T - 1) & 1)], ((T - 1) >> 1) & 1, &s_abort);
     // Once every group's last P V has completed, no MMA or copy reads or writes the Q / K / V / P
