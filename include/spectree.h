@@ -116,7 +116,9 @@ typedef struct spec_attn_args {
   int32_t reserved1;      /* must be 0 */
 } spec_attn_args;
 
-/* Bytes of workspace spec_tree_attention needs for these shapes (0 on invalid args). */
+/* Bytes of workspace spec_tree_attention needs for these shapes (0 on invalid args).  The
+ * workspace (device memory, 16-byte aligned: the split partials are written there by bulk
+ * copies; SPEC_ERR_INVALID_ARGUMENT otherwise) holds the per-split partial outputs. */
 size_t spec_tree_attention_workspace(const spec_attn_args* args);
 
 spec_status spec_tree_attention(const spec_attn_args* args, void* workspace,

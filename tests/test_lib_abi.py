@@ -106,7 +106,14 @@ def test_workspace_queries_are_host_only(L):
     fake = ctypes.c_void_p(1 << 20)  # aligned non-null pointers, never dereferenced by the query
     a = st.AttnArgs(dtype=1, batch=2, n_max=63, num_q_heads=32, num_kv_heads=8, head_dim=128, kv_capacity=4096,
                     q=fake, k_cache=fake, v_cache=fake, prefix_len=fake, n_nodes=fake, parent=fake, out=fake)
-    assert L.spec_tree_attention_workspace(ctypes.byref(a)) > 2 * 63 * 32 * 128 * 4
+    need = L.spec_tree_attention_workspace(ctypes.byref(a))
+    assert need > 2 * 63 * 32 * 128 * 4
+    # the partials leave through bulk copies, so a workspace off a 16-byte boundary is refused
+    # before anything is launched (as are a missing one and a short one)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert L.spec_tree_attention(ctypes.byref(a), odd, need, None, None) == 1
+    assert L.spec_tree_attention(ctypes.byref(a), None, need, None, None) == 1
+    assert L.spec_tree_attention(ctypes.byref(a), fake, need - 1, None, None) == 3
     v = st.VerifyArgs(dtype=1, batch=1, n_max=63, hidden=4096, vocab=128256, rule=2, temperature=1.0,
                       draft_vocab=128256, path_cap=64, hidden_states=fake, lm_head_weight=fake, tokens=fake,
                       parent=fake, n_nodes=fake, draft_probs=fake, accept_len=fake, path=fake, bonus_token=fake)
