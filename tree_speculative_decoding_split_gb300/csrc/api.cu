@@ -320,10 +320,11 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
       if (!make_map_bf16(&tmQ, a->q, 4, qd, qs, qb)) return SPEC_ERR_CUDA;
       p.q_tma = 1;
     }
+    p.direct = p.n_split == 1 ? 1 : 0;
     record(a->timing_begin, stream);
     if (launch_attention_tc(&tmQ, &tmK, &tmV, p, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     record(a->timing_end, stream);
-    launch_attention_merge_bf16(p, stream);
+    if (!p.direct) launch_attention_merge_bf16(p, stream);
   }
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -156,9 +156,22 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   }
   bad_tree = __syncthreads_or(bad_tree);
   bad_cap = __syncthreads_or(bad_cap);
+  // With a single split the kernel writes the final rows itself (no merge); rows it does not
+  // compute (bad request, padded node) are zeroed here as the merge would.
+  auto zero_rows = [&]() {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    for (int c = tid; c < kRowsCta * (D / 8); c += kTcThreads) {
+      const int rr = c / (D / 8), row = row0 + rr;
+      if (row >= rows_total) continue;
+      const size_t orow = ((size_t)b * p.N + row / p.G) * p.Hq + g * p.G + row % p.G;
+      *reinterpret_cast<uint4*>(out + orow * D + (c % (D / 8)) * 8) = make_uint4(0, 0, 0, 0);
+      if (p.lse && c % (D / 8) == 0) p.lse[orow] = 0.f;
+    }
+  };
   const int err = bad_tree ? SPEC_ERR_BAD_TREE : (bad_cap ? SPEC_ERR_CAPACITY : 0);
-  if (err) {  // the merge kernel zeroes this request's outputs
+  if (err) {  // the merge kernel (or, with one split, this CTA) zeroes this request's outputs
     if (tid == 0 && rg == 0 && split == 0 && g == 0) set_status(p.dev_status, err);
+    if (p.direct) zero_rows();
     return;
   }
   // Split s covers keys [s * chunk, (s + 1) * chunk); the split holding key L (the first tree
@@ -184,9 +197,17 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       p.req_bad[b] = badt;
       if (badt && rg == 0 && g == 0) set_status(p.dev_status, SPEC_ERR_CAPACITY);
     }
+    if (badt && p.direct) {
+      zero_rows();
+      return;
+    }
   }
   const int T = ke > kb ? (int)((ke - t0 + kKT - 1) / kKT) : 0;
   if (T == 0) {  // no keys here: the merge skips this split
+    if (p.direct) {
+      zero_rows();
+      return;
+    }
     for (int rr = tid; rr < kRowsCta; rr += kTcThreads) {
       if (row0 + rr >= rows_total) break;
       const int row = row0 + rr, i = row / p.G, h = g * p.G + row % p.G;
@@ -556,21 +577,54 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&pfull[2 * a + (t & 1)]);
     }
-    const bool fin = ok && mbar_wait_bounded(&ofull[2 * a + ((T - 1) & 1)], ((T - 1) >> 1) & 1, &s_abort);
+    // the TMEM loads below are warp-collective: the warp takes one branch
+    const bool fin = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&ofull[2 * a + ((T - 1) & 1)], ((T - 1) >> 1) & 1, &s_abort));
     // Once every group's last P V has completed, no MMA or copy reads or writes the Q / K / V / P
     // region any more: the O rows are staged there and leave through the bulk-copy engine.
     named_bar_sync(1, 128 * kGroups);
     const bool valid = row < rows_total;
+    const int i_node = row / p.G;
     size_t orow = 0;
-    if (valid) {
-      const int i = row / p.G, hq = g * p.G + row % p.G;
-      orow = ((size_t)b * p.N + i) * p.Hq + hq;
-    }
-    if (fin) {
+    if (valid) orow = ((size_t)b * p.N + i_node) * p.Hq + g * p.G + row % p.G;
+    uint8_t* srow = base + rr * C::kORow;
+    if (p.direct) {
+      // one split: the final bf16 row and its natural-log LSE (zeros for padded nodes and after a
+      // failed wait)
+      const bool live = fin && i_node < n;
+      if (fin) tc_fence_after();
+      const float inv = (live && l_run > 0.f) ? 1.f / l_run : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (fin) {
+          tmem_ld_x32(tO + c * 32, o);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 8)
+          *reinterpret_cast<uint4*>(srow + (c * 32 + j) * 2) =
+              make_uint4(pack_bf16x2(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv),
+                         pack_bf16x2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv),
+                         pack_bf16x2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv),
+                         pack_bf16x2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv));
+      }
+      if (valid) {
+        if (p.lse) p.lse[orow] = (live && l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : 0.f;
+        fence_proxy_async_smem();
+        bulk_store_row(static_cast<__nv_bfloat16*>(p.out) + orow * D, srow, D * 2);
+        bulk_wait_read();
+      }
+      if (!fin && lane == 0) {
+        s_abort = 1;
+        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+      }
+    } else if (fin) {
       tc_fence_after();
       if (valid) p.part_ml[orow * p.n_split + split] = make_float2(m_run, l_run);
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint8_t* srow = base + rr * C::kORow;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];

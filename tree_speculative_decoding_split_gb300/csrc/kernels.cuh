@@ -44,6 +44,7 @@ struct AttnParams {
   int bs, bs_shift, max_blocks, num_blocks;
   int32_t* req_bad;  // [B] written by the tail CTAs: the request's table has an entry out of range
   int q_tma;         // bf16: Q rows arrive by TMA through the (d, Hq, N, B) map (128 % G == 0)
+  int direct;        // bf16, one split: the kernel writes out / lse itself and no merge runs
 };
 
 struct AttnPlan {
