@@ -117,7 +117,7 @@ spec_status check_attn(const spec_attn_args* a) {
 }
 
 struct AttnLayout {
-  int32_t* depth; uint32_t* anc; int32_t* bad; float* part_o; float2* part_ml;
+  int32_t* depth; uint32_t* anc; int32_t* bad; int32_t* tree_bad; float* part_o; float2* part_ml;
   AttnPlan plan;
   size_t bytes;
 };
@@ -131,6 +131,7 @@ AttnLayout layout_attn(const spec_attn_args* a, void* ws) {
   l.depth = c.take<int32_t>((size_t)B * N);
   l.anc = c.take<uint32_t>((size_t)B * N * W);
   l.bad = c.take<int32_t>(B);
+  l.tree_bad = c.take<int32_t>(B);
   l.part_o = nullptr;
   l.part_ml = nullptr;
   if (a->dtype == SPEC_DTYPE_BF16) {
@@ -270,6 +271,7 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
   p.n_nodes = a->n_nodes;
   p.anc = l.anc;
   p.bad = l.bad;
+  p.tree_bad = l.tree_bad;
   p.parent = a->parent;
   p.part_o = l.part_o;
   p.part_ml = l.part_ml;

@@ -20,7 +20,7 @@ constexpr int kKT = 64;    // keys per tile of the bf16 kernel (split sizes are 
 }  // namespace
 
 // K1m: merge of the splits, one warp per output row (b, i, h); lane s holds split s.  Requests
-// with an invalid tree (checked again here: a handful of loads per warp) get zero outputs.
+// whose tree, capacity or block table the attention kernel found invalid get zero outputs.
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_bf16_kernel(const AttnParams p) {
   constexpr int EPL = D / 32;  // elements per lane, contiguous
@@ -32,15 +32,8 @@ __global__ void __launch_bounds__(256) attn_merge_bf16_kernel(const AttnParams p
   const int i = (int)((orow / p.Hq) % p.N);
   const int n = p.n_nodes[b];
   const long long L = p.prefix_len[b];
-  bool zero = n < 1 || n > p.N || i >= n || L < 0 || L + n > p.L_cap || (p.table && p.req_bad[b]);
-  if (!zero) {
-    bool bad = false;
-    for (int c = lane; c < n; c += 32) {
-      const int par = p.parent[(size_t)b * p.N + c];
-      bad |= (c == 0) ? par != -1 : (par < 0 || par >= c);
-    }
-    zero = __any_sync(0xffffffffu, bad);
-  }
+  const bool zero = n < 1 || n > p.N || i >= n || L < 0 || L + n > p.L_cap || p.tree_bad[b] ||
+                    (p.table && p.req_bad[b]);
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D + lane * EPL;
   if (zero) {
 #pragma unroll

@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     }
   };
   const int err = bad_tree ? SPEC_ERR_BAD_TREE : (bad_cap ? SPEC_ERR_CAPACITY : 0);
+  if (tid == 0 && split == 0 && rg == 0 && g == 0) p.tree_bad[b] = err ? 1 : 0;  // for the merge
   if (err) {  // the merge kernel (or, with one split, this CTA) zeroes this request's outputs
     if (tid == 0 && rg == 0 && split == 0 && g == 0) set_status(p.dev_status, err);
     if (p.direct) zero_rows();
