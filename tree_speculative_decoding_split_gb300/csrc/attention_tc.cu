@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   // the swizzled tile); keys below kb are masked.  Contiguous: tiles start at kb.
   const bool paged = p.table != nullptr;
   const long long t0 = paged ? (kb & ~(long long)(kKT - 1)) : kb;
-  if (paged && tail) {  // every tail CTA of the request checks its whole table (same verdict)
+  if (paged && tail) {  // every tree-split CTA of the request checks its whole table (same verdict)
     const long long used = (L + n + p.bs - 1) >> p.bs_shift;
     int badt = 0;
     for (long long j = tid; j < used; j += kTcThreads) {
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     return;
   }
 
-  // ---- ancestor bits of this CTA's rows (tail split) ----
+  // ---- ancestor bits of this CTA's rows (tree split) ----
   if (tail) {
     // pointer jumping: s_nanc[c] = nodes from c up to, not including, s_jmp[c]
     for (int c = tid; c < n; c += kTcThreads) {
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     const uint32_t tO = tmem + C::kColO + a * D + lane_off;
     const uint32_t tP = tmem + C::kColP + 2 * a * (kKT / 2) + lane_off;  // + (t & 1) * kKT / 2
     float m_run = -INFINITY, l_run = 0.f;
-    const uint32_t* anc = sAnc + rr * kAncWords;  // this row's ancestor words (tail split)
+    const uint32_t* anc = sAnc + rr * kAncWords;  // this row's ancestor words (tree split)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       if (!mbar_wait_bounded(&sfull[a], t & 1, &s_abort)) {

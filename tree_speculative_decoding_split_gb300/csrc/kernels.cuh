@@ -42,7 +42,7 @@ struct AttnParams {
   // paged KV (bf16): pools [num_blocks][Hkv][bs][d]; table [B][max_blocks]; nullptr = contiguous
   const int32_t* table;
   int bs, bs_shift, max_blocks, num_blocks;
-  int32_t* req_bad;  // [B] written by the tail CTAs: the request's table has an entry out of range
+  int32_t* req_bad;  // [B] written by the tree-split CTAs: the request's table has an entry out of range
   int32_t* tree_bad; // [B] bf16: written by CTA (split 0, row group 0, KV head 0) of each request --
                      // the request's tree or capacity check failed (the merge zeroes its rows)
   int q_tma;         // bf16: Q rows arrive by TMA through the (d, Hq, N, B) map (128 % G == 0)
