@@ -121,3 +121,23 @@ def test_workspace_queries_are_host_only(L):
     assert need >= 63 * 128256 * 4  # rejection keeps the fp32 logits
     v.rule = 0
     assert L.spec_verify_accept_workspace(ctypes.byref(v)) < need
+
+
+def test_attention_split_plan_from_the_workspace_query(L):
+    """The key-split count shows in the workspace (fp32 partials per split).  A batch of 32
+    4096-token prefixes (256 CTAs of 65 key tiles fill more than one round of SMs) runs one split
+    per KV head; a single 2048-token request is cut into 4-tile splits so that its 16 row groups
+    reach every SM."""
+    fake = ctypes.c_void_p(1 << 20)
+
+    def splits(B, L_cap):
+        a = st.AttnArgs(dtype=1, batch=B, n_max=63, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        kv_capacity=L_cap, q=fake, k_cache=fake, v_cache=fake, prefix_len=fake,
+                        n_nodes=fake, parent=fake, out=fake)
+        rows = B * 63 * 32
+        ws = L.spec_tree_attention_workspace(ctypes.byref(a))
+        return ws // (rows * (128 * 4 + 8))  # everything else in the workspace is far smaller
+
+    assert splits(32, 4096 + 63) == 1
+    assert splits(1, 2048 + 63) == 9
+
