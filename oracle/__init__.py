@@ -17,7 +17,9 @@ attention for single-chain trees and against plain decoding for a single node; r
 against closed forms and library routines; path selection against the invariants of [GUIDE]
 section "棄却サンプリング" and [MTP] section "ツリー検証"; rejection sampling against the target
 distribution by a chi-square test over 10^6 seeded trials (with a planted-mistake negative
-control); Philox against an independent library implementation; Medusa expansion against the
+control); the margin detector (greedy gap, typical log-ratio, rejection ratio band, bonus
+window) and the draft-to-target scatter against hand-computed cases; Philox against an
+independent library implementation; Medusa expansion against the
 18-path example of [GLOSS] section "ツリー構造の候補構築", brute-force top-k and the input
 generator's independent topology builder.  Nothing is "parity unpinned".
 """
@@ -27,7 +29,7 @@ from .tree import (validate_tree, ancestors_or_self, depths, tree_mask, root_to_
                    children)
 from .attention import tree_attention, tree_attention_rows  # noqa: F401
 from .lmhead import logits, row_stats  # noqa: F401
-from .accept import verify_request, verify_accept, MARGIN  # noqa: F401
+from .accept import verify_request, verify_accept, draft_in_target_vocab, MARGIN  # noqa: F401
 from .compact import compact_kv  # noqa: F401
 from .medusa import head_topk, cartesian_tuples, pruned_topology, medusa_expand  # noqa: F401
 from .paged import gather_paged, scatter_paged  # noqa: F401

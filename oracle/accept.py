@@ -159,6 +159,21 @@ def verify_request(parent, n, tokens, z, rule, tau, eps, delta, seed, b, draft_r
                 path_margins=margins, bonus_margin=bool(near), bonus_window=(lo, hi))
 
 
+def draft_in_target_vocab(draft_row, draft_to_target, V):
+    """The draft distribution of one node in the target vocabulary (float64 [V]).
+
+    With a draft-to-target id map (EAGLE-3's smaller draft vocabulary), draft entry j lands on
+    target id draft_to_target[j] and every target id outside the map has draft probability 0;
+    without a map the row is already in the target vocabulary.
+    """
+    row = np.asarray(draft_row, dtype=np.float64)
+    if draft_to_target is None:
+        return row.copy()
+    De = np.zeros(V)
+    De[np.asarray(draft_to_target)] = row
+    return De
+
+
 def verify_accept(hidden, W, tokens, parent, n_nodes, rule, tau, eps, delta, seed,
                   draft_probs=None, draft_to_target=None, requests=None):
     """Verify a batch.  hidden [B][N][Hd], W [V][Hd] (float32 holding exact values, or float64).
@@ -180,10 +195,6 @@ def verify_accept(hidden, W, tokens, parent, n_nodes, rule, tau, eps, delta, see
         draft_row = None
         if rule == "rejection":
             def draft_row(e, b=b):
-                if draft_to_target is None:
-                    return np.asarray(draft_probs[b, e], dtype=np.float64)
-                De = np.zeros(V)
-                De[np.asarray(draft_to_target)] = np.asarray(draft_probs[b, e], dtype=np.float64)
-                return De
+                return draft_in_target_vocab(draft_probs[b, e], draft_to_target, V)
         out[b] = verify_request(parent[b], n, tokens[b], z, rule, tau, eps, delta, seed, b, draft_row)
     return out
