@@ -3,15 +3,21 @@
 
 A step is the whole verification hot path over one batch: tree attention (one layer), LM head +
 acceptance + longest accepted path, and KV compaction -- the three C-ABI calls
-spec_tree_attention, spec_verify_accept and spec_compact_kv.  The workload is the Llama-3.1-8B
-shaped layer with batch 1, a 2048-token prefix, the static 63-node Medusa-style tree and typical
-acceptance (eps 0.09, delta 0.3).  Metric: verified tree-tokens/s (tree nodes verified per second).
+spec_tree_attention, spec_verify_accept and spec_compact_kv, launched as one captured round.
+Metric: verified tree-tokens/s (tree nodes verified per second).
+
+The headline workload is the largest one that fits one GPU: a 70B-shaped layer (64 query heads,
+8 KV heads, head_dim 128, hidden 8192, vocabulary 128256, bf16), batch 4 with prefixes of 32768,
+65536, 98304 and 131072 tokens, 255-node trees (depth <= 8, branching 1-4), greedy acceptance.
+The EAGLE-3-shaped batch-32 workload (8B layer, prefix 4096, dynamic 63-node trees, mapped
+draft vocabulary, rejection sampling) is measured in the same run and reported as a second full
+line under "second_workload".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
 Under torchrun each rank runs an independent replica on its own GPU (the path needs no exchange);
 the JSON line reports the whole-job rate from the slowest rank.  ``--impl reference`` times the
-fp64 CPU oracle on the host cores instead.
+fp64 CPU oracle on the host cores instead, one bounded sample per step.
 """
 
 import argparse
@@ -19,7 +25,6 @@ import ctypes
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -30,16 +35,25 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verified tree-tokens/s per GB300 and % of roofline (HBM / bf16 TC) vs CPU oracle"
 UNIT = "tree-tokens/s"
-WORKLOAD = 2  # gen.configs: llama8b-b1-l2048-medusa63-typical
+WORKLOAD = 5         # gen.configs: llama70b-b4-l32kto128k-bfs255-greedy (largest single-GPU workload)
+SECOND_WORKLOAD = 4  # gen.configs: eagle3-llama8b-b32-l4096-dynamic63-rejection
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+CSRC = os.path.join(ROOT, "tree_speculative_decoding_split_gb300", "csrc")
+# kernel -> the source files its counters depend on (a committed traffic figure is used only
+# while these are unchanged)
+KERNEL_SOURCES = {
+    "attn_tc_kernel": ["attention_tc.cu", "tc_ptx.cuh", "common.cuh"],
+    "lmhead_tc_kernel": ["lmhead.cu", "tc_ptx.cuh", "common.cuh"],
+    "lmhead_tc_rows_kernel": ["lmhead.cu", "tc_ptx.cuh", "common.cuh"],
+}
 
 
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -48,6 +62,13 @@ def _args():
                         "direct: the three C-ABI calls per step")
     p.add_argument("--workload", type=int, default=WORKLOAD,
                    help="gen.configs workload id (the headline metric is quoted on the default)")
+    p.add_argument("--second-workload", type=int, default=SECOND_WORKLOAD,
+                   help="workload reported as a second full line (0: none)")
+    p.add_argument("--no-next", action="store_true", help="leave out the next_rows measurements")
+    p.add_argument("--profile", action="store_true",
+                   help="profiling harness: run the workload's three calls --warmup + --steps times "
+                        "without timing anything and print nothing (for ncu)")
+    p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     return p.parse_args()
 
 
@@ -77,6 +98,8 @@ def _threads_used():
 
 def _work(case):
     """Algorithmic bytes / flops of the step and of its kernels (no tile re-reads counted)."""
+    import numpy as np
+    from gen import trees as T
     nodes = int(case.n_nodes.sum())
     rows = case.B * case.N
     kv_bytes = sum(2 * case.Hkv * (int(case.prefix_len[b]) + int(case.n_nodes[b])) * case.d * 2
@@ -86,25 +109,52 @@ def _work(case):
     h_bytes = rows * case.Hd * 2
     logits_bytes = rows * case.V * 4 if case.rule == "rejection" else 0
     lm_flops = 2.0 * rows * case.Hd * case.V
-    attn_flops = sum(4.0 * case.d * case.Hq * int(case.n_nodes[b]) * int(case.prefix_len[b]) for b in range(case.B))
+    # prefix keys for every node, plus each node's ancestors-or-self among the tree keys
+    tree_keys = sum(int((T.depths(case.parent[b, : case.n_nodes[b]]) + 1).sum()) for b in range(case.B))
+    attn_flops = 4.0 * case.d * case.Hq * (sum(int(case.n_nodes[b]) * int(case.prefix_len[b])
+                                               for b in range(case.B)) + tree_keys)
     return dict(nodes=nodes, kv_bytes=kv_bytes, qo_bytes=qo_bytes, w_bytes=w_bytes, h_bytes=h_bytes,
                 logits_bytes=logits_bytes, lm_flops=lm_flops, attn_flops=attn_flops,
-                lm_kernel_bytes=w_bytes + h_bytes + logits_bytes, attn_kernel_bytes=kv_bytes + qo_bytes)
+                lm_kernel_bytes=w_bytes + h_bytes + logits_bytes, attn_kernel_bytes=kv_bytes + qo_bytes,
+                tree_keys=int(np.int64(tree_keys)))
 
 
-def _traffic_from_profile(kernel_file):
-    """DRAM bytes per launch of the LM-head kernel from the committed ncu summary, if the kernel source
-    is unchanged since the counters were taken (else None)."""
-    prof = os.path.join(ROOT, "profiles", "lmhead_tc_llama8b_b1_medusa63.md")
-    if not os.path.exists(prof):
+def _sources_sha(kernel):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kernel, []):
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()
+
+
+def traffic_entry(kernel, workload):
+    """DRAM read + write bytes per launch of ``kernel`` on ``workload`` from the committed ncu
+    summary profiles/traffic.json, if the kernel's sources are unchanged since the counters were
+    taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
         return None
-    text = open(prof).read()
-    m_t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    m_h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    if not (m_t and m_h):
-        return None
-    src = hashlib.sha256(open(kernel_file, "rb").read()).hexdigest()
-    return int(m_t.group(1)) if src == m_h.group(1) else None
+    for e in json.load(open(path)).get("entries", []):
+        if e.get("kernel") == kernel and e.get("workload") == workload:
+            if e.get("sources_sha256") == _sources_sha(kernel):
+                return e
+    return None
+
+
+def _roofline(kernel, flops, nbytes, ms, hbm, tc, peak_kind, workload):
+    """Roofline object of one kernel: the binding roof among HBM bytes and bf16 tensor FLOPs."""
+    t_bytes = nbytes / (hbm * 1e9)
+    t_flops = flops / (tc * 1e12)
+    e = traffic_entry(kernel, workload)
+    traffic = e["traffic_bytes_per_launch"] if e else None
+    if t_flops > t_bytes:
+        ach = flops / (ms * 1e-3) / 1e12
+        return {"kernel": kernel, "bound": "tensor", "achieved": ach, "peak": tc, "unit": "TFLOP/s", "frac": ach / tc,
+                "traffic": traffic, "algorithmic_flops": flops, "algorithmic_bytes": nbytes, "ms": ms,
+                "peak_source": f"{peak_kind} bf16_tflops (burst)"}
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+            "traffic": traffic, "algorithmic_bytes": nbytes, "algorithmic_flops": flops, "ms": ms,
+            "peak_source": f"{peak_kind} hbm_gbs"}
 
 
 # ---- clocks -------------------------------------------------------------------------------------
@@ -116,10 +166,9 @@ class ClockSampler:
 
     def __init__(self, gpu_index):
         self.proc = None
-        self.gpu = gpu_index
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                          "-lms", "50", "-i", str(gpu_index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -190,28 +239,49 @@ def _device_tensors(case, dev):
                 map=None if case.draft_to_target is None else t(case.draft_to_target.astype(np.int32)))
 
 
-def _launches_per_step(case):
-    attn = 3 if case.dtype == "bf16" else 2                   # tree prep, split-KV, merge | prep, fp32 rows
-    verify = 2 if case.dtype == "bf16" else 3                  # LM head (+stats) [+ fp32 stats], row finalise
+def _attention_splits(L, aa, case):
+    """Key splits of the attention plan, read back from the workspace query (fp32 partials of
+    d + 2 floats per row and split dominate it)."""
+    rows = case.B * case.N * case.Hq
+    return max(1, int(L.spec_tree_attention_workspace(ctypes.byref(aa)) // (rows * (case.d * 4 + 8))))
+
+
+def _launches_per_step(case, n_split):
+    attn = (2 if n_split > 1 else 1) if case.dtype == "bf16" else 2   # split-KV [+ merge] | prep + fp32 rows
+    verify = 2 if case.dtype == "bf16" else 3                          # LM head, row finalise [+ fp32 stats]
     if case.rule == "rejection":
-        verify += 1                                            # rejection walk
+        verify += 1                                                    # rejection walk
         if case.draft_to_target is not None:
-            verify += 1                                        # draft-map inversion
-    return attn + verify + 1                                   # + compaction
+            verify += 1                                                # draft-map inversion
+    return attn + verify + 1                                           # + compaction
 
 
-def run_native(a, rank, world, dist):
+class _Flush:
+    """Writes, then reads back, a buffer twice the size of L2, so that the next step starts from a
+    cold L2 of clean lines (the flush's write-backs are not charged to the step)."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.sink = torch.empty(1, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        import torch
+        self.buf.zero_()
+        torch.sum(self.buf.view(torch.int64), dim=0, keepdim=True, out=self.sink)
+
+
+def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
+    """Times the workload's verification step and returns its JSON line (rank 0) or None."""
     import numpy as np
     import torch
     import tree_speculative_decoding_split_gb300 as st
     from gen import make_config_case
 
-    st.build()
     L = st.lib()
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    case = make_config_case(a.workload, seed=a.seed + rank)
+    case = make_config_case(cfg, seed=seed)
     t = _device_tensors(case, dev)
     stream = torch.cuda.current_stream()
     sp = ctypes.c_void_p(stream.cuda_stream)
@@ -226,14 +296,8 @@ def run_native(a, rank, world, dist):
     ws_a = torch.empty(need_a, dtype=torch.uint8, device=dev)
     ws_v = torch.empty(need_v, dtype=torch.uint8, device=dev)
     pa, pv, pst = ctypes.c_void_p(ws_a.data_ptr()), ctypes.c_void_p(ws_v.data_ptr()), ctypes.c_void_p(status.data_ptr())
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_sink = torch.empty(1, dtype=torch.int64, device=dev)
-
-    def l2_flush():
-        # write a buffer twice the size of L2, then read it back, so that the step starts from a
-        # cold L2 holding clean lines (no write-backs of the flush charged to the step)
-        flush.zero_()
-        torch.sum(flush.view(torch.int64), dim=0, keepdim=True, out=flush_sink)
+    l2_flush = _Flush(dev)
+    n_split = _attention_splits(L, aa, case)
 
     def step():
         c1 = L.spec_tree_attention(ctypes.byref(aa), pa, need_a, pst, sp)
@@ -242,18 +306,29 @@ def run_native(a, rank, world, dist):
         if c1 or c2 or c3:
             raise RuntimeError(f"C ABI returned {c1} {c2} {c3}")
 
+    def check_status():
+        if int(status.item()) != 0:
+            raise RuntimeError("device status " + st.status_string(int(status.item())))
+
+    if a.profile:
+        for _ in range(max(1, a.warmup) + max(1, a.steps)):
+            step()
+        torch.cuda.synchronize()
+        check_status()
+        return None
+
     def events(n):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         for e in evs:
             e.record(stream)  # materialise the underlying cudaEvent_t
         return evs
 
-    for _ in range(max(3, a.warmup)):
+    W = max(3, a.warmup)
+    for _ in range(W):
         l2_flush()
         step()
     torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError("device status " + st.status_string(int(status.item())))
+    check_status()
 
     K = a.steps
 
@@ -286,13 +361,36 @@ def run_native(a, rank, world, dist):
         torch.cuda.synchronize()
         return [ev_s[i].elapsed_time(ev_e[i]) for i in range(n)]
 
-    rnd = None
-    if a.mode == "graph":
-        rnd = st.Round(aa, va, ca, dev_status=status)
-        for _ in range(max(3, a.warmup)):
-            l2_flush()
-            rnd.launch(stream)
-        torch.cuda.synchronize()
+    rnd = st.Round(aa, va, ca, dev_status=status)
+    for _ in range(W):
+        l2_flush()
+        rnd.launch(stream)
+    torch.cuda.synchronize()
+
+    # ---- end to end through spec_round_launch_host: pinned host inputs -> device, the round,
+    # results -> pinned host, one C call per step ----
+    n_tree = int(case.n_nodes.max())
+    Lp = [int(x) for x in case.prefix_len]
+    step_inputs = ["q", "hidden", "tokens", "parent", "n_nodes", "prefix_len"]
+    if t["draft"] is not None:  # rejection sampling: the draft distributions arrive with every step
+        step_inputs.append("draft")
+    host = {k: t[k].cpu().pin_memory() for k in step_inputs}
+    ins = [st.host_copy(host[k], t[k]) for k in step_inputs]
+    for b in range(case.B):  # the tree's new K/V rows, one strided copy per request and cache
+        for name in ("k", "v"):
+            rows = t[name][b, :, Lp[b]: Lp[b] + n_tree].contiguous().cpu().pin_memory()
+            host[f"{name}_tree_{b}"] = rows
+            ins.append(st.host_copy(rows, t[name][b, :, Lp[b]: Lp[b] + n_tree], rows=case.Hkv))
+    out_names = ("accept_len", "path", "bonus_token", "margin_count", "bonus_margin")
+    res_host = {k: torch.empty(outs[k].shape, dtype=outs[k].dtype).pin_memory() for k in out_names}
+    res_host["new_len"] = torch.empty(new_len.shape, dtype=new_len.dtype).pin_memory()
+    outs_c = [st.host_copy(res_host[k], outs[k]) for k in out_names] + [st.host_copy(res_host["new_len"], new_len)]
+    h2d = sum(c.row_bytes * c.rows for c in ins)
+    d2h = sum(c.row_bytes * c.rows for c in outs_c)
+    for _ in range(3):
+        l2_flush()
+        rnd.launch_host(ins, outs_c, stream)
+    torch.cuda.synchronize()
 
     torch.cuda.synchronize()
     if dist:
@@ -302,148 +400,126 @@ def run_native(a, rank, world, dist):
     time.sleep(0.3)
     # Per-kernel device times (the roofline's inputs) come from the direct calls, whose
     # library-recorded events bracket the attention and LM-head kernels; events recorded inside
-    # a CUDA graph are not timable.  In graph mode the step time comes from the round's launches.
+    # a CUDA graph are not timable.  The step time comes from the round's launches.
     direct_ms, attn_ms, lm_ms = timed_direct(K)
-    step_ms = timed_graph(rnd, K) if rnd is not None else direct_ms
-    clk = clocks.stop()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ms = statistics.fmean(step_ms)
-    other_ms = statistics.fmean(direct_ms) if rnd is not None else None
-    if int(status.item()) != 0:
-        raise RuntimeError("device status " + st.status_string(int(status.item())))
-
-    # ---- end to end: pinned host inputs -> device, the three calls, results -> pinned host ----
-    n_tree = int(case.n_nodes.max())
-    host = {}
-    host["q"] = t["q"].cpu().pin_memory()
-    host["hidden"] = t["hidden"].cpu().pin_memory()
-    host["tokens"] = t["tokens"].cpu().pin_memory()
-    host["parent"] = t["parent"].cpu().pin_memory()
-    host["n_nodes"] = t["n_nodes"].cpu().pin_memory()
-    host["prefix_len"] = t["prefix_len"].cpu().pin_memory()
-    Lp = [int(x) for x in case.prefix_len]
-    host["k_tree"] = [t["k"][b, :, Lp[b]:Lp[b] + n_tree].contiguous().cpu().pin_memory() for b in range(case.B)]
-    host["v_tree"] = [t["v"][b, :, Lp[b]:Lp[b] + n_tree].contiguous().cpu().pin_memory() for b in range(case.B)]
-    res_host = {k: torch.empty(outs[k].shape, dtype=torch.int32).pin_memory() for k in ("accept_len", "path", "bonus_token")}
-    nl_host = torch.empty(new_len.shape, dtype=torch.int32).pin_memory()
-    step_inputs = ["q", "hidden", "tokens", "parent", "n_nodes", "prefix_len"]
-    if t["draft"] is not None:  # rejection sampling: the draft distributions arrive with every step
-        host["draft"] = t["draft"].cpu().pin_memory()
-        step_inputs.append("draft")
-    h2d = sum(host[k].numel() * host[k].element_size() for k in step_inputs)
-    h2d += sum(x.numel() * x.element_size() for x in host["k_tree"] + host["v_tree"])
-    d2h = sum(x.numel() * 4 for x in res_host.values()) + nl_host.numel() * 4
-
-    def e2e_step():
-        for k in step_inputs:
-            t[k].copy_(host[k], non_blocking=True)
-        for b in range(case.B):
-            t["k"][b, :, Lp[b]:Lp[b] + n_tree].copy_(host["k_tree"][b], non_blocking=True)
-            t["v"][b, :, Lp[b]:Lp[b] + n_tree].copy_(host["v_tree"][b], non_blocking=True)
-        if rnd is not None:
-            rnd.launch(stream)
-        else:
-            step()
-        for k in res_host:
-            res_host[k].copy_(outs[k], non_blocking=True)
-        nl_host.copy_(new_len, non_blocking=True)
-
+    graph_ms = timed_graph(rnd, K)
+    step_ms = graph_ms if a.mode == "graph" else direct_ms
     KE = max(10, min(K, 500))
-    for _ in range(3):
-        l2_flush()
-        e2e_step()
-    torch.cuda.synchronize()
     es, ee = events(KE), events(KE)
-    if dist:
-        dist.barrier()
     torch.cuda.synchronize()
     for i in range(KE):
         l2_flush()
         es[i].record(stream)
-        e2e_step()
+        rnd.launch_host(ins, outs_c, stream)
         ee[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = statistics.fmean(es[i].elapsed_time(ee[i]) for i in range(KE))
+    e2e_list = [es[i].elapsed_time(ee[i]) for i in range(KE)]
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    check_status()
+    ms = statistics.median(step_ms)
+    other_ms = statistics.median(direct_ms if a.mode == "graph" else graph_ms)
+    e2e_ms = statistics.median(e2e_list)
+    # margin cases (decisions within 1e-4 of their threshold) of the last step, counted on the GPU
+    margins = int(res_host["margin_count"].sum())
+    bonus_margins = int(res_host["bonus_margin"].sum())
+    alen = [int(x) for x in res_host["accept_len"]]
 
-    ms, e2e_ms, other_agg = aggregate_ranks([ms, e2e_ms, other_ms or 0.0], dist, dev)
-    other_ms = other_agg if other_ms is not None else None
+    ms, e2e_ms, other_ms = aggregate_ranks([ms, e2e_ms, other_ms], dist, dev)
     if rank != 0:
+        rnd.close()
         return None
 
     w = _work(case)
     hbm, tc, tc_sus, peak_kind = _peaks()
-    lm_avg = statistics.fmean(lm_ms)
-    attn_avg = statistics.fmean(attn_ms)
-    lm_achieved = w["lm_kernel_bytes"] / (lm_avg * 1e-3) / 1e9
-    lm_tflops = w["lm_flops"] / (lm_avg * 1e-3) / 1e12
-    lm_tc_bound = w["lm_flops"] / (tc * 1e12) > w["lm_kernel_bytes"] / (hbm * 1e9)
-    # the committed counters are for the benchmark workload's LM-head kernel only
-    traffic = (_traffic_from_profile(os.path.join(ROOT, "tree_speculative_decoding_split_gb300", "csrc", "lmhead.cu"))
-               if a.workload == WORKLOAD else None)
+    lm_med = statistics.median(lm_ms)
+    attn_med = statistics.median(attn_ms)
+    lm_kernel = "lmhead_tc_rows_kernel" if case.B * case.N > 64 else "lmhead_tc_kernel"
+    rf_attn = _roofline("attn_tc_kernel", w["attn_flops"], w["attn_kernel_bytes"], attn_med, hbm, tc, peak_kind,
+                        case.name)
+    rf_lm = _roofline(lm_kernel, w["lm_flops"], w["lm_kernel_bytes"], lm_med, hbm, tc, peak_kind, case.name)
+    dominant = rf_attn if attn_med >= lm_med else rf_lm
+    # the benchmark spec's combined roofline of the step: max(KV + weight bytes at HBM bandwidth,
+    # LM-head FLOPs at the bf16 tensor peak); the full one adds every byte and the attention FLOPs
     step_bytes = w["kv_bytes"] + w["qo_bytes"] + w["w_bytes"] + w["h_bytes"] + w["logits_bytes"]
-    t_hbm = step_bytes / (hbm * 1e9)
-    t_tc = (w["lm_flops"] + w["attn_flops"]) / (tc_sus * 1e12)
-    t_ns = max((w["kv_bytes"] + w["w_bytes"]) / (hbm * 1e9), w["lm_flops"] / (tc_sus * 1e12))
+    t_comb = max((w["kv_bytes"] + w["w_bytes"]) / (hbm * 1e9), w["lm_flops"] / (tc * 1e12))
+    t_full = max(step_bytes / (hbm * 1e9), (w["lm_flops"] + w["attn_flops"]) / (tc * 1e12))
     line = {
         "metric": METRIC, "value": job_rate(world, w["nodes"], ms), "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": max(3, a.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": case.name, "batch": case.B, "prefix_len": [int(x) for x in case.prefix_len][:8],
-                   "tree_nodes": int(case.n_nodes[0]), "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d,
-                   "hidden": case.Hd, "vocab": case.V, "rule": case.rule, "eps": case.eps, "delta": case.delta,
-                   "parallelism": f"replicas x{world}", "l2": "flushed before every step (256 MB write, then read)",
+                   "tree_nodes": [int(x) for x in case.n_nodes][:8], "q_heads": case.Hq, "kv_heads": case.Hkv,
+                   "head_dim": case.d, "hidden": case.Hd, "vocab": case.V, "rule": case.rule, "temperature": case.tau,
+                   "eps": case.eps, "delta": case.delta, "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every step (256 MB write, then read)",
                    "launch": ("one CUDA-graph launch of the captured round per step (spec_round_launch)"
-                              if rnd is not None else "three C-ABI calls per step")},
+                              if a.mode == "graph" else "three C-ABI calls per step"),
+                   "statistic": "median over the timed steps"},
         "e2e": {"value": job_rate(world, w["nodes"], e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": K * _launches_per_step(case),
-        "roofline": ({"kernel": "lmhead_tc_kernel (LM head GEMM + row statistics)", "bound": "tensor",
-                      "achieved": lm_tflops, "peak": tc, "unit": "TFLOP/s", "frac": lm_tflops / tc,
-                      "traffic": traffic, "algorithmic_flops": w["lm_flops"], "ms": lm_avg,
-                      "peak_source": f"{peak_kind} bf16_tflops (burst)"} if lm_tc_bound else
-                     {"kernel": "lmhead_tc_kernel (LM head GEMM + row statistics)", "bound": "hbm",
-                      "achieved": lm_achieved, "peak": hbm, "unit": "GB/s", "frac": lm_achieved / hbm,
-                      "traffic": traffic, "algorithmic_bytes": w["lm_kernel_bytes"], "ms": lm_avg,
-                      "peak_source": f"{peak_kind} hbm_gbs"}),
-        "kernels": {"tree_attention_splitkv_ms": attn_avg, "lmhead_ms": lm_avg,
-                    "attention_achieved_gbs": w["attn_kernel_bytes"] / (attn_avg * 1e-3) / 1e9,
-                    "attention_achieved_tflops": w["attn_flops"] / (attn_avg * 1e-3) / 1e12,
-                    "attention_roofline_frac": max(w["attn_kernel_bytes"] / (hbm * 1e9),
-                                                   w["attn_flops"] / (tc * 1e12)) / (attn_avg * 1e-3),
-                    "lmhead_achieved_tflops": lm_tflops},
-        "roofline_step": {"combined_s": t_ns, "frac_combined": t_ns / (ms * 1e-3),
-                          "full_s": max(t_hbm, t_tc), "frac_full": max(t_hbm, t_tc) / (ms * 1e-3),
-                          "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 sustained {tc_sus} TFLOP/s"},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "call": "spec_round_launch_host: pinned host inputs copied in, the round, results copied out"},
+        "gpu_launches": K * _launches_per_step(case, n_split),
+        "roofline": dominant,
+        "roofline_kernels": {"tree_attention": rf_attn, "lm_head": rf_lm},
+        "kernels": {"tree_attention_splitkv_ms": attn_med, "lmhead_ms": lm_med, "attention_key_splits": n_split,
+                    "attention_roofline_frac": rf_attn["frac"], "lmhead_roofline_frac": rf_lm["frac"]},
+        "roofline_step": {"combined_s": t_comb, "frac_combined": t_comb / (ms * 1e-3),
+                          "full_s": t_full, "frac_full": t_full / (ms * 1e-3),
+                          "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 {tc} TFLOP/s (burst)",
+                          "frac_combined_sustained_peak": max((w["kv_bytes"] + w["w_bytes"]) / (hbm * 1e9),
+                                                              w["lm_flops"] / (tc_sus * 1e12)) / (ms * 1e-3)},
+        "margins": {"decisions_within_1e-4": margins, "bonus_within_1e-4": bonus_margins,
+                    "requests": case.B, "accept_len": alen[:8]},
         "clocks": clk,
+        ("direct_calls" if a.mode == "graph" else "graph_round"): {
+            "ms_per_step": other_ms, "value": job_rate(world, w["nodes"], other_ms),
+            "note": "same workload, " + ("the three C-ABI calls per step" if a.mode == "graph" else "one graph launch")},
     }
-    if world == 1:
-        nxt = {}
-        if a.workload == WORKLOAD:
-            nxt["medusa_expand"] = _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm)
-        nxt["eagle_dynamic_tree"] = _bench_eagle(st, L, dev, stream, l2_flush, events, K, case)
-        nxt["paged_attention"] = {f"block_{bs}": _bench_paged(st, L, dev, stream, l2_flush, events, K, case, t, w, hbm, tc,
-                                                              bs, attn_avg) for bs in (16, 64)}
-        line["next_rows"] = nxt
-    if other_ms is not None:
-        line["direct_calls"] = {"ms_per_step": other_ms, "value": job_rate(world, w["nodes"], other_ms),
-                                "note": "same workload, the three C-ABI calls per step instead of the graph"}
-    if world == 1 and not a.no_cpu_baseline and a.workload == WORKLOAD:
-        line["cpu_baseline"] = _cpu_baseline(case)
+    if world == 1 and with_cpu and not a.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, a.cpu_budget)
+    if world == 1 and not a.no_next and cfg == a.workload:
+        line["next_rows"] = {
+            "medusa_expand": _bench_medusa(st, L, dev, stream, l2_flush, events, K, hbm),
+            "eagle_dynamic_tree": _bench_eagle(st, L, dev, stream, l2_flush, events, K),
+            "paged_attention": {f"block_{bs}": _bench_paged(st, L, dev, stream, l2_flush, events, K, t, w, hbm, tc, bs,
+                                                            attn_med) for bs in (16, 64)},
+        }
+    rnd.close()
+    del t, ws_a, ws_v, l2_flush
+    torch.cuda.empty_cache()
     return line
 
 
-def _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm):
-    """Static Medusa expansion at the workload's shapes: B requests, 5 heads of bf16 logits over
-    the vocabulary, the workload's 63-node topology from per-head top-(3, 3, 2, 2, 1)."""
+def _timed_calls(l2_flush, events, stream, call, n):
+    import torch
+    for _ in range(3):
+        l2_flush()
+        call()
+    es, ee = events(n), events(n)
+    torch.cuda.synchronize()
+    for i in range(n):
+        l2_flush()
+        es[i].record(stream)
+        call()
+        ee[i].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(es[i].elapsed_time(ee[i]) for i in range(n))
+
+
+def _bench_medusa(st, L, dev, stream, l2_flush, events, K, hbm):
+    """Static Medusa expansion at the 8B-shaped batch-1 shapes: 5 heads of bf16 logits over the
+    128256-token vocabulary, the 63-node topology from per-head top-(3, 3, 2, 2, 1)."""
     import numpy as np
     import torch
     from gen import bf16 as BF
+    B, V = 1, 128256
     topk_heads = (3, 3, 2, 2, 1)
-    parent, rank = st.medusa_topology(topk_heads, int(case.n_nodes.max()))
+    parent, rank = st.medusa_topology(topk_heads, 63)
     rng = np.random.default_rng(5)
-    x = BF.f32_to_bf16_bits(rng.standard_normal((case.B, len(topk_heads), case.V)).astype(np.float32))
+    x = BF.f32_to_bf16_bits(rng.standard_normal((B, len(topk_heads), V)).astype(np.float32))
     logits = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
     tp, tr = torch.from_numpy(parent).to(dev), torch.from_numpy(rank).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -456,35 +532,23 @@ def _bench_medusa(st, L, dev, stream, l2_flush, events, K, case, hbm):
         if L.spec_medusa_expand(ctypes.byref(ma), pw, need, pst, sp):
             raise RuntimeError("spec_medusa_expand failed")
 
-    for _ in range(3):
-        l2_flush()
-        call()
     n = min(K, 500)
-    es, ee = events(n), events(n)
-    torch.cuda.synchronize()
-    for i in range(n):
-        l2_flush()
-        es[i].record(stream)
-        call()
-        ee[i].record(stream)
-    torch.cuda.synchronize()
+    ms = _timed_calls(l2_flush, events, stream, call, n)
     if int(status.item()) != 0:
         raise RuntimeError("device status " + st.status_string(int(status.item())))
-    ms = statistics.fmean(es[i].elapsed_time(ee[i]) for i in range(n))
     nbytes = logits.numel() * 2
     return {"ms": ms, "steps": n, "bound": "hbm", "bytes": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
             "frac": nbytes / (ms * 1e-3) / 1e9 / hbm, "launches_per_call": 2,
-            "shape": {"batch": case.B, "heads": len(topk_heads), "vocab": case.V, "topk": list(topk_heads),
+            "shape": {"batch": B, "heads": len(topk_heads), "vocab": V, "topk": list(topk_heads),
                       "nodes": int(len(parent)), "dtype": "bf16"}}
 
 
-def _bench_eagle(st, L, dev, stream, l2_flush, events, K, case):
-    """Dynamic draft tree at the workload's batch: one expansion layer (frontier 8, top-8 over a
-    32000-entry draft vocabulary) and the selection of an N-node tree from 8 stacked layers."""
+def _bench_eagle(st, L, dev, stream, l2_flush, events, K):
+    """Dynamic draft tree at the EAGLE-3 batch of 32: one expansion layer (frontier 8, top-8 over a
+    32000-entry draft vocabulary) and the selection of a 63-node tree from 8 stacked layers."""
     import numpy as np
     import torch
-    B, F, k, Vd, D = case.B, 8, 8, 32000, 8
-    N = int(min(case.N, 255))
+    B, F, k, Vd, D, N = 32, 8, 8, 32000, 8, 63
     rng = np.random.default_rng(9)
     z = rng.standard_normal((B, F, Vd)).astype(np.float32)
     lp = torch.from_numpy(z - np.log(np.exp(z.astype(np.float64)).sum(-1, keepdims=True)).astype(np.float32)).to(dev)
@@ -495,30 +559,17 @@ def _bench_eagle(st, L, dev, stream, l2_flush, events, K, case):
     Pn = rng.integers(0, C, (B, D, C)).astype(np.int32)
     Sn = np.zeros((B, D, C), dtype=np.float32)
     Sn[:, 0] = -rng.exponential(1.0, (B, C))
-    for l in range(1, D):
-        Sn[:, l] = np.take_along_axis(Sn[:, l - 1], Pn[:, l], axis=1) - rng.exponential(1.0, (B, C))
+    for layer in range(1, D):
+        Sn[:, layer] = np.take_along_axis(Sn[:, layer - 1], Pn[:, layer], axis=1) - rng.exponential(1.0, (B, C))
     S = torch.from_numpy(Sn).to(dev)
     Tk = torch.from_numpy(rng.integers(0, Vd, (B, D, C)).astype(np.int32)).to(dev)
     P = torch.from_numpy(Pn).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-
-    def timed(call, n):
-        for _ in range(3):
-            l2_flush()
-            call()
-        es, ee = events(n), events(n)
-        torch.cuda.synchronize()
-        for i in range(n):
-            l2_flush()
-            es[i].record(stream)
-            call()
-            ee[i].record(stream)
-        torch.cuda.synchronize()
-        return statistics.fmean(es[i].elapsed_time(ee[i]) for i in range(n))
-
     n = min(K, 300)
-    layer_ms = timed(lambda: st.eagle_expand(lp, fs, k, F, dev_status=status, stream=stream), n)
-    tree_ms = timed(lambda: st.eagle_tree(S, Tk, P, N, dev_status=status, stream=stream), n)
+    layer_ms = _timed_calls(l2_flush, events, stream, lambda: st.eagle_expand(lp, fs, k, F, dev_status=status,
+                                                                              stream=stream), n)
+    tree_ms = _timed_calls(l2_flush, events, stream, lambda: st.eagle_tree(S, Tk, P, N, dev_status=status,
+                                                                           stream=stream), n)
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError("device status " + st.status_string(int(status.item())))
@@ -527,7 +578,7 @@ def _bench_eagle(st, L, dev, stream, l2_flush, events, K, case):
             "note": "timed through the Python binding (argument marshalling included)"}
 
 
-def _bench_paged(st, L, dev, stream, l2_flush, events, K, case, t, w, hbm, tc, bs, contiguous_ms):
+def _bench_paged(st, L, dev, stream, l2_flush, events, K, t, w, hbm, tc, bs, contiguous_ms):
     """Tree attention of the workload with its KV cache scattered over a shuffled block pool."""
     import torch
     B, Hkv, L_cap, d = t["k"].shape
@@ -537,11 +588,12 @@ def _bench_paged(st, L, dev, stream, l2_flush, events, K, case, t, w, hbm, tc, b
     table = torch.randperm(nb, generator=g).reshape(B, mb).to(torch.int32).to(dev)
 
     def pool_of(cache):
-        padded = torch.zeros((B, Hkv, mb * bs, d), dtype=cache.dtype, device=dev)
-        padded[:, :, :L_cap] = cache
-        blocks = padded.view(B, Hkv, mb, bs, d).permute(0, 2, 1, 3, 4).reshape(B * mb, Hkv, bs, d)
-        pool = torch.empty(blocks.shape, dtype=blocks.dtype, device=dev)
-        pool[table.reshape(-1).long()] = blocks
+        pool = torch.empty((nb, Hkv, bs, d), dtype=cache.dtype, device=dev)
+        flat = table.reshape(-1).long()
+        for b in range(B):  # one request at a time keeps the temporary small
+            padded = torch.zeros((Hkv, mb * bs, d), dtype=cache.dtype, device=dev)
+            padded[:, :L_cap] = cache[b]
+            pool[flat[b * mb:(b + 1) * mb]] = padded.view(Hkv, mb, bs, d).permute(1, 0, 2, 3)
         return pool
 
     pk, pv = pool_of(t["k"]), pool_of(t["v"])
@@ -569,66 +621,115 @@ def _bench_paged(st, L, dev, stream, l2_flush, events, K, case, t, w, hbm, tc, b
     aa.timing_begin = aa.timing_end = None
     if int(status.item()) != 0:
         raise RuntimeError("device status " + st.status_string(int(status.item())))
-    ms = statistics.fmean(eb[i].elapsed_time(ee[i]) for i in range(n))
+    ms = statistics.median(eb[i].elapsed_time(ee[i]) for i in range(n))
     frac = max(w["attn_kernel_bytes"] / (hbm * 1e9), w["attn_flops"] / (tc * 1e12)) / (ms * 1e-3)
+    del pk, pv
     return {"kernel_ms": ms, "contiguous_kernel_ms": contiguous_ms, "roofline_frac": frac, "steps": n,
             "pool_blocks": nb, "table_entries_per_request": mb}
 
 
 # ---- oracle (CPU baseline / reference arm) ------------------------------------------------------
 
-def _oracle_inputs(case):
-    return dict(q=case.f64("q"), k=case.f64("k_cache"), v=case.f64("v_cache"), h=case.f64("hidden"),
-                W=case.f32("W"))
+def _widen(case, name, sl):
+    """float64 copy of a slice of one input (bf16 bits widened exactly)."""
+    import numpy as np
+    from gen import bf16 as BF
+    a = getattr(case, name)[sl]
+    return BF.bf16_bits_to_f64(a) if case.dtype == "bf16" else np.asarray(a, dtype=np.float64)
 
 
-def _oracle_step(case, x):
+def oracle_request_sample(case, b, g):
+    """Times the oracle on request b: tree attention on KV head g (its G query heads), the LM head,
+    acceptance and longest path, and KV compaction.  Returns (tree nodes of b, estimated seconds
+    of the whole request = Hkv x the attention sample + the rest)."""
+    import numpy as np
     import oracle
-    oracle.tree_attention(x["q"], x["k"], x["v"], case.prefix_len, case.n_nodes, case.parent)
-    res = oracle.verify_accept(x["h"], x["W"], case.tokens, case.parent, case.n_nodes, case.rule, case.tau, case.eps,
-                               case.delta, case.seed, draft_probs=case.draft_probs,
+    G = case.Hq // case.Hkv
+    Lb, n = int(case.prefix_len[b]), int(case.n_nodes[b])
+    q = _widen(case, "q", np.s_[b: b + 1, :, g * G:(g + 1) * G])
+    k = _widen(case, "k_cache", np.s_[b: b + 1, g: g + 1, : Lb + n])
+    v = _widen(case, "v_cache", np.s_[b: b + 1, g: g + 1, : Lb + n])
+    h = _widen(case, "hidden", np.s_[b: b + 1])
+    Wt = case.f32("W") if not hasattr(case, "_W32") else case._W32
+    case._W32 = Wt
+    sl = np.s_[b: b + 1]
+    t0 = time.perf_counter()
+    oracle.tree_attention(q, k, v, case.prefix_len[sl], case.n_nodes[sl], case.parent[sl])
+    t1 = time.perf_counter()
+    res = oracle.verify_accept(h, Wt, case.tokens[sl], case.parent[sl], case.n_nodes[sl], case.rule, case.tau,
+                               case.eps, case.delta, case.seed,
+                               draft_probs=None if case.draft_probs is None else case.draft_probs[sl],
                                draft_to_target=case.draft_to_target)
-    paths = [r["path"] for r in res]
-    alen = [r["accept_len"] for r in res]
-    oracle.compact_kv(case.k_cache, case.v_cache, case.prefix_len, paths, alen, case.N)
+    t2 = time.perf_counter()
+    oracle.compact_kv(case.k_cache[sl], case.v_cache[sl], case.prefix_len[sl], [res[0]["path"]],
+                      [res[0]["accept_len"]], case.N)
+    t3 = time.perf_counter()
+    return n, case.Hkv * (t1 - t0) + (t2 - t1) + (t3 - t2)
 
 
-def _cpu_baseline(case, budget_s=20.0):
-    x = _oracle_inputs(case)
-    times = []
-    t_all = time.perf_counter()
-    while not times or (time.perf_counter() - t_all < budget_s and len(times) < 5):
+def cpu_baseline(case, budget_s=20.0):
+    """The oracle on a bounded sample of the workload: requests in order (cycling the KV head that
+    stands for all of them), until ``budget_s`` seconds of oracle work have been spent (at least
+    one request).  Rate = sampled tree nodes / their estimated oracle time."""
+    nodes = est = 0.0
+    done = []
+    spent = 0.0
+    b = 0
+    while not done or spent < budget_s:
         t0 = time.perf_counter()
-        _oracle_step(case, x)
-        times.append(time.perf_counter() - t0)
-    nodes = int(case.n_nodes.sum())
-    return {"value": nodes / statistics.fmean(times), "unit": UNIT, "cores": _threads_used(), "kind": "oracle",
-            "sample": f"{len(times)} full steps of the workload (all {nodes} nodes, all heads, full vocabulary)",
-            "s_per_step": statistics.fmean(times)}
+        n, e = oracle_request_sample(case, b % case.B, b % case.Hkv)
+        spent += time.perf_counter() - t0
+        nodes += n
+        est += e
+        done.append(b % case.B)
+        b += 1
+        if b >= 4 * case.B:
+            break
+    return {"value": nodes / est, "unit": UNIT, "cores": _threads_used(), "kind": "oracle",
+            "sample": (f"{len(done)} request samples (requests {sorted(set(done))[:8]} of {case.B}): per request, "
+                       f"tree attention of one KV head (its {case.Hq // case.Hkv} query heads, all nodes, all keys) "
+                       f"scaled by {case.Hkv} KV heads, plus LM head over the full vocabulary, acceptance, longest "
+                       "path and KV compaction in full"),
+            "oracle_seconds": spent, "s_per_step_estimate": est / nodes * float(case.n_nodes.sum())}
 
 
 def run_reference(a):
     from gen import make_config_case
     case = make_config_case(a.workload, seed=a.seed)
-    x = _oracle_inputs(case)
-    for _ in range(a.warmup if a.warmup < 3 else 1):
-        _oracle_step(case, x)
-    times = []
-    for _ in range(a.steps if a.steps <= 20 else 20):
-        t0 = time.perf_counter()
-        _oracle_step(case, x)
-        times.append(time.perf_counter() - t0)
-    nodes = int(case.n_nodes.sum())
-    s = statistics.fmean(times)
-    v = nodes / s
-    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": a.gpus, "steps": len(times),
-            "warmup": a.warmup, "ms_per_step": s * 1e3, "higher_is_better": True, "scaling": "weak",
+    for i in range(min(a.warmup, 1)):
+        oracle_request_sample(case, i % case.B, i % case.Hkv)
+    nodes = est = 0.0
+    for i in range(a.steps):
+        n, e = oracle_request_sample(case, i % case.B, i % case.Hkv)
+        nodes += n
+        est += e
+    v = nodes / est
+    ms = float(case.n_nodes.sum()) / v * 1e3
+    sample = (f"{a.steps} steps, step i = request i mod {case.B}: tree attention of KV head i mod {case.Hkv} "
+              f"scaled by {case.Hkv}, plus LM head, acceptance and compaction of that request in full")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
+            "warmup": min(a.warmup, 1), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": case.name, "batch": case.B, "prefix_len": [int(x) for x in case.prefix_len][:8],
-                       "tree_nodes": nodes, "rule": case.rule},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": _threads_used(), "kind": "oracle",
-                             "sample": f"{len(times)} full steps of the workload (capped at 20 timed steps)"},
+                       "tree_nodes": [int(x) for x in case.n_nodes][:8], "rule": case.rule},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": _threads_used(), "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_native(a, rank, world, dist):
+    import torch
+    import tree_speculative_decoding_split_gb300 as st
+    st.build()
+    st.lib()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    line = measure_workload(a, a.workload, rank, world, dist, a.seed + rank, with_cpu=True)
+    if a.profile:
+        return None
+    if a.second_workload and a.second_workload != a.workload:
+        second = measure_workload(a, a.second_workload, rank, world, dist, a.seed + rank, with_cpu=True)
+        if line is not None:
+            line["second_workload"] = second
+    return line
 
 
 def main():

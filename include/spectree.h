@@ -186,6 +186,10 @@ typedef struct spec_verify_args {
   void* timing_end;               /* optional cudaEvent_t recorded right after it */
 } spec_verify_args;
 
+/* Bytes of workspace spec_verify_accept needs for these shapes (0 on invalid args).  The
+ * workspace (device memory, 16-byte aligned: statistics records and fp32 logits are stored there
+ * as 16-byte vectors; SPEC_ERR_INVALID_ARGUMENT otherwise) holds the LM head's per-row records,
+ * the row statistics and, for rejection sampling, the fp32 logits. */
 size_t spec_verify_accept_workspace(const spec_verify_args* args);
 
 spec_status spec_verify_accept(const spec_verify_args* args, void* workspace,
@@ -243,8 +247,11 @@ spec_status spec_compact_kv(const spec_compact_args* args, int32_t* dev_status, 
  *     rejected with SPEC_ERR_WORKSPACE_TOO_SMALL before anything is launched (at a 128256-token
  *     vocabulary this fits greedy / typical verification of up to a few hundred tree rows;
  *     rejection sampling keeps fp32 logits and fits only small rows x vocabulary products).
- *   - The first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *   - Calls look up the array's device address on the current device (a cheap runtime query)
+ *     and remember it per device.  While `stream` is being captured the remembered address is
+ *     used instead, so make one call on the device before any stream capture.  A device reset
+ *     (cudaDeviceReset) invalidates the remembered address; the next call outside a capture
+ *     looks it up again.
  *   - All calls on a device share the one array and it keeps the last call's contents; every
  *     call overwrites what it reads.  Calls whose kernels overlap on the GPU (different streams,
  *     or different host threads without ordering) race on the array and must not be issued.
@@ -411,6 +418,37 @@ spec_status spec_round_create(const spec_attn_args* attn, void* attn_workspace, 
                               int32_t* dev_status, spec_round** out);
 spec_status spec_round_launch(const spec_round* round, void* stream);
 void spec_round_destroy(spec_round* round);
+
+/* One round end to end from host memory: the step's inputs are copied in, the round runs, and
+ * its results are copied out, all enqueued on `stream` in that order by one call.  (Deployment
+ * convenience, like the round itself: the pages describe what a round computes, not where its
+ * inputs come from.)
+ *
+ * Each spec_host_copy moves `rows` rows of `row_bytes` bytes; row r starts at
+ * host + r * host_pitch and at device + r * device_pitch (pitches are ignored when rows == 1).
+ * A strided destination lets one copy place, say, a request's new tree K rows of every KV head
+ * into the cache slots [prefix_len, prefix_len + n) of a [Hkv][L_cap][d] block.  The device
+ * pointers are normally buffers the round was created on (q, hidden_states, tokens, parent,
+ * n_nodes, prefix_len, draft_probs, cache slots; accept_len, path, bonus_token, new_len, ...).
+ *   - Host memory should be page-locked (cudaHostAlloc / cudaHostRegister); with pageable memory
+ *     the copies are staged by the driver and the call returns only after they are done.
+ *   - The call returns once everything is enqueued: synchronise `stream` before reading the
+ *     outputs on the host or refilling the input buffers.
+ *   - A copy with row_bytes == 0 or rows == 0 is skipped.
+ * Errors: SPEC_ERR_INVALID_ARGUMENT (round == NULL, a negative count, NULL arrays with a positive
+ * count, a NULL pointer in a non-empty copy, a pitch below row_bytes with rows > 1),
+ * SPEC_ERR_CUDA (a copy or the graph launch could not be enqueued). */
+typedef struct spec_host_copy {
+  void* host;             /* host memory */
+  void* device;           /* device memory */
+  size_t row_bytes;       /* bytes per row */
+  size_t rows;            /* rows (1 = one contiguous block of row_bytes) */
+  size_t host_pitch;      /* bytes between rows on the host (rows > 1) */
+  size_t device_pitch;    /* bytes between rows on the device (rows > 1) */
+} spec_host_copy;
+
+spec_status spec_round_launch_host(const spec_round* round, const spec_host_copy* inputs, int32_t n_inputs,
+                                   const spec_host_copy* outputs, int32_t n_outputs, void* stream);
 
 /* Static English description of a status code (never NULL). */
 const char* spec_status_string(spec_status status);

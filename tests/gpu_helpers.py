@@ -9,8 +9,12 @@ Tolerances (written here, used by every GPU test):
   the 1e-4 margin;
 * accepted length, path, bonus token and compacted KV / source slots: bit-exact, except for requests
   whose evaluated decisions include a margin case (counted and reported), which are checked for
-  validity instead.
+  validity instead;
+* margin counts (decisions within 1e-4 of their threshold) and the bonus flag: the GPU's against the
+  oracle's, up to decisions at the band's edge.
 """
+
+from typing import NamedTuple
 
 import numpy as np
 import torch
@@ -114,11 +118,54 @@ def check_attention(case, got_o, got_l, rows=None):
     return err, lerr
 
 
+class VerifyCheck(NamedTuple):
+    exact: int           # requests whose path, length and bonus were compared bit for bit
+    excluded: int        # requests with a margin case (path or bonus) among their decisions
+    paths_exact: int     # requests whose path and length were compared bit for bit
+    margins_gpu: int     # margin cases the GPU counted over the compared requests
+    margins_oracle: int  # margin cases the oracle counted over the same requests
+
+
+def oracle_request_at_band(case, b, band):
+    """The oracle's verdict on request b with the margin band set to ``band``.  Decisions do not
+    depend on the band; only which of them count as near-threshold does."""
+    import oracle.accept as acc
+    old = acc.MARGIN
+    acc.MARGIN = band
+    try:
+        return oracle_verify(case, requests=[b])[b]
+    finally:
+        acc.MARGIN = old
+
+
+def _check_margins(case, b, got, r):
+    """The GPU's margin count and bonus flag against the oracle's.  A decision the oracle puts
+    within the band is evaluated by the GPU as well (every decision before it is outside the band,
+    so both sides agree on it), so an oracle count >= 1 implies a GPU count >= 1 and a count of 0
+    implies 0 -- unless a decision sits at the band's edge, where float32 and float64 may fall on
+    either side; those are recognised by re-running the oracle with the band 10 % wider or narrower."""
+    gm = int(got["margin_count"][b])
+    gb = int(got["bonus_margin"][b])
+    if r["path_margins"] == 0:
+        if gm != 0:
+            wide = oracle_request_at_band(case, b, oracle.MARGIN * 1.1)
+            assert gm <= wide["path_margins"], (b, gm, r["path_margins"], wide["path_margins"])
+    elif gm == 0:
+        narrow = oracle_request_at_band(case, b, oracle.MARGIN * 0.9)
+        assert narrow["path_margins"] == 0, (b, gm, r["path_margins"])
+    same_end = int(got["accept_len"][b]) == r["accept_len"] and \
+        got["path"][b, r["accept_len"]] == r["path"][-1]
+    if same_end and bool(gb) != bool(r["bonus_margin"]):
+        # the bonus decision is taken at the same endpoint: the flags must agree up to the edge
+        other = oracle_request_at_band(case, b, oracle.MARGIN * (1.1 if gb else 0.9))
+        assert bool(other["bonus_margin"]) == bool(gb), (b, gb, r["bonus_margin"])
+
+
 def check_verify(case, got, ref, requests=None, stats_rows=None):
-    """Bit-exact comparison of accept_len / path / bonus outside margin cases; returns the number of
-    requests compared exactly and the number excluded as margin cases."""
+    """Bit-exact comparison of accept_len / path / bonus outside margin cases, and of the margin
+    counts against the oracle's; returns a VerifyCheck."""
     todo = range(case.B) if requests is None else requests
-    exact = excluded = 0
+    exact = excluded = paths_exact = mg_gpu = mg_orc = 0
     for b in todo:
         r = ref[b]
         n = int(case.n_nodes[b])
@@ -129,11 +176,16 @@ def check_verify(case, got, ref, requests=None, stats_rows=None):
         for j in range(1, gl + 1):
             assert 0 < gp[j] < n and case.parent[b, gp[j]] == gp[j - 1], (b, gp[: gl + 1])
         assert (gp[gl + 1:] == -1).all()
+        if "margin_count" in got and "bonus_margin" in got:
+            _check_margins(case, b, got, r)
+            mg_gpu += int(got["margin_count"][b])
+            mg_orc += int(r["path_margins"])
         if r["path_margins"]:
             excluded += 1
             continue
         assert gl == r["accept_len"], (b, gl, r["accept_len"])
         assert gp[: gl + 1].tolist() == r["path"], (b, gp[: gl + 1], r["path"])
+        paths_exact += 1
         if r["bonus_margin"]:
             lo, hi = r["bonus_window"]
             assert lo <= int(got["bonus_token"][b]) <= hi, (b, got["bonus_token"][b], r["bonus_window"])
@@ -141,7 +193,7 @@ def check_verify(case, got, ref, requests=None, stats_rows=None):
         else:
             assert int(got["bonus_token"][b]) == r["bonus"], (b, got["bonus_token"][b], r["bonus"])
             exact += 1
-    return exact, excluded
+    return VerifyCheck(exact, excluded, paths_exact, mg_gpu, mg_orc)
 
 
 def check_row_stats(case, got, rows):

@@ -3,6 +3,7 @@
 import numpy as np
 import pytest
 
+import oracle
 from gen import make_case, make_config_case, trees as T
 import gpu_helpers as H
 
@@ -100,6 +101,18 @@ def test_llama70b_b4_long_context_sampled():
     o, l, status = H.gpu_attention(case, t)
     assert status == 0
     H.check_attention(case, o, l, rows=_sample_rows(case, 24, 5))
+    # every row of the longest request (131072 prefix keys, 255 nodes) on KV head 0: its 8 query
+    # heads x 255 nodes against the oracle on that slice of the problem
+    b = int(np.argmax(case.prefix_len))
+    L, n, G = int(case.prefix_len[b]), int(case.n_nodes[b]), case.Hq // case.Hkv
+    q = case.f64("q")[b: b + 1, :, :G]
+    kf = np.asarray(case.f32("k_cache")[b: b + 1, :1, : L + n], dtype=np.float64)
+    vf = np.asarray(case.f32("v_cache")[b: b + 1, :1, : L + n], dtype=np.float64)
+    O, LSE = oracle.tree_attention(q, kf, vf, case.prefix_len[b: b + 1], case.n_nodes[b: b + 1],
+                                   case.parent[b: b + 1])
+    err = np.abs(o[b: b + 1, :n, :G] - O[:, :n]).max()
+    lerr = (np.abs(l[b: b + 1, :n, :G] - LSE[:, :n]) / np.maximum(np.abs(LSE[:, :n]), 1e-6)).max()
+    assert L == 131072 and err < H.ATTN_TOL["bf16"] and lerr < H.LSE_RTOL, (err, lerr)
     # padded rows are exactly zero
     for b in range(case.B):
         n = int(case.n_nodes[b])

@@ -93,5 +93,5 @@ def test_expanded_tree_feeds_typical_acceptance():
     out = H.gpu_verify(case, H.to_device(case, d))
     assert out["status"] == 0
     ref = H.oracle_verify(case)
-    exact, excluded = H.check_verify(case, out, ref)
-    assert exact + excluded == 2
+    c = H.check_verify(case, out, ref)
+    assert c.exact + c.excluded == 2

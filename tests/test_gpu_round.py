@@ -83,3 +83,109 @@ def test_round_rejects_bad_arguments_at_creation():
     with pytest.raises(st.SpecError) as e:
         st.Round(verify=va)
     assert e.value.code == 1
+
+
+def _round_vs_oracle(case, d):
+    """Launch the captured round once on ``case`` and compare every output with the oracle:
+    attention within the bf16 tolerances, accepted length / path / bonus / margin counts as in
+    the direct-call tests, compacted caches and source slots bit for bit."""
+    import oracle
+    t = H.to_device(case, d)
+    k0, v0 = case.k_cache.copy(), case.v_cache.copy()
+    aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"])
+    va, outs = st.verify_args(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], case.rule, case.tau,
+                              case.eps, case.delta, case.seed, t["draft"], t["map"], path_cap=case.N)
+    ca, src, nl = st.compact_args(t["k"], t["v"], t["prefix_len"], outs["path"], outs["accept_len"])
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    r = st.Round(aa, va, ca, dev_status=status)
+    r.launch()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    H.check_attention(case, out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))
+    got = {k: v.cpu().numpy() for k, v in outs.items()}
+    ref = H.oracle_verify(case)
+    c = H.check_verify(case, got, ref)
+    # compaction follows the accepted path: the oracle's where it was compared bit for bit, the
+    # GPU's own (already checked for validity) where a margin case excluded the request
+    paths, alen = [], []
+    for b in range(case.B):
+        if ref[b]["path_margins"]:
+            n = int(got["accept_len"][b])
+            paths.append(got["path"][b, : n + 1].tolist())
+            alen.append(n)
+        else:
+            paths.append(ref[b]["path"])
+            alen.append(ref[b]["accept_len"])
+    kr, vr, sr, nr = oracle.compact_kv(k0, v0, case.prefix_len, paths, np.array(alen), case.N)
+    view = np.int16 if case.dtype == "bf16" else np.float32
+    kg = t["k"].view(torch.int16).cpu().numpy() if case.dtype == "bf16" else t["k"].cpu().numpy()
+    vg = t["v"].view(torch.int16).cpu().numpy() if case.dtype == "bf16" else t["v"].cpu().numpy()
+    assert (kg == kr.view(view)).all() and (vg == vr.view(view)).all()
+    assert (src.cpu().numpy() == sr).all() and (nl.cpu().numpy() == nr).all()
+    r.close()
+    return c
+
+
+@pytest.mark.parametrize("rule", ["greedy", "typical", "rejection"])
+def test_round_against_the_oracle(rule):
+    d = H.dev()
+    c = _round_vs_oracle(_case(rule, 11), d)
+    assert c.paths_exact >= 1 and c.exact + c.excluded == 2
+
+
+def test_round_on_the_llama8b_b1_medusa63_workload_against_the_oracle():
+    """The B1 / 2048-token prefix / static 63-node tree / typical acceptance workload, as one
+    graph launch, against the oracle end to end."""
+    d = H.dev()
+    c = _round_vs_oracle(H.config_case(2, 0), d)
+    assert c.exact == 1
+
+
+def test_round_from_host_buffers_matches_the_device_round():
+    """spec_round_launch_host: the step's inputs copied in from pinned host memory (the tree's
+    K/V rows by one strided copy per request), the round, and the results copied out -- equal,
+    bit for bit, to a round on the same inputs already on the device."""
+    d = H.dev()
+    case = _case("rejection", 21)
+    t = H.to_device(case, d)
+    aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"])
+    va, outs = st.verify_args(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], case.rule, case.tau,
+                              case.eps, case.delta, case.seed, t["draft"], t["map"], path_cap=case.N)
+    ca, src, nl = st.compact_args(t["k"], t["v"], t["prefix_len"], outs["path"], outs["accept_len"])
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    r = st.Round(aa, va, ca, dev_status=status)
+    # reference: the same inputs, already on the device
+    r.launch()
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in outs.items()}
+    ref_k, ref_nl = t["k"].clone(), nl.clone()
+    # reset the round's buffers: caches back to the case's, inputs scrambled, outputs poisoned
+    fresh = H.to_device(case, d)
+    t["k"].copy_(fresh["k"])
+    t["v"].copy_(fresh["v"])
+    for key in ("q", "hidden", "tokens", "parent", "draft"):
+        t[key].zero_()
+    for v in outs.values():
+        v.fill_(-7)
+    nl.fill_(-7)
+    n = int(case.n_nodes.max())
+    Lp = [int(x) for x in case.prefix_len]
+    host = {key: fresh[key].cpu().pin_memory() for key in ("q", "hidden", "tokens", "parent", "draft")}
+    ins = [st.host_copy(host[key], t[key]) for key in host]
+    for b in range(case.B):
+        for cache, fc in ((t["k"], fresh["k"]), (t["v"], fresh["v"])):
+            rows = fc[b, :, Lp[b]: Lp[b] + n].contiguous().cpu().pin_memory()
+            ins.append(st.host_copy(rows, cache[b, :, Lp[b]: Lp[b] + n], rows=case.Hkv))
+            cache[b, :, Lp[b]: Lp[b] + n].zero_()  # the tree slots now arrive only from the host
+    res = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    res_nl = torch.empty(nl.shape, dtype=nl.dtype).pin_memory()
+    outs_c = [st.host_copy(res[k], outs[k]) for k in res] + [st.host_copy(res_nl, nl)]
+    torch.cuda.synchronize()
+    r.launch_host(ins, outs_c)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for k in res:
+        assert torch.equal(res[k], ref[k].cpu()), k
+    assert torch.equal(res_nl, ref_nl.cpu())
+    assert torch.equal(t["k"].view(torch.int16), ref_k.view(torch.int16))
+    r.close()

@@ -45,9 +45,11 @@ int main(void) {
   printf("spec_attn_args size %zu\n", sizeof(spec_attn_args));
   printf("spec_verify_args size %zu\n", sizeof(spec_verify_args));
   printf("spec_compact_args size %zu\n", sizeof(spec_compact_args));
+  printf("spec_host_copy size %zu\n", sizeof(spec_host_copy));
   P(spec_attn_args, kv_capacity) P(spec_attn_args, q) P(spec_attn_args, lse) P(spec_attn_args, timing_end)
   P(spec_verify_args, seed) P(spec_verify_args, hidden_states) P(spec_verify_args, row_argmax) P(spec_verify_args, timing_end)
   P(spec_compact_args, kv_capacity) P(spec_compact_args, k_cache) P(spec_compact_args, new_len)
+  P(spec_host_copy, row_bytes) P(spec_host_copy, device_pitch)
   return 0;
 }
 """
@@ -62,7 +64,8 @@ int main(void) {
         if line:
             t, f, v = line.split()
             got[(t, f)] = int(v)
-    py = {"spec_attn_args": st.AttnArgs, "spec_verify_args": st.VerifyArgs, "spec_compact_args": st.CompactArgs}
+    py = {"spec_attn_args": st.AttnArgs, "spec_verify_args": st.VerifyArgs, "spec_compact_args": st.CompactArgs,
+          "spec_host_copy": st.HostCopy}
     for (t, f), v in got.items():
         cls = py[t]
         if f == "size":
@@ -100,6 +103,19 @@ def test_host_argument_errors_return_before_launch(L):
     assert L.spec_round_create(None, None, 0, None, None, 0, None, None, None) == 1   # out == NULL
     assert L.spec_round_launch(None, None) == 1
     L.spec_round_destroy(None)
+    # the host-buffer launch checks its copy descriptors (and the round) before enqueuing anything
+    fn = L.spec_round_launch_host
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+    fn.restype = ctypes.c_int32
+    fake = ctypes.c_void_p(1 << 20)
+    assert fn(None, None, 0, None, 0, None) == 1                      # no round
+    assert fn(fake, None, -1, None, 0, None) == 1                     # negative count
+    assert fn(fake, None, 1, None, 0, None) == 1                      # NULL array, positive count
+    bad = (st.HostCopy * 1)(st.HostCopy(host=None, device=fake, row_bytes=16, rows=1))
+    assert fn(fake, ctypes.cast(bad, ctypes.c_void_p), 1, None, 0, None) == 1   # NULL host pointer
+    pitch = (st.HostCopy * 1)(st.HostCopy(host=fake, device=fake, row_bytes=64, rows=4, host_pitch=32,
+                                          device_pitch=64))
+    assert fn(fake, None, 0, ctypes.cast(pitch, ctypes.c_void_p), 1, None) == 1  # pitch below a row
 
 
 def test_workspace_queries_are_host_only(L):
@@ -119,6 +135,11 @@ def test_workspace_queries_are_host_only(L):
                       parent=fake, n_nodes=fake, draft_probs=fake, accept_len=fake, path=fake, bonus_token=fake)
     need = L.spec_verify_accept_workspace(ctypes.byref(v))
     assert need >= 63 * 128256 * 4  # rejection keeps the fp32 logits
+    # records and logits are stored as 16-byte vectors: a workspace off a 16-byte boundary, a
+    # missing one and a short one are refused before anything is launched
+    assert L.spec_verify_accept(ctypes.byref(v), odd, need, None, None) == 1
+    assert L.spec_verify_accept(ctypes.byref(v), None, need, None, None) == 1
+    assert L.spec_verify_accept(ctypes.byref(v), fake, need - 1, None, None) == 3
     v.rule = 0
     assert L.spec_verify_accept_workspace(ctypes.byref(v)) < need
 

@@ -13,6 +13,7 @@ runs in the library's CUDA kernels; if the library has not been built, every cal
     eagle_expand(...)     -> dict of outputs      one layer of a dynamic (EAGLE-2 style) draft tree
     eagle_tree(...)       -> dict of outputs      the tree from all layers' candidates
     Round(...)                                    the three verification calls as one graph launch
+                                                  (also from host buffers: Round.launch_host)
 """
 
 import ctypes
@@ -63,6 +64,11 @@ class CompactArgs(ctypes.Structure):
                 ("path", _vp), ("accept_len", _vp), ("src_slot", _vp), ("new_len", _vp), ("block_table", _vp),
                 ("block_size", ctypes.c_int32), ("max_blocks", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
                 ("reserved1", ctypes.c_int32)]
+
+
+class HostCopy(ctypes.Structure):
+    _fields_ = [("host", _vp), ("device", _vp), ("row_bytes", ctypes.c_size_t), ("rows", ctypes.c_size_t),
+                ("host_pitch", ctypes.c_size_t), ("device_pitch", ctypes.c_size_t)]
 
 
 class MedusaArgs(ctypes.Structure):
@@ -116,6 +122,9 @@ def lib():
         L.spec_round_create.restype = ctypes.c_int32
         L.spec_round_launch.argtypes = [_vp, _vp]
         L.spec_round_launch.restype = ctypes.c_int32
+        L.spec_round_launch_host.argtypes = [_vp, ctypes.POINTER(HostCopy), ctypes.c_int32,
+                                             ctypes.POINTER(HostCopy), ctypes.c_int32, _vp]
+        L.spec_round_launch_host.restype = ctypes.c_int32
         L.spec_round_destroy.argtypes = [_vp]
         L.spec_round_destroy.restype = None
         L.spec_medusa_expand_workspace.argtypes = [ctypes.POINTER(MedusaArgs)]
@@ -432,6 +441,17 @@ class Round:
             raise RuntimeError("round destroyed")
         _check(lib().spec_round_launch(self._handle, _stream(stream)), "spec_round_launch")
 
+    def launch_host(self, inputs, outputs, stream=None):
+        """One round from host memory (spec_round_launch_host): ``inputs`` and ``outputs`` are
+        sequences of HostCopy descriptors (see ``host_copy``), copied in before and out after the
+        round, all enqueued on ``stream`` by one C call.  Synchronise before reading the outputs."""
+        if self._handle is None:
+            raise RuntimeError("round destroyed")
+        ins = (HostCopy * max(len(inputs), 1))(*inputs)
+        outs = (HostCopy * max(len(outputs), 1))(*outputs)
+        _check(lib().spec_round_launch_host(self._handle, ins, len(inputs), outs, len(outputs), _stream(stream)),
+               "spec_round_launch_host")
+
     def close(self):
         if getattr(self, "_handle", None) is not None:
             lib().spec_round_destroy(self._handle)
@@ -442,6 +462,29 @@ class Round:
             self.close()
         except Exception:
             pass
+
+
+def host_copy(host, device, rows=None):
+    """HostCopy descriptor between a host tensor and a device tensor of the same byte size.
+
+    With ``rows`` = None both must be contiguous (one block).  With ``rows`` = r, the host tensor is
+    contiguous [r][...] and ``device`` is a view of r equal-sized rows at a constant stride (e.g. a
+    request's tree slots of every KV head in a [Hkv][L_cap][d] cache block); each row must itself
+    be contiguous."""
+    nbytes = host.numel() * host.element_size()
+    if rows is None:
+        if not (host.is_contiguous() and device.is_contiguous()) or \
+                device.numel() * device.element_size() != nbytes:
+            raise ValueError("host_copy: contiguous tensors of equal size expected")
+        return HostCopy(host=_vp(host.data_ptr()), device=_vp(device.data_ptr()), row_bytes=nbytes, rows=1)
+    r = int(rows)
+    if device.shape[0] != r or not host.is_contiguous() or not device[0].is_contiguous() or \
+            device.numel() * device.element_size() != nbytes:
+        raise ValueError("host_copy: rows of the device view must be contiguous and match the host tensor")
+    row = nbytes // r
+    pitch = device.stride(0) * device.element_size()
+    return HostCopy(host=_vp(host.data_ptr()), device=_vp(device.data_ptr()), row_bytes=row, rows=r,
+                    host_pitch=row, device_pitch=pitch)
 
 
 def medusa_topology(topk, n_nodes):

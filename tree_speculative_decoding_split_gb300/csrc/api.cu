@@ -340,7 +340,7 @@ spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_
                                int32_t* dev_status, void* stream_ptr) {
   spec_status st = check_verify(a);
   if (st != SPEC_OK) return st;
-  if (!workspace) return SPEC_ERR_INVALID_ARGUMENT;
+  if (!workspace || !aligned16(workspace)) return SPEC_ERR_INVALID_ARGUMENT;
   if (workspace_bytes < layout_verify(a, nullptr).bytes) return SPEC_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const VerifyLayout l = layout_verify(a, workspace);

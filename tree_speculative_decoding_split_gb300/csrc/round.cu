@@ -65,6 +65,48 @@ extern "C" spec_status spec_round_launch(const spec_round* round, void* stream) 
   return cudaGraphLaunch(round->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+namespace {
+
+spec_status check_copies(const spec_host_copy* c, int32_t n) {
+  if (n < 0 || (n > 0 && !c)) return SPEC_ERR_INVALID_ARGUMENT;
+  for (int32_t i = 0; i < n; ++i) {
+    if (c[i].row_bytes == 0 || c[i].rows == 0) continue;  // nothing to copy
+    if (!c[i].host || !c[i].device) return SPEC_ERR_INVALID_ARGUMENT;
+    if (c[i].rows > 1 && (c[i].host_pitch < c[i].row_bytes || c[i].device_pitch < c[i].row_bytes))
+      return SPEC_ERR_INVALID_ARGUMENT;
+  }
+  return SPEC_OK;
+}
+
+cudaError_t enqueue_copy(const spec_host_copy& c, bool to_device, cudaStream_t s) {
+  if (c.row_bytes == 0 || c.rows == 0) return cudaSuccess;
+  if (c.rows == 1)
+    return to_device ? cudaMemcpyAsync(c.device, c.host, c.row_bytes, cudaMemcpyHostToDevice, s)
+                     : cudaMemcpyAsync(c.host, c.device, c.row_bytes, cudaMemcpyDeviceToHost, s);
+  return to_device ? cudaMemcpy2DAsync(c.device, c.device_pitch, c.host, c.host_pitch, c.row_bytes, c.rows,
+                                       cudaMemcpyHostToDevice, s)
+                   : cudaMemcpy2DAsync(c.host, c.host_pitch, c.device, c.device_pitch, c.row_bytes, c.rows,
+                                       cudaMemcpyDeviceToHost, s);
+}
+
+}  // namespace
+
+extern "C" spec_status spec_round_launch_host(const spec_round* round, const spec_host_copy* inputs,
+                                              int32_t n_inputs, const spec_host_copy* outputs, int32_t n_outputs,
+                                              void* stream) {
+  spec_status st = check_copies(inputs, n_inputs);
+  if (st == SPEC_OK) st = check_copies(outputs, n_outputs);
+  if (st != SPEC_OK) return st;
+  if (!round) return SPEC_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t i = 0; i < n_inputs; ++i)
+    if (enqueue_copy(inputs[i], true, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaGraphLaunch(round->exec, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  for (int32_t i = 0; i < n_outputs; ++i)
+    if (enqueue_copy(outputs[i], false, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
 extern "C" void spec_round_destroy(spec_round* round) {
   if (!round) return;
   cudaGraphExecDestroy(round->exec);
