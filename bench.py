@@ -44,6 +44,7 @@ CSRC = os.path.join(ROOT, "tree_speculative_decoding_split_gb300", "csrc")
 # while these are unchanged)
 KERNEL_SOURCES = {
     "attn_tc_kernel": ["attention_tc.cu", "tc_ptx.cuh", "common.cuh"],
+    "attn_sk_kernel": ["attention_sk.cu", "tc_ptx.cuh", "common.cuh"],
     "lmhead_tc_kernel": ["lmhead.cu", "tc_ptx.cuh", "common.cuh"],
     "lmhead_tc_rows_kernel": ["lmhead.cu", "tc_ptx.cuh", "common.cuh"],
 }
@@ -239,21 +240,29 @@ def _device_tensors(case, dev):
                 map=None if case.draft_to_target is None else t(case.draft_to_target.astype(np.int32)))
 
 
-def _attention_splits(L, aa, case):
-    """Key splits of the attention plan, read back from the workspace query (fp32 partials of
-    d + 2 floats per row and split dominate it)."""
+def _attention_plan(L, aa, case, sms):
+    """(stream_k, key splits) of the attention plan, read back from the workspace query: the
+    stream-K kernel's workspace holds two 256-row partial slots per SM, the split kernel's fp32
+    partials of d + 2 floats per row and split."""
+    ws = int(L.spec_tree_attention_workspace(ctypes.byref(aa)))
+    sk = sms * 2 * 256 * (case.d * 4 + 8)
+    if case.dtype == "bf16" and sk <= ws < sk + (8 << 20):
+        return True, 1
     rows = case.B * case.N * case.Hq
-    return max(1, int(L.spec_tree_attention_workspace(ctypes.byref(aa)) // (rows * (case.d * 4 + 8))))
+    return False, max(1, ws // (rows * (case.d * 4 + 8)))
 
 
-def _launches_per_step(case, n_split):
-    attn = (2 if n_split > 1 else 1) if case.dtype == "bf16" else 2   # split-KV [+ merge] | prep + fp32 rows
+def _launches_per_step(case, n_split, stream_k, fused):
+    if case.dtype != "bf16":
+        attn = 2                                                       # tree prep + fp32 rows
+    else:
+        attn = 2 if (stream_k or n_split > 1) else 1                   # counters memset + stream-K | split-KV [+ merge]
     verify = 2 if case.dtype == "bf16" else 3                          # LM head, row finalise [+ fp32 stats]
     if case.rule == "rejection":
         verify += 1                                                    # rejection walk
         if case.draft_to_target is not None:
             verify += 1                                                # draft-map inversion
-    return attn + verify + 1                                           # + compaction
+    return attn + verify + (0 if fused else 1)                         # compaction folded into acceptance
 
 
 class _Flush:
@@ -297,7 +306,7 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
     ws_v = torch.empty(need_v, dtype=torch.uint8, device=dev)
     pa, pv, pst = ctypes.c_void_p(ws_a.data_ptr()), ctypes.c_void_p(ws_v.data_ptr()), ctypes.c_void_p(status.data_ptr())
     l2_flush = _Flush(dev)
-    n_split = _attention_splits(L, aa, case)
+    stream_k, n_split = _attention_plan(L, aa, case, torch.cuda.get_device_properties(dev).multi_processor_count)
 
     def step():
         c1 = L.spec_tree_attention(ctypes.byref(aa), pa, need_a, pst, sp)
@@ -437,7 +446,7 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
     lm_med = statistics.median(lm_ms)
     attn_med = statistics.median(attn_ms)
     lm_kernel = "lmhead_tc_rows_kernel" if case.B * case.N > 64 else "lmhead_tc_kernel"
-    rf_attn = _roofline("attn_tc_kernel", w["attn_flops"], w["attn_kernel_bytes"], attn_med, hbm, tc, peak_kind,
+    rf_attn = _roofline("attn_sk_kernel" if stream_k else "attn_tc_kernel", w["attn_flops"], w["attn_kernel_bytes"], attn_med, hbm, tc, peak_kind,
                         case.name)
     rf_lm = _roofline(lm_kernel, w["lm_flops"], w["lm_kernel_bytes"], lm_med, hbm, tc, peak_kind, case.name)
     dominant = rf_attn if attn_med >= lm_med else rf_lm
@@ -455,16 +464,18 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
                    "head_dim": case.d, "hidden": case.Hd, "vocab": case.V, "rule": case.rule, "temperature": case.tau,
                    "eps": case.eps, "delta": case.delta, "parallelism": f"replicas x{world}",
                    "l2": "flushed before every step (256 MB write, then read)",
-                   "launch": ("one CUDA-graph launch of the captured round per step (spec_round_launch)"
+                   "launch": ("one CUDA-graph launch of the captured round per step (spec_round_launch; "
+                              "compaction folded into the acceptance kernels)"
                               if a.mode == "graph" else "three C-ABI calls per step"),
                    "statistic": "median over the timed steps"},
         "e2e": {"value": job_rate(world, w["nodes"], e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "call": "spec_round_launch_host: pinned host inputs copied in, the round, results copied out"},
-        "gpu_launches": K * _launches_per_step(case, n_split),
+        "gpu_launches": K * _launches_per_step(case, n_split, stream_k, a.mode == "graph"),
         "roofline": dominant,
         "roofline_kernels": {"tree_attention": rf_attn, "lm_head": rf_lm},
-        "kernels": {"tree_attention_splitkv_ms": attn_med, "lmhead_ms": lm_med, "attention_key_splits": n_split,
+        "kernels": {"tree_attention_ms": attn_med, "lmhead_ms": lm_med,
+                    "attention_kernel": "persistent stream-K" if stream_k else f"split-KV, {n_split} key splits",
                     "attention_roofline_frac": rf_attn["frac"], "lmhead_roofline_frac": rf_lm["frac"]},
         "roofline_step": {"combined_s": t_comb, "frac_combined": t_comb / (ms * 1e-3),
                           "full_s": t_full, "frac_full": t_full / (ms * 1e-3),
@@ -482,6 +493,7 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
         line["cpu_baseline"] = cpu_baseline(case, a.cpu_budget)
     if world == 1 and not a.no_next and cfg == a.workload:
         line["next_rows"] = {
+            "llama8b_b1_round": _bench_b1_round(a, st, L, dev, stream, l2_flush, events, K),
             "medusa_expand": _bench_medusa(st, L, dev, stream, l2_flush, events, K, hbm),
             "eagle_dynamic_tree": _bench_eagle(st, L, dev, stream, l2_flush, events, K),
             "paged_attention": {f"block_{bs}": _bench_paged(st, L, dev, stream, l2_flush, events, K, t, w, hbm, tc, bs,
@@ -507,6 +519,50 @@ def _timed_calls(l2_flush, events, stream, call, n):
         ee[i].record(stream)
     torch.cuda.synchronize()
     return statistics.median(es[i].elapsed_time(ee[i]) for i in range(n))
+
+
+def _bench_b1_round(a, st, L, dev, stream, l2_flush, events, K):
+    """The batch-1 Llama-8B-shaped round (2048-token prefix, static 63-node tree, typical
+    acceptance), where launches are a visible share of the step: one graph launch (compaction
+    folded into acceptance), the three C-ABI calls, and two calls with the folded compaction."""
+    import torch
+    from gen import make_config_case
+    case = make_config_case(2, seed=a.seed)
+    t = _device_tensors(case, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"])
+    va, outs = st.verify_args(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], case.rule, case.tau,
+                              case.eps, case.delta, case.seed, None, None, path_cap=case.N)
+    ca, src_slot, new_len = st.compact_args(t["k"], t["v"], t["prefix_len"], outs["path"], outs["accept_len"])
+    need_a = L.spec_tree_attention_workspace(ctypes.byref(aa))
+    need_v = L.spec_verify_accept_workspace(ctypes.byref(va))
+    ws_a = torch.empty(need_a, dtype=torch.uint8, device=dev)
+    ws_v = torch.empty(need_v, dtype=torch.uint8, device=dev)
+    pa, pv, pst = ctypes.c_void_p(ws_a.data_ptr()), ctypes.c_void_p(ws_v.data_ptr()), ctypes.c_void_p(status.data_ptr())
+    sp = ctypes.c_void_p(stream.cuda_stream)
+
+    def three():
+        if (L.spec_tree_attention(ctypes.byref(aa), pa, need_a, pst, sp) or
+                L.spec_verify_accept(ctypes.byref(va), pv, need_v, pst, sp) or L.spec_compact_kv(ctypes.byref(ca), pst, sp)):
+            raise RuntimeError("C ABI call failed")
+
+    def two():
+        if (L.spec_tree_attention(ctypes.byref(aa), pa, need_a, pst, sp) or
+                L.spec_verify_accept_compact(ctypes.byref(va), pv, need_v, ctypes.byref(ca), pst, sp)):
+            raise RuntimeError("C ABI call failed")
+
+    rnd = st.Round(aa, va, ca, dev_status=status)
+    n = min(K, 200)
+    res = {"graph_ms": _timed_calls(l2_flush, events, stream, lambda: rnd.launch(stream), n),
+           "three_calls_ms": _timed_calls(l2_flush, events, stream, three, n),
+           "two_calls_folded_compaction_ms": _timed_calls(l2_flush, events, stream, two, n), "steps": n,
+           "tree_tokens": int(case.n_nodes.sum())}
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status " + st.status_string(int(status.item())))
+    res["graph_tree_tokens_per_s"] = res["tree_tokens"] / (res["graph_ms"] * 1e-3)
+    rnd.close()
+    return res
 
 
 def _bench_medusa(st, L, dev, stream, l2_flush, events, K, hbm):

@@ -231,6 +231,19 @@ typedef struct spec_compact_args {
 
 spec_status spec_compact_kv(const spec_compact_args* args, int32_t* dev_status, void* stream);
 
+/* spec_verify_accept followed by spec_compact_kv of its own outputs, with the compaction folded
+ * into the kernel that decides each request (the last row-statistics block of the request for
+ * greedy / typical acceptance, the end of the rejection walk), so the round has one launch less.
+ * (qiita, section "棄却サンプリング": the accepted prefix is kept, everything after a rejection is
+ * discarded; which kernel performs the move is not part of the method.)
+ * `compact` must name the verification's outputs: compact->path == verify->path,
+ * compact->accept_len == verify->accept_len, equal path_cap and batch; SPEC_ERR_INVALID_ARGUMENT
+ * otherwise.  Results (accept_len, path, bonus, margins, the caches, src_slot, new_len, device
+ * status codes) are exactly those of the two calls in sequence.  Workspace: as
+ * spec_verify_accept_workspace(verify). */
+spec_status spec_verify_accept_compact(const spec_verify_args* verify, void* workspace, size_t workspace_bytes,
+                                       const spec_compact_args* compact, int32_t* dev_status, void* stream);
+
 /* ---------------------------------------------------------------------------------------
  * spec_verify_accept without a caller workspace.  (The pages have no counterpart: this is a
  * deployment convenience, not part of the method.)
@@ -391,8 +404,9 @@ spec_status spec_eagle_tree(const spec_eagle_tree_args* args, int32_t* dev_statu
  *
  * spec_round_create captures, in this order, spec_tree_attention(attn, attn_workspace),
  * spec_verify_accept(verify, verify_workspace) and spec_compact_kv(compact) into a CUDA graph
- * and instantiates it.  Any of the three may be NULL to leave that call out; at least one must
- * be given.
+ * and instantiates it; when `compact` names the verification's outputs (same path, accept_len,
+ * path_cap and batch) the last two are captured as spec_verify_accept_compact.  Any of the three
+ * may be NULL to leave that call out; at least one must be given.
  *   - Everything in the argument structs is frozen at creation: device pointers, shapes,
  *     scalars (rule, temperature, eps, delta, seed), dev_status and the optional timing events.
  *     The CONTENTS of the device buffers are read when the round runs, so a serving loop refills

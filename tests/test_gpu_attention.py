@@ -118,3 +118,74 @@ def test_llama70b_b4_long_context_sampled():
         n = int(case.n_nodes[b])
         if n < case.N:
             assert (o[b, n:] == 0).all() and (l[b, n:] == 0).all()
+
+
+# ---- the persistent stream-K kernel (long caches) ----------------------------------------------
+
+def _align(x):
+    return (x + 255) // 256 * 256
+
+
+def _stream_k_workspace(B, N, Hq, Hkv, d, sms):
+    """Workspace bytes of the stream-K path: tree scratch, arrival counters per 256-row block and
+    group, and two partial slots of 256 rows per CTA."""
+    G = Hq // Hkv
+    W = (N + 31) // 32
+    blocks = (N * G + 255) // 256
+    return (_align(B * N * 4) + _align(B * N * W * 4) + 2 * _align(B * 4) + _align(B * Hkv * blocks * 2 * 4)
+            + _align(sms * 2 * 256 * 8) + _align(sms * 2 * 256 * d * 4))
+
+
+def _run_stream_k(case, d):
+    import ctypes
+    import torch
+    import tree_speculative_decoding_split_gb300 as st
+    t = H.to_device(case, d)
+    aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"])
+    sms = torch.cuda.get_device_properties(d).multi_processor_count
+    need = st.lib().spec_tree_attention_workspace(ctypes.byref(aa))
+    assert need == _stream_k_workspace(case.B, case.N, case.Hq, case.Hkv, case.d, sms), "not the stream-K path"
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device=d)  # counters start as garbage
+    code = st.lib().spec_tree_attention(ctypes.byref(aa), ctypes.c_void_p(ws.data_ptr()), need,
+                                        ctypes.c_void_p(status.data_ptr()),
+                                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    torch.cuda.synchronize()
+    return (out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            int(status.item()))
+
+
+@pytest.mark.parametrize("hd,Hq,Hkv", [(128, 8, 2), (64, 4, 4), (128, 16, 2)])
+def test_stream_k_few_tiles_in_a_long_cache(hd, Hq, Hkv):
+    """A 40000-slot cache takes the stream-K kernel, but the prefixes are short: fewer tiles than
+    SMs, so segments split into many one-tile pieces that the last arrival merges, including a
+    piece of tree keys only; ragged trees with padded nodes, an empty prefix and G = 1 / 4 / 8."""
+    d = H.dev()
+    rng = np.random.default_rng(hd + Hq)
+    parents = [T.random_bfs_tree(rng, n, 6)[0] for n in (37, 5, 60, 1)]
+    case = make_case(dtype="bf16", Hq=Hq, Hkv=Hkv, d=hd, Hd=64, V=16, prefix_len=[700, 0, 1300, 64],
+                     parents=parents, tokens=("given", np.zeros((4, 60), dtype=np.int32)), seed=13,
+                     L_cap=40000)
+    o, l, status = _run_stream_k(case, d)
+    assert status == 0
+    H.check_attention(case, o, l)
+    for b in range(case.B):
+        assert (o[b, case.n_nodes[b]:] == 0).all() and (l[b, case.n_nodes[b]:] == 0).all()
+
+
+def test_stream_k_bad_tree_and_capacity_zero_their_rows():
+    d = H.dev()
+    rng = np.random.default_rng(5)
+    good = T.random_bfs_tree(rng, 30, 5)[0]
+    bad = good.copy()
+    bad[9] = 20  # parent after its child
+    case = make_case(dtype="bf16", Hq=8, Hkv=2, d=128, Hd=64, V=16, prefix_len=[3000, 2500, 4000],
+                     parents=[good, bad, good], tokens=("given", np.zeros((3, 30), dtype=np.int32)), seed=4,
+                     L_cap=30000)
+    case.prefix_len[2] = 30000 - 10  # prefix + tree beyond the cache: a capacity error
+    o, l, status = _run_stream_k(case, d)
+    assert status in (4, 7)  # first error wins: SPEC_ERR_BAD_TREE or SPEC_ERR_CAPACITY
+    assert (o[1] == 0).all() and (l[1] == 0).all() and (o[2] == 0).all() and (l[2] == 0).all()
+    rows = [(0, i, h) for i in range(30) for h in (0, 3, 7)]
+    H.check_attention(case, o, l, rows=rows)

@@ -101,3 +101,62 @@ def test_host_errors_raise():
     ws = torch.empty(need, dtype=torch.uint8, device=d)
     code = L.spec_tree_attention(ctypes.byref(a), ctypes.c_void_p(ws.data_ptr()), need - 1, None, None)
     assert code == 3  # SPEC_ERR_WORKSPACE_TOO_SMALL, returned before any launch
+
+
+def _fused_vs_separate(case, d, block_table=None):
+    """spec_verify_accept_compact against spec_verify_accept followed by spec_compact_kv, on two
+    copies of the same inputs: every output and both caches bit for bit."""
+    t1, t2 = H.to_device(case, d), H.to_device(case, d)
+    s1 = torch.zeros(1, dtype=torch.int32, device=d)
+    s2 = torch.zeros(1, dtype=torch.int32, device=d)
+    r1 = st.verify_accept(t1["hidden"], t1["W"], t1["tokens"], t1["parent"], t1["n_nodes"], case.rule, case.tau,
+                          case.eps, case.delta, case.seed, draft_probs=t1["draft"], draft_to_target=t1["map"],
+                          path_cap=case.N, dev_status=s1)
+    src1, nl1 = st.compact_kv(t1["k"], t1["v"], t1["prefix_len"], r1["path"], r1["accept_len"], dev_status=s1)
+    r2 = st.verify_accept_compact(t2["hidden"], t2["W"], t2["tokens"], t2["parent"], t2["n_nodes"], case.rule,
+                                  t2["k"], t2["v"], t2["prefix_len"], case.tau, case.eps, case.delta, case.seed,
+                                  draft_probs=t2["draft"], draft_to_target=t2["map"], path_cap=case.N, dev_status=s2)
+    torch.cuda.synchronize()
+    assert int(s1.item()) == int(s2.item())
+    for key in ("accept_len", "path", "bonus_token", "margin_count", "bonus_margin"):
+        assert torch.equal(r1[key], r2[key]), key
+    assert torch.equal(src1, r2["src_slot"]) and torch.equal(nl1, r2["new_len"])
+    for name in ("k", "v"):
+        a, b = t1[name], t2[name]
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), name
+    return r2, int(s2.item())
+
+
+@pytest.mark.parametrize("rule,dtype,V", [("greedy", "bf16", 3000), ("typical", "f32", 2000),
+                                          ("rejection", "bf16", 5000), ("rejection", "bf16", 300001),
+                                          ("typical", "bf16", 30011)])
+def test_verify_with_folded_compaction_matches_separate_calls(rule, dtype, V):
+    """Greedy / typical fold the compaction into the last row block of each request, rejection into
+    the end of the walk (clusters of CTAs at V = 5000, one CTA per request at V = 300001); the
+    oracle pins the separate calls (test_compaction_bit_exact and the verify tests)."""
+    d = H.dev()
+    rng = np.random.default_rng(V)
+    parents = [T.random_bfs_tree(rng, 40, 6)[0], T.chain_tree(12), T.random_bfs_tree(rng, 25, 3)[0]]
+    case = make_case(dtype=dtype, Hq=4, Hkv=3, d=64 if dtype == "f32" else 128, Hd=128, V=V,
+                     prefix_len=[17, 300, 0], parents=parents, rule=rule, tau=0.0 if rule == "greedy" else 0.9,
+                     eps=0.09, delta=0.3, seed=V + 3,
+                     tokens=("iid", 0.8, 0.4) if rule == "rejection" else ("rank", 0.9), rng=rng)
+    r, status = _fused_vs_separate(case, d)
+    assert status == 0
+    ref = H.oracle_verify(case)
+    H.check_verify(case, {k: v.cpu().numpy() for k, v in r.items()}, ref)
+
+
+def test_folded_compaction_on_a_bad_tree_and_a_short_path_capacity():
+    d = H.dev()
+    rng = np.random.default_rng(3)
+    good = T.random_bfs_tree(rng, 20, 4)[0]
+    bad = good.copy()
+    bad[7] = 15
+    case = make_case(dtype="bf16", Hq=4, Hkv=2, d=128, Hd=128, V=1000, prefix_len=[9, 9], parents=[good, bad],
+                     rule="greedy", tau=0.0, seed=1, tokens=("rank", 0.9), rng=rng)
+    r, status = _fused_vs_separate(case, d)
+    assert status == 4  # SPEC_ERR_BAD_TREE
+    assert int(r["accept_len"][1]) == 0 and int(r["new_len"][1]) == 10

@@ -173,8 +173,10 @@ def test_round_from_host_buffers_matches_the_device_round():
     host = {key: fresh[key].cpu().pin_memory() for key in ("q", "hidden", "tokens", "parent", "draft")}
     ins = [st.host_copy(host[key], t[key]) for key in host]
     for b in range(case.B):
-        for cache, fc in ((t["k"], fresh["k"]), (t["v"], fresh["v"])):
-            rows = fc[b, :, Lp[b]: Lp[b] + n].contiguous().cpu().pin_memory()
+        for name in ("k", "v"):
+            cache = t[name]
+            rows = fresh[name][b, :, Lp[b]: Lp[b] + n].contiguous().cpu().pin_memory()
+            host[f"{name}{b}"] = rows  # the descriptors hold raw pointers: keep the buffers alive
             ins.append(st.host_copy(rows, cache[b, :, Lp[b]: Lp[b] + n], rows=case.Hkv))
             cache[b, :, Lp[b]: Lp[b] + n].zero_()  # the tree slots now arrive only from the host
     res = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}

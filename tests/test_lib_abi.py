@@ -140,6 +140,16 @@ def test_workspace_queries_are_host_only(L):
     assert L.spec_verify_accept(ctypes.byref(v), odd, need, None, None) == 1
     assert L.spec_verify_accept(ctypes.byref(v), None, need, None, None) == 1
     assert L.spec_verify_accept(ctypes.byref(v), fake, need - 1, None, None) == 3
+    # the folded compaction must name the verification's own path and length
+    c = st.CompactArgs(dtype=1, batch=1, num_kv_heads=8, head_dim=128, kv_capacity=4096, path_cap=64,
+                       k_cache=fake, v_cache=fake, prefix_len=fake, path=fake, accept_len=fake)
+    other = ctypes.c_void_p((1 << 20) + 4096)
+    c.path = other
+    assert L.spec_verify_accept_compact(ctypes.byref(v), fake, need, ctypes.byref(c), None, None) == 1
+    c.path, c.path_cap = fake, 63
+    assert L.spec_verify_accept_compact(ctypes.byref(v), fake, need, ctypes.byref(c), None, None) == 1
+    c.path_cap, c.head_dim = 64, 96
+    assert L.spec_verify_accept_compact(ctypes.byref(v), fake, need, ctypes.byref(c), None, None) == 2
     v.rule = 0
     assert L.spec_verify_accept_workspace(ctypes.byref(v)) < need
 

@@ -7,6 +7,7 @@ runs in the library's CUDA kernels; if the library has not been built, every cal
 
     tree_attention(...)   -> (out, lse)          one attention layer over the draft tree
     verify_accept(...)    -> dict of outputs      LM head, acceptance, longest path, bonus token
+    verify_accept_compact(...) -> dict            the same, with the KV compaction folded in
     compact_kv(...)       -> (src_slot, new_len)  in-place KV compaction of the accepted path
     medusa_expand(...)    -> dict of outputs      draft tree tokens from Medusa heads' top-k
     medusa_topology(...)  -> (parent, rank)       pruned Cartesian topology (host arrays)
@@ -116,6 +117,9 @@ def lib():
         L.spec_verify_accept_workspace.restype = ctypes.c_size_t
         L.spec_status_string.argtypes = [ctypes.c_int32]
         L.spec_status_string.restype = ctypes.c_char_p
+        L.spec_verify_accept_compact.argtypes = [ctypes.POINTER(VerifyArgs), _vp, ctypes.c_size_t,
+                                                 ctypes.POINTER(CompactArgs), _vp, _vp]
+        L.spec_verify_accept_compact.restype = ctypes.c_int32
         L.spec_round_create.argtypes = [ctypes.POINTER(AttnArgs), _vp, ctypes.c_size_t, ctypes.POINTER(VerifyArgs),
                                         _vp, ctypes.c_size_t, ctypes.POINTER(CompactArgs), _vp,
                                         ctypes.POINTER(_vp)]
@@ -381,6 +385,30 @@ def compact_kv(k_cache, v_cache, prefix_len, path, accept_len, src_slot=None, ne
     return src_slot, new_len
 
 
+def verify_accept_compact(hidden, weight, tokens, parent, n_nodes, rule, k_cache, v_cache, prefix_len,
+                          temperature=0.0, eps=0.09, delta=0.3, seed=0, draft_probs=None, draft_to_target=None,
+                          path_cap=None, hooks=False, workspace=None, dev_status=None, stream=None, outputs=None,
+                          block_table=None):
+    """verify_accept, then the in-place compaction of the accepted paths (spec_verify_accept_compact:
+    the compaction runs inside the acceptance kernels).  Returns the verify outputs plus
+    ``src_slot`` and ``new_len``."""
+    a, outputs = verify_args(hidden, weight, tokens, parent, n_nodes, rule, temperature, eps, delta, seed,
+                             draft_probs, draft_to_target, path_cap, hooks, outputs)
+    c, src_slot, new_len = compact_args(k_cache, v_cache, prefix_len, outputs["path"], outputs["accept_len"],
+                                        block_table=block_table)
+    L = lib()
+    need = L.spec_verify_accept_workspace(ctypes.byref(a))
+    if need == 0:
+        _check(L.spec_verify_accept(ctypes.byref(a), None, 0, None, None), "spec_verify_accept")
+    ws = _workspace(need, hidden.device, workspace)
+    st = _status_buffer(dev_status, hidden.device)
+    _check(L.spec_verify_accept_compact(ctypes.byref(a), _ptr(ws), need, ctypes.byref(c), _ptr(st), _stream(stream)),
+           "spec_verify_accept_compact")
+    outputs["src_slot"] = src_slot
+    outputs["new_len"] = new_len
+    return outputs
+
+
 def verify_accept_noalloc(hidden, weight, tokens, parent, n_nodes, rule, temperature=0.0, eps=0.09, delta=0.3,
                           seed=0, draft_probs=None, draft_to_target=None, path_cap=None, hooks=False,
                           dev_status=None, stream=None, outputs=None):
@@ -470,7 +498,8 @@ def host_copy(host, device, rows=None):
     With ``rows`` = None both must be contiguous (one block).  With ``rows`` = r, the host tensor is
     contiguous [r][...] and ``device`` is a view of r equal-sized rows at a constant stride (e.g. a
     request's tree slots of every KV head in a [Hkv][L_cap][d] cache block); each row must itself
-    be contiguous."""
+    be contiguous.  The descriptor holds raw pointers: keep both tensors alive until the copies
+    have run."""
     nbytes = host.numel() * host.element_size()
     if rows is None:
         if not (host.is_contiguous() and device.is_contiguous()) or \

@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "compact.cuh"
 #include "kernels.cuh"
 
 namespace spectree {
@@ -205,6 +206,17 @@ __device__ __forceinline__ float block_sum_f(float v, float* s_tmp) {
 
 // ---- K2r: row finalisation (+ fused greedy / typical acceptance) ------------------------------
 
+// Compacts request b's accepted K/V (the path and length this call just wrote) on KV heads g0,
+// g0 + gstep, ..., with the block's dynamic shared memory as staging.
+__device__ __forceinline__ void fused_compact_tail(const AcceptParams& p, int b, int g0, int gstep) {
+  extern __shared__ uint4 s_cbuf[];
+  __syncthreads();
+  const int len = p.accept_len[b];
+  compact_request(p.cp, p.path + (size_t)b * p.path_cap, len, b, g0, gstep, s_cbuf,
+                  reinterpret_cast<int*>(s_cbuf + kCompactBufChunks));
+}
+
+
 constexpr int kFinThreads = 256;
 
 __global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(const FinalizeParams p) {
@@ -297,10 +309,13 @@ __global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(const Finaliz
   if (!s_last) return;
   __threadfence();  // every row of request b is visible from here on
   accept_tree_block(p.acc, b);
+  if (p.acc.fuse_compact) fused_compact_tail(p.acc, b, 0, 1);
 }
 
+constexpr int kFusedCompactSmem = kCompactBufChunks * 16 + kCompactBufChunks / 8 * 4;
+
 void launch_row_finalize(const FinalizeParams& p, cudaStream_t stream) {
-  row_finalize_kernel<<<p.R, kFinThreads, 0, stream>>>(p);
+  row_finalize_kernel<<<p.R, kFinThreads, p.acc.fuse_compact ? kFusedCompactSmem : 0, stream>>>(p);
 }
 
 // ---- rejection sampling ---------------------------------------------------------------------
@@ -309,7 +324,7 @@ namespace {
 constexpr int kRejThreads = 1024;
 }
 
-__global__ void __launch_bounds__(kRejThreads) accept_rejection_block_kernel(const AcceptParams p) {
+__device__ void rejection_block_walk(const AcceptParams& p) {
   __shared__ int s_parent[kMaxNodes];
   __shared__ int s_tok[kMaxNodes];
   __shared__ int s_kids[kMaxNodes];
@@ -464,6 +479,11 @@ __global__ void __launch_bounds__(kRejThreads) accept_rejection_block_kernel(con
   }
 }
 
+__global__ void __launch_bounds__(kRejThreads) accept_rejection_block_kernel(const AcceptParams p) {
+  rejection_block_walk(p);
+  if (p.fuse_compact) fused_compact_tail(p, blockIdx.x, 0, 1);
+}
+
 // ---- rejection sampling on a thread-block cluster ---------------------------------------------
 
 namespace {
@@ -508,8 +528,7 @@ __device__ __forceinline__ int next_child(const uint32_t (*kids)[kAncWords], int
 // CTAs pass the same sequence of cluster barriers.  Exchanged values (partial sums, the next
 // sibling's R and D entries) are double-buffered by barrier parity: a slot is rewritten only two
 // barriers after it was read.
-__global__ void __launch_bounds__(kRcThreads, 1)
-    accept_rejection_cluster_kernel(const AcceptParams p) {
+__device__ void rejection_cluster_walk(const AcceptParams& p) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ float4 s_dyn4[];
@@ -796,6 +815,18 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   }
 }
 
+__global__ void __launch_bounds__(kRcThreads, 1)
+    accept_rejection_cluster_kernel(const AcceptParams p) {
+  namespace cg = cooperative_groups;
+  rejection_cluster_walk(p);
+  if (p.fuse_compact) {
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();  // rank 0's path and length are visible to the whole cluster; no remote access follows
+    const int kc = (int)cl.num_blocks();
+    fused_compact_tail(p, blockIdx.x / kc, (int)cl.block_rank(), kc);
+  }
+}
+
 bool rejection_uses_cluster(int V) { return V >= 1 && V <= kRcMaxCluster * kRcSlice; }
 
 namespace {
@@ -858,7 +889,7 @@ int rejection_cluster_size(int B, int V, const int* max_clusters) {
 
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {
   if (!rejection_uses_cluster(p.V)) {
-    accept_rejection_block_kernel<<<p.B, kRejThreads, 0, stream>>>(p);
+    accept_rejection_block_kernel<<<p.B, kRejThreads, p.fuse_compact ? kFusedCompactSmem : 0, stream>>>(p);
     return cudaGetLastError();
   }
   const ClusterOccupancy& occ = cluster_occupancy();

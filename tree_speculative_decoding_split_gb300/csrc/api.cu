@@ -118,15 +118,31 @@ spec_status check_attn(const spec_attn_args* a) {
 
 struct AttnLayout {
   int32_t* depth; uint32_t* anc; int32_t* bad; int32_t* tree_bad; float* part_o; float2* part_ml;
+  float* sk_o; float2* sk_ml; int32_t* sk_cnt;
   AttnPlan plan;
   size_t bytes;
 };
+
+// The persistent stream-K kernel takes contiguous bf16 caches whose Q rows load by TMA, when the
+// work at full capacity spans at least kSkMinTilesPerSm key tiles per SM (smaller problems run
+// the one-launch split kernel, whose CTAs carry less fixed work).
+bool use_stream_k(const spec_attn_args* a, int G, int sms) {
+  if (a->dtype != SPEC_DTYPE_BF16 || a->block_table || G > 128 || 128 % G != 0 || a->batch > kSkMaxBatch)
+    return false;
+  const long long blocks = ((long long)a->n_max * G + kSkRows - 1) / kSkRows;
+  const long long tiles = (a->kv_capacity + 63) / 64 * a->batch * a->num_kv_heads * blocks;
+  // the kernel indexes tiles with 32-bit integers
+  return tiles >= (long long)kSkMinTilesPerSm * sms && tiles < 0x7fffffffLL;
+}
 
 AttnLayout layout_attn(const spec_attn_args* a, void* ws) {
   AttnLayout l;
   const int B = a->batch, N = a->n_max, W = (N + 31) / 32;
   const int G = a->num_q_heads / a->num_kv_heads;
-  l.plan = plan_attention(B, N, G, a->num_kv_heads, a->kv_capacity, num_sms_current());
+  const int sms = num_sms_current();
+  l.plan = plan_attention(B, N, G, a->num_kv_heads, a->kv_capacity, sms);
+  l.plan.sk = use_stream_k(a, G, sms) ? 1 : 0;
+  l.plan.sk_grid = sms;
   Carver c(ws);
   l.depth = c.take<int32_t>((size_t)B * N);
   l.anc = c.take<uint32_t>((size_t)B * N * W);
@@ -134,7 +150,15 @@ AttnLayout layout_attn(const spec_attn_args* a, void* ws) {
   l.tree_bad = c.take<int32_t>(B);
   l.part_o = nullptr;
   l.part_ml = nullptr;
-  if (a->dtype == SPEC_DTYPE_BF16) {
+  l.sk_o = nullptr;
+  l.sk_ml = nullptr;
+  l.sk_cnt = nullptr;
+  if (l.plan.sk) {
+    l.plan.n_rg = (N * G + kSkRows - 1) / kSkRows;
+    l.sk_cnt = c.take<int32_t>((size_t)B * a->num_kv_heads * l.plan.n_rg * 2);
+    l.sk_ml = c.take<float2>((size_t)sms * 2 * kSkRows);
+    l.sk_o = c.take<float>((size_t)sms * 2 * kSkRows * a->head_dim);
+  } else if (a->dtype == SPEC_DTYPE_BF16) {
     const size_t rows = (size_t)B * N * a->num_q_heads;
     l.part_o = c.take<float>(rows * l.plan.n_split * a->head_dim);
     l.part_ml = c.take<float2>(rows * l.plan.n_split);
@@ -240,6 +264,29 @@ spec_status check_compact(const spec_compact_args* a) {
   return SPEC_OK;
 }
 
+CompactParams compact_params(const spec_compact_args* a, int32_t* dev_status) {
+  CompactParams c;
+  std::memset(&c, 0, sizeof(c));
+  c.k = static_cast<uint8_t*>(a->k_cache);
+  c.v = static_cast<uint8_t*>(a->v_cache);
+  c.row_bytes = a->head_dim * (a->dtype == SPEC_DTYPE_BF16 ? 2 : 4);
+  c.prefix_len = a->prefix_len;
+  c.Hkv = a->num_kv_heads;
+  c.L_cap = a->kv_capacity;
+  c.path_cap = a->path_cap;
+  c.src_slot = a->src_slot;
+  c.new_len = a->new_len;
+  c.dev_status = dev_status;
+  if (a->block_table) {
+    c.pg.table = a->block_table;
+    c.pg.bs = a->block_size;
+    c.pg.bs_shift = log2_of(a->block_size);
+    c.pg.max_blocks = a->max_blocks;
+    c.pg.num_blocks = a->num_blocks;
+  }
+  return c;
+}
+
 }  // namespace
 
 extern "C" {
@@ -322,6 +369,17 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
       if (!make_map_bf16(&tmQ, a->q, 4, qd, qs, qb)) return SPEC_ERR_CUDA;
       p.q_tma = 1;
     }
+    if (l.plan.sk) {
+      p.sk_o = l.sk_o;
+      p.sk_ml = l.sk_ml;
+      p.sk_cnt = l.sk_cnt;
+      const size_t cnt_bytes = (size_t)B * Hkv * l.plan.n_rg * 2 * sizeof(int32_t);
+      if (cudaMemsetAsync(l.sk_cnt, 0, cnt_bytes, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+      record(a->timing_begin, stream);
+      if (launch_attention_sk(&tmQ, &tmK, &tmV, p, l.plan.sk_grid, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+      record(a->timing_end, stream);
+      return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    }
     p.direct = p.n_split == 1 ? 1 : 0;
     record(a->timing_begin, stream);
     if (launch_attention_tc(&tmQ, &tmK, &tmV, p, stream) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -336,8 +394,14 @@ size_t spec_verify_accept_workspace(const spec_verify_args* a) {
   return layout_verify(a, nullptr).bytes;
 }
 
-spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_t workspace_bytes,
-                               int32_t* dev_status, void* stream_ptr) {
+}  // extern "C"
+
+namespace {
+
+// spec_verify_accept, and with `cmp` non-null the compaction of each request's accepted path,
+// folded into the tail of the kernel that decides the request.
+spec_status verify_accept_impl(const spec_verify_args* a, void* workspace, size_t workspace_bytes,
+                               const spec_compact_args* cmp, int32_t* dev_status, void* stream_ptr) {
   spec_status st = check_verify(a);
   if (st != SPEC_OK) return st;
   if (!workspace || !aligned16(workspace)) return SPEC_ERR_INVALID_ARGUMENT;
@@ -394,6 +458,10 @@ spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_
   ap.accept_len = a->accept_len; ap.path = a->path; ap.bonus = a->bonus_token;
   ap.margin_count = a->margin_count; ap.bonus_margin = a->bonus_margin;
   ap.dev_status = dev_status;
+  if (cmp) {
+    ap.fuse_compact = 1;
+    ap.cp = compact_params(cmp, dev_status);
+  }
 
   FinalizeParams fp;
   std::memset(&fp, 0, sizeof(fp));
@@ -410,21 +478,31 @@ spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" {
+
+spec_status spec_verify_accept(const spec_verify_args* a, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream_ptr) {
+  return verify_accept_impl(a, workspace, workspace_bytes, nullptr, dev_status, stream_ptr);
+}
+
+spec_status spec_verify_accept_compact(const spec_verify_args* a, void* workspace, size_t workspace_bytes,
+                                       const spec_compact_args* c, int32_t* dev_status, void* stream_ptr) {
+  spec_status st = check_verify(a);
+  if (st != SPEC_OK) return st;
+  st = check_compact(c);
+  if (st != SPEC_OK) return st;
+  if (c->path != a->path || c->accept_len != a->accept_len || c->path_cap != a->path_cap || c->batch != a->batch)
+    return SPEC_ERR_INVALID_ARGUMENT;
+  return verify_accept_impl(a, workspace, workspace_bytes, c, dev_status, stream_ptr);
+}
+
 spec_status spec_compact_kv(const spec_compact_args* a, int32_t* dev_status, void* stream_ptr) {
   spec_status st = check_compact(a);
   if (st != SPEC_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  PagedKV pg = {};
-  if (a->block_table) {
-    pg.table = a->block_table;
-    pg.bs = a->block_size;
-    pg.bs_shift = log2_of(a->block_size);
-    pg.max_blocks = a->max_blocks;
-    pg.num_blocks = a->num_blocks;
-  }
-  launch_compact_kv(a->k_cache, a->v_cache, a->dtype == SPEC_DTYPE_BF16 ? 2 : 4, a->prefix_len, a->path,
-                    a->accept_len, a->batch, a->num_kv_heads, a->head_dim, a->kv_capacity, a->path_cap, a->src_slot,
-                    a->new_len, dev_status, pg, stream);
+  launch_compact_kv(compact_params(a, dev_status), a->path, a->accept_len, a->batch, stream);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

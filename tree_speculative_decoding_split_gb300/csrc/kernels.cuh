@@ -47,11 +47,23 @@ struct AttnParams {
                      // the request's tree or capacity check failed (the merge zeroes its rows)
   int q_tma;         // bf16: Q rows arrive by TMA through the (d, Hq, N, B) map (128 % G == 0)
   int direct;        // bf16, one split: the kernel writes out / lse itself and no merge runs
+  // persistent stream-K kernel (n_rg then counts 256-row blocks)
+  float* sk_o;       // [grid][2][256][d] normalised partial outputs of the CTAs' partial pieces
+  float2* sk_ml;     // [grid][2][256] (running max in log2 units, sum) of those partials
+  int32_t* sk_cnt;   // [B * Hkv * n_rg][2] arrival counters, zeroed before each launch
 };
 
 struct AttnPlan {
   int n_rg, chunk, n_split, groups;
+  int sk;            // 1: the persistent stream-K kernel (attention_sk.cu) runs instead
+  int sk_grid;       // its CTAs (one per SM)
 };
+constexpr int kSkMaxBatch = 1024;  // requests the stream-K kernel schedules in shared memory
+constexpr int kSkRows = 256;       // (node, GQA head) rows per stream-K segment
+// Stream-K when the work (at full capacity) spans at least this many tiles per SM.
+constexpr int kSkMinTilesPerSm = 4;
+cudaError_t launch_attention_sk(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                const AttnParams& p, int grid, cudaStream_t stream);
 AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_sms);
 void launch_attention_merge_bf16(const AttnParams& p, cudaStream_t stream);
 int attention_tc_rows_per_cta(int groups);
@@ -83,6 +95,24 @@ cudaError_t launch_lmhead_bf16(const CUtensorMap* tmW, const CUtensorMap* tmH, c
                                int num_sms, cudaStream_t stream);
 void launch_lmhead_f32(const float* H, const float* W, const LmParams& p, cudaStream_t stream);
 
+// ---- K4: KV compaction ----------------------------------------------------------------------
+struct PagedKV {
+  const int32_t* table;  // [B][max_blocks], nullptr = contiguous caches
+  int bs, bs_shift, max_blocks, num_blocks;
+};
+struct CompactParams {
+  uint8_t* k;                // caches (or pools), updated in place
+  uint8_t* v;
+  int row_bytes;             // bytes of one K (or V) row: head_dim x element size
+  const int32_t* prefix_len; // [B]
+  int Hkv;
+  long long L_cap;
+  int path_cap;
+  int32_t* src_slot;         // [B][path_cap] or nullptr
+  int32_t* new_len;          // [B] or nullptr
+  int32_t* dev_status;
+  PagedKV pg;
+};
 // ---- K3: acceptance + longest path ----------------------------------------------------------
 struct AcceptParams {
   int B, N, V, Vd, rule, path_cap;
@@ -100,6 +130,8 @@ struct AcceptParams {
   float* rbuf;                 // [B][2][V] residual buffers (rejection)
   int32_t* accept_len; int32_t* path; int32_t* bonus; int32_t* margin_count; int32_t* bonus_margin;
   int32_t* dev_status;
+  int fuse_compact;            // compact the accepted path's K/V at the end of the decision
+  CompactParams cp;            // (its path and length are this call's outputs)
 };
 
 // K2r: per-row statistics from the LM-head records, the child logit of each node, and (greedy /
@@ -180,14 +212,8 @@ struct EagleTreeParams {
 };
 void launch_eagle_tree(const EagleTreeParams& p, cudaStream_t stream);
 
-// ---- K4: KV compaction ----------------------------------------------------------------------
-struct PagedKV {
-  const int32_t* table;  // [B][max_blocks], nullptr = contiguous caches
-  int bs, bs_shift, max_blocks, num_blocks;
-};
-void launch_compact_kv(void* k, void* v, int elem_bytes, const int32_t* prefix_len,
-                       const int32_t* path, const int32_t* accept_len, int B, int Hkv, int d,
-                       long long L_cap, int path_cap, int32_t* src_slot, int32_t* new_len,
-                       int32_t* dev_status, const PagedKV& pg, cudaStream_t stream);
+constexpr int kCompactBufChunks = 2048;  // 32 KB of staged rows (64 bf16 rows of d = 128, K and V)
+void launch_compact_kv(const CompactParams& c, const int32_t* path, const int32_t* accept_len, int B,
+                       cudaStream_t stream);
 
 }  // namespace spectree

@@ -34,8 +34,14 @@ extern "C" spec_status spec_round_create(const spec_attn_args* attn, void* attn_
   }
   spec_status st = SPEC_OK;
   if (attn) st = spec_tree_attention(attn, attn_workspace, attn_workspace_bytes, dev_status, s);
-  if (st == SPEC_OK && verify) st = spec_verify_accept(verify, verify_workspace, verify_workspace_bytes, dev_status, s);
-  if (st == SPEC_OK && compact) st = spec_compact_kv(compact, dev_status, s);
+  // a compaction of the verification's own outputs is folded into the acceptance kernels
+  const bool fuse = verify && compact && compact->path == verify->path && compact->accept_len == verify->accept_len &&
+                    compact->path_cap == verify->path_cap && compact->batch == verify->batch;
+  if (st == SPEC_OK && fuse)
+    st = spec_verify_accept_compact(verify, verify_workspace, verify_workspace_bytes, compact, dev_status, s);
+  else if (st == SPEC_OK && verify)
+    st = spec_verify_accept(verify, verify_workspace, verify_workspace_bytes, dev_status, s);
+  if (st == SPEC_OK && compact && !fuse) st = spec_compact_kv(compact, dev_status, s);
   cudaGraph_t graph = nullptr;
   const cudaError_t end = cudaStreamEndCapture(s, &graph);  // always ends the capture
   cudaStreamDestroy(s);
