@@ -45,8 +45,10 @@ CSRC = os.path.join(ROOT, "tree_speculative_decoding_split_gb300", "csrc")
 KERNEL_SOURCES = {
     "attn_tc_kernel": ["attention_tc.cu", "tc_ptx.cuh", "common.cuh"],
     "attn_sk_kernel": ["attention_sk.cu", "tc_ptx.cuh", "common.cuh"],
+    "attn_merge_bf16_kernel": ["attention.cu", "common.cuh"],
     "lmhead_tc_kernel": ["lmhead.cu", "tc_ptx.cuh", "common.cuh"],
     "lmhead_tc_rows_kernel": ["lmhead.cu", "tc_ptx.cuh", "common.cuh"],
+    "compact_kv_kernel": ["compact.cu", "compact.cuh", "common.cuh"],
 }
 
 

@@ -91,7 +91,7 @@ typedef struct spec_attn_args {
   int32_t head_dim;       /* d: 64 or 128 */
   int64_t kv_capacity;    /* L_cap, slots per (request, KV head) in the caches */
   float scale;            /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
-  int32_t reserved0;      /* must be 0 */
+  int32_t schedule;       /* SPEC_ATTN_SPLIT_KV (0) or SPEC_ATTN_STREAM_K (1), see below */
   const void* q;          /* [B][N][Hq][d] */
   const void* k_cache;    /* [B][Hkv][L_cap][d] */
   const void* v_cache;    /* [B][Hkv][L_cap][d] */
@@ -115,6 +115,20 @@ typedef struct spec_attn_args {
   int32_t num_blocks;     /* blocks per pool; num_blocks * Hkv < 2^31 */
   int32_t reserved1;      /* must be 0 */
 } spec_attn_args;
+
+/* Work schedules of the bf16 kernels (the results are the same up to rounding):
+ *   SPEC_ATTN_SPLIT_KV  one CTA per (request, KV head, key split, 256 rows), the key splits chosen
+ *                       on the host from kv_capacity and merged by a second kernel when there
+ *                       are several.  Every layout and size.
+ *   SPEC_ATTN_STREAM_K  a persistent kernel, one CTA per SM, each taking an equal share of all
+ *                       key tiles; partially covered (request, KV head, row block) segments are
+ *                       merged by the last CTA to finish one.  Contiguous bf16 caches, Hq / Hkv
+ *                       dividing 128, batch <= 1024; SPEC_ERR_UNSUPPORTED otherwise.  Balances
+ *                       batches of very uneven prefixes without a host-side plan, but pays at
+ *                       every segment boundary for partial stores and reloads, which the split
+ *                       kernel does not. */
+#define SPEC_ATTN_SPLIT_KV 0
+#define SPEC_ATTN_STREAM_K 1
 
 /* Bytes of workspace spec_tree_attention needs for these shapes (0 on invalid args).  The
  * workspace (device memory, 16-byte aligned: the split partials are written there by bulk

@@ -120,7 +120,7 @@ def test_llama70b_b4_long_context_sampled():
             assert (o[b, n:] == 0).all() and (l[b, n:] == 0).all()
 
 
-# ---- the persistent stream-K kernel (long caches) ----------------------------------------------
+# ---- the persistent stream-K schedule ----------------------------------------------------------
 
 def _align(x):
     return (x + 255) // 256 * 256
@@ -141,7 +141,8 @@ def _run_stream_k(case, d):
     import torch
     import tree_speculative_decoding_split_gb300 as st
     t = H.to_device(case, d)
-    aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"])
+    aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"],
+                                schedule="stream_k")
     sms = torch.cuda.get_device_properties(d).multi_processor_count
     need = st.lib().spec_tree_attention_workspace(ctypes.byref(aa))
     assert need == _stream_k_workspace(case.B, case.N, case.Hq, case.Hkv, case.d, sms), "not the stream-K path"
@@ -158,9 +159,9 @@ def _run_stream_k(case, d):
 
 @pytest.mark.parametrize("hd,Hq,Hkv", [(128, 8, 2), (64, 4, 4), (128, 16, 2)])
 def test_stream_k_few_tiles_in_a_long_cache(hd, Hq, Hkv):
-    """A 40000-slot cache takes the stream-K kernel, but the prefixes are short: fewer tiles than
-    SMs, so segments split into many one-tile pieces that the last arrival merges, including a
-    piece of tree keys only; ragged trees with padded nodes, an empty prefix and G = 1 / 4 / 8."""
+    """Stream-K with short prefixes in a 40000-slot cache: fewer tiles than SMs, so segments split
+    into many one-tile pieces that the last arrival merges, including a piece of tree keys only;
+    ragged trees with padded nodes, an empty prefix and G = 1 / 4 / 8."""
     d = H.dev()
     rng = np.random.default_rng(hd + Hq)
     parents = [T.random_bfs_tree(rng, n, 6)[0] for n in (37, 5, 60, 1)]
@@ -189,3 +190,14 @@ def test_stream_k_bad_tree_and_capacity_zero_their_rows():
     assert (o[1] == 0).all() and (l[1] == 0).all() and (o[2] == 0).all() and (l[2] == 0).all()
     rows = [(0, i, h) for i in range(30) for h in (0, 3, 7)]
     H.check_attention(case, o, l, rows=rows)
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+def test_stream_k_on_the_8b_workloads(cfg):
+    """The B8 ragged-prefix and B32 workloads under the stream-K schedule, against the oracle
+    (all rows at B8, sampled rows at B32)."""
+    d = H.dev()
+    case = H.config_case(cfg, 1 if cfg == 3 else 2)
+    o, l, status = _run_stream_k(case, d)
+    assert status == 0
+    H.check_attention(case, o, l, rows=None if cfg == 3 else _sample_rows(case, 96, 4))

@@ -91,6 +91,15 @@ def test_host_argument_errors_return_before_launch(L):
     assert L.spec_tree_attention(ctypes.byref(a), None, 0, None, None) == 1          # null tensors
     a.n_max = 256
     assert L.spec_tree_attention(ctypes.byref(a), None, 0, None, None) == 2          # > 255 nodes
+    fake = ctypes.c_void_p(1 << 20)
+    a = st.AttnArgs(dtype=1, batch=1, n_max=4, num_q_heads=12, num_kv_heads=4, head_dim=64, kv_capacity=16,
+                    q=fake, k_cache=fake, v_cache=fake, prefix_len=fake, n_nodes=fake, parent=fake, out=fake)
+    a.schedule = 2
+    assert L.spec_tree_attention(ctypes.byref(a), None, 0, None, None) == 1          # unknown schedule
+    a.schedule = 1
+    assert L.spec_tree_attention(ctypes.byref(a), None, 0, None, None) == 2          # stream-K: 128 % G != 0
+    a.num_q_heads, a.dtype = 8, 0
+    assert L.spec_tree_attention(ctypes.byref(a), None, 0, None, None) == 2          # stream-K: bf16 only
     v = st.VerifyArgs(dtype=1, batch=1, n_max=4, hidden=100, vocab=50, rule=0, path_cap=4)
     assert L.spec_verify_accept(ctypes.byref(v), None, 0, None, None) == 2           # bf16 hidden % 64
     v.hidden, v.rule, v.temperature = 128, 2, 0.0

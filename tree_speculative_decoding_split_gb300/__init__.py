@@ -40,7 +40,7 @@ class AttnArgs(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("batch", ctypes.c_int32), ("n_max", ctypes.c_int32),
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("kv_capacity", ctypes.c_int64), ("scale", ctypes.c_float),
-                ("reserved0", ctypes.c_int32), ("q", _vp), ("k_cache", _vp), ("v_cache", _vp),
+                ("schedule", ctypes.c_int32), ("q", _vp), ("k_cache", _vp), ("v_cache", _vp),
                 ("prefix_len", _vp), ("n_nodes", _vp), ("parent", _vp), ("out", _vp), ("lse", _vp),
                 ("timing_begin", _vp), ("timing_end", _vp), ("block_table", _vp), ("block_size", ctypes.c_int32),
                 ("max_blocks", ctypes.c_int32), ("num_blocks", ctypes.c_int32), ("reserved1", ctypes.c_int32)]
@@ -230,9 +230,14 @@ def _paged(k_cache, block_table, B, dev):
     return bs, block_table.shape[1], nb, Hkv
 
 
-def attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=None, scale=0.0, block_table=None):
+SCHEDULES = {"split_kv": 0, "stream_k": 1}
+
+
+def attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=None, scale=0.0, block_table=None,
+              schedule="split_kv"):
     """Build the C argument struct for tree attention (tensors are validated here).  With
-    ``block_table`` [B][max_blocks] the caches are paged pools [num_blocks][Hkv][block_size][d]."""
+    ``block_table`` [B][max_blocks] the caches are paged pools [num_blocks][Hkv][block_size][d];
+    ``schedule`` is "split_kv" (default) or "stream_k" (see spec_attn_args.schedule)."""
     torch = _torch()
     _need(q, "q")
     dev = q.device
@@ -261,7 +266,7 @@ def attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=No
     _need(out, "out", q.dtype, dev)
     _need(lse, "lse", torch.float32, dev)
     a = AttnArgs(dtype=_dtype_code(q), batch=B, n_max=N, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
-                 kv_capacity=L_cap, scale=float(scale), reserved0=0, q=_ptr(q), k_cache=_ptr(k_cache),
+                 kv_capacity=L_cap, scale=float(scale), schedule=SCHEDULES[schedule], q=_ptr(q), k_cache=_ptr(k_cache),
                  v_cache=_ptr(v_cache), prefix_len=_ptr(prefix_len), n_nodes=_ptr(n_nodes), parent=_ptr(parent),
                  out=_ptr(out), lse=_ptr(lse), block_table=_ptr(block_table), block_size=paged[0],
                  max_blocks=paged[1], num_blocks=paged[2], reserved1=0)
@@ -269,9 +274,10 @@ def attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=No
 
 
 def tree_attention(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, lse=None, scale=0.0,
-                   workspace=None, dev_status=None, stream=None, block_table=None):
+                   workspace=None, dev_status=None, stream=None, block_table=None, schedule="split_kv"):
     """Tree attention (see spec_tree_attention).  Returns (out, lse)."""
-    a, out, lse = attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out, lse, scale, block_table)
+    a, out, lse = attn_args(q, k_cache, v_cache, prefix_len, n_nodes, parent, out, lse, scale, block_table,
+                            schedule)
     L = lib()
     need = L.spec_tree_attention_workspace(ctypes.byref(a))
     if need == 0:

@@ -97,7 +97,7 @@ spec_status check_attn(const spec_attn_args* a) {
   if (a->dtype != SPEC_DTYPE_F32 && a->dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
   if (a->head_dim != 64 && a->head_dim != 128) return SPEC_ERR_UNSUPPORTED;
   if (a->batch < 1 || a->n_max < 1 || a->num_q_heads < 1 || a->num_kv_heads < 1 || a->kv_capacity < 1 ||
-      a->reserved0 != 0)
+      (a->schedule != SPEC_ATTN_SPLIT_KV && a->schedule != SPEC_ATTN_STREAM_K))
     return SPEC_ERR_INVALID_ARGUMENT;
   if (a->n_max > SPEC_MAX_NODES) return SPEC_ERR_UNSUPPORTED;
   if (a->num_q_heads % a->num_kv_heads) return SPEC_ERR_INVALID_ARGUMENT;
@@ -113,6 +113,14 @@ spec_status check_attn(const spec_attn_args* a) {
     const spec_status ps = check_paged(a->block_size, a->max_blocks, a->num_blocks, a->num_kv_heads, a->kv_capacity);
     if (ps != SPEC_OK) return ps;
   }
+  if (a->schedule == SPEC_ATTN_STREAM_K) {
+    const int G = a->num_q_heads / a->num_kv_heads;
+    if (a->dtype != SPEC_DTYPE_BF16 || a->block_table || G > 128 || 128 % G != 0 || a->batch > kSkMaxBatch)
+      return SPEC_ERR_UNSUPPORTED;
+    const long long blocks = ((long long)a->n_max * G + kSkRows - 1) / kSkRows;
+    if ((a->kv_capacity + 63) / 64 * a->batch * a->num_kv_heads * blocks >= 0x7fffffffLL)
+      return SPEC_ERR_UNSUPPORTED;  // the kernel indexes tiles with 32-bit integers
+  }
   return SPEC_OK;
 }
 
@@ -123,25 +131,13 @@ struct AttnLayout {
   size_t bytes;
 };
 
-// The persistent stream-K kernel takes contiguous bf16 caches whose Q rows load by TMA, when the
-// work at full capacity spans at least kSkMinTilesPerSm key tiles per SM (smaller problems run
-// the one-launch split kernel, whose CTAs carry less fixed work).
-bool use_stream_k(const spec_attn_args* a, int G, int sms) {
-  if (a->dtype != SPEC_DTYPE_BF16 || a->block_table || G > 128 || 128 % G != 0 || a->batch > kSkMaxBatch)
-    return false;
-  const long long blocks = ((long long)a->n_max * G + kSkRows - 1) / kSkRows;
-  const long long tiles = (a->kv_capacity + 63) / 64 * a->batch * a->num_kv_heads * blocks;
-  // the kernel indexes tiles with 32-bit integers
-  return tiles >= (long long)kSkMinTilesPerSm * sms && tiles < 0x7fffffffLL;
-}
-
 AttnLayout layout_attn(const spec_attn_args* a, void* ws) {
   AttnLayout l;
   const int B = a->batch, N = a->n_max, W = (N + 31) / 32;
   const int G = a->num_q_heads / a->num_kv_heads;
   const int sms = num_sms_current();
   l.plan = plan_attention(B, N, G, a->num_kv_heads, a->kv_capacity, sms);
-  l.plan.sk = use_stream_k(a, G, sms) ? 1 : 0;
+  l.plan.sk = a->schedule == SPEC_ATTN_STREAM_K ? 1 : 0;
   l.plan.sk_grid = sms;
   Carver c(ws);
   l.depth = c.take<int32_t>((size_t)B * N);

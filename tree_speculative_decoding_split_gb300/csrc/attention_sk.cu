@@ -534,21 +534,6 @@ __global__ void __launch_bounds__(SkCfg<D>::kThreads, 1)
       size_t orow = 0;
       if (valid) orow = ((size_t)b * p.N + node) * p.Hq + g * p.G + row % p.G;
       if (fin) tc_fence_after();
-      // writes the final bf16 row from 32-column chunks produced by `chunk` and the LSE
-      auto write_final = [&](auto&& chunk, float lse2) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          chunk(c, o);
-#pragma unroll
-          for (int j = 0; j < 32; j += 8)
-            *reinterpret_cast<uint4*>(out + c * 32 + j) =
-                make_uint4(pack_bf16x2(o[j], o[j + 1]), pack_bf16x2(o[j + 2], o[j + 3]),
-                           pack_bf16x2(o[j + 4], o[j + 5]), pack_bf16x2(o[j + 6], o[j + 7]));
-        }
-        if (p.lse) p.lse[orow] = lse2 * 0.69314718055994531f;
-      };
       if (whole) {
         const float inv = (live && l_run > 0.f) ? 1.f / l_run : 0.f;
         if (valid && p.lse) p.lse[orow] = (live && l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : 0.f;
@@ -597,8 +582,8 @@ __global__ void __launch_bounds__(SkCfg<D>::kThreads, 1)
         __threadfence();
         named_bar_sync(bar_id, 128);
         const int segid = (b * p.Hkv + g) * p.n_rg + rg;
+        const int c_first = sc.cta_of(pc.seg_off), c_last = sc.cta_of(pc.seg_off + pc.T - 1);
         if (rl == 0) {
-          const int c_first = sc.cta_of(pc.seg_off), c_last = sc.cta_of(pc.seg_off + pc.T - 1);
           int last = 0;
           if (ok) last = atomicAdd(&p.sk_cnt[segid * kNG + a], 1) == (c_last - c_first);
           s_last[a] = last;
@@ -606,45 +591,82 @@ __global__ void __launch_bounds__(SkCfg<D>::kThreads, 1)
         named_bar_sync(bar_id, 128);
         if (s_last[a]) {
           __threadfence();
-          // merge every piece of the segment (this one included) for this thread's row; lane CTA
-          // c is block c * n_rg + rg, whose partial slots hold its pieces
-          const int c_first = sc.cta_of(pc.seg_off), c_last = sc.cta_of(pc.seg_off + pc.T - 1);
-          float M = -INFINITY;
-          for (int c = c_first; c <= c_last; ++c) {
+          // Merge every piece of the segment for this thread's row.  This CTA's own piece is still
+          // in TMEM (O unnormalised, with m_run / l_run); the other pieces' partials (lane CTA c is
+          // block c * n_rg + rg) are read from L2 with several loads in flight at once -- under a
+          // saturated memory system a round trip costs about a microsecond.
+          constexpr int kBatch = 2;  // other pieces whose rows are in flight together
+          auto rec_of = [&](int c) -> size_t {
             const int sl = (sc.begin(c) >= pc.seg_off) ? 0 : 1;
-            const float2 ml = __ldcg(p.sk_ml + (((size_t)c * p.n_rg + rg) * 2 + sl) * kSegRows + rr);
-            if (ml.y > 0.f) M = fmaxf(M, ml.x);
-          }
-          float wsum = 0.f;
-          for (int c = c_first; c <= c_last; ++c) {
-            const int sl = (sc.begin(c) >= pc.seg_off) ? 0 : 1;
-            const float2 ml = __ldcg(p.sk_ml + (((size_t)c * p.n_rg + rg) * 2 + sl) * kSegRows + rr);
-            if (ml.y > 0.f) wsum += ml.y * exp2f(ml.x - M);
-          }
-          const float inv = (live && wsum > 0.f) ? 1.f / wsum : 0.f;
-          const float lse2 = (live && wsum > 0.f) ? M + log2f(wsum) : 0.f;
-          if (valid)
-            write_final([&](int ch, float (&o)[32]) {
+            return (((size_t)c * p.n_rg + rg) * 2 + sl) * kSegRows + rr;
+          };
+          float M = (fin && l_run > 0.f) ? m_run : -INFINITY;
+          for (int c0 = c_first; c0 <= c_last; c0 += 4) {  // records, four at a time
+            float2 ml[4];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = 0.f;
-              if (!live) return;
-              for (int c = c_first; c <= c_last; ++c) {
-                const int sl = (sc.begin(c) >= pc.seg_off) ? 0 : 1;
-                const size_t q = (((size_t)c * p.n_rg + rg) * 2 + sl) * kSegRows + rr;
-                const float2 ml = __ldcg(p.sk_ml + q);
-                if (!(ml.y > 0.f)) continue;
-                const float wgt = ml.y * exp2f(ml.x - M) * inv;
-                const float4* src = reinterpret_cast<const float4*>(p.sk_o + q * D + ch * 32);
+            for (int k2 = 0; k2 < 4; ++k2)
+              ml[k2] = (c0 + k2 <= c_last && c0 + k2 != cta) ? __ldcg(p.sk_ml + rec_of(c0 + k2))
+                                                             : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2)
+              if (ml[k2].y > 0.f) M = fmaxf(M, ml[k2].x);
+          }
+          const float own = (fin && l_run > 0.f) ? exp2f(m_run - M) : 0.f;
+          float wsum = l_run * own;
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + orow * D;
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ++ch) {
+            float acc[32];
+            uint32_t o[32];
+            if (fin) {  // warp-collective
+              tmem_ld_x32(tO + ch * 32, o);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = own * __uint_as_float(o[j]);
+#pragma unroll 1
+            for (int c0 = c_first; c0 <= c_last; c0 += kBatch) {
+              float2 ml[kBatch];
+              size_t q[kBatch];
+              float4 x[kBatch][8];
+#pragma unroll
+              for (int k2 = 0; k2 < kBatch; ++k2) {
+                const bool use = c0 + k2 <= c_last && c0 + k2 != cta;
+                q[k2] = use ? rec_of(c0 + k2) : 0;
+                ml[k2] = use ? __ldcg(p.sk_ml + q[k2]) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  x[k2][j] = use ? __ldcg(reinterpret_cast<const float4*>(p.sk_o + q[k2] * D + ch * 32) + j)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+              for (int k2 = 0; k2 < kBatch; ++k2) {
+                const float w = (ml[k2].y > 0.f) ? ml[k2].y * exp2f(ml[k2].x - M) : 0.f;
+                if (ch == 0) wsum += w;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                  const float4 x = __ldcg(src + j);
-                  o[4 * j] = fmaf(wgt, x.x, o[4 * j]);
-                  o[4 * j + 1] = fmaf(wgt, x.y, o[4 * j + 1]);
-                  o[4 * j + 2] = fmaf(wgt, x.z, o[4 * j + 2]);
-                  o[4 * j + 3] = fmaf(wgt, x.w, o[4 * j + 3]);
+                  acc[4 * j] = fmaf(w, x[k2][j].x, acc[4 * j]);
+                  acc[4 * j + 1] = fmaf(w, x[k2][j].y, acc[4 * j + 1]);
+                  acc[4 * j + 2] = fmaf(w, x[k2][j].z, acc[4 * j + 2]);
+                  acc[4 * j + 3] = fmaf(w, x[k2][j].w, acc[4 * j + 3]);
                 }
               }
-            }, lse2);
+            }
+            if (valid) {
+              // partials are normalised o; the own piece is unnormalised O: both weighted to units
+              // of 2^M above, so dividing by the total weight gives the row
+              const float inv = (live && wsum > 0.f) ? 1.f / wsum : 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; j += 8)
+                *reinterpret_cast<uint4*>(out + ch * 32 + j) =
+                    make_uint4(pack_bf16x2(acc[j] * inv, acc[j + 1] * inv), pack_bf16x2(acc[j + 2] * inv, acc[j + 3] * inv),
+                               pack_bf16x2(acc[j + 4] * inv, acc[j + 5] * inv), pack_bf16x2(acc[j + 6] * inv, acc[j + 7] * inv));
+            }
+          }
+          if (valid && p.lse) p.lse[orow] = (live && wsum > 0.f) ? (M + log2f(wsum)) * 0.69314718055994531f : 0.f;
           if (bad && g == 0 && rg == 0 && rr == 0)
             set_status(p.dev_status, tree_bad ? SPEC_ERR_BAD_TREE : SPEC_ERR_CAPACITY);
         }

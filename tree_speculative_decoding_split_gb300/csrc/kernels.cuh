@@ -60,8 +60,6 @@ struct AttnPlan {
 };
 constexpr int kSkMaxBatch = 1024;  // requests the stream-K kernel schedules in shared memory
 constexpr int kSkRows = 256;       // (node, GQA head) rows per stream-K segment
-// Stream-K when the work (at full capacity) spans at least this many tiles per SM.
-constexpr int kSkMinTilesPerSm = 4;
 cudaError_t launch_attention_sk(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                                 const AttnParams& p, int grid, cudaStream_t stream);
 AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_sms);
