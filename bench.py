@@ -244,14 +244,14 @@ def _device_tensors(case, dev):
 
 def _attention_plan(L, aa, case, sms):
     """(stream_k, key splits) of the attention plan, read back from the workspace query: the
-    stream-K kernel's workspace holds two 256-row partial slots per SM, the split kernel's fp32
-    partials of d + 2 floats per row and split."""
+    stream-K kernel's workspace holds two 256-row partial slots per SM, the split kernel's partials
+    of d bf16 values and two floats per row and split."""
     ws = int(L.spec_tree_attention_workspace(ctypes.byref(aa)))
     sk = sms * 2 * 256 * (case.d * 4 + 8)
     if case.dtype == "bf16" and sk <= ws < sk + (8 << 20):
         return True, 1
     rows = case.B * case.N * case.Hq
-    return False, max(1, ws // (rows * (case.d * 4 + 8)))
+    return False, max(1, ws // (rows * (case.d * 2 + 8)))
 
 
 def _launches_per_step(case, n_split, stream_k, fused):

@@ -125,7 +125,7 @@ spec_status check_attn(const spec_attn_args* a) {
 }
 
 struct AttnLayout {
-  int32_t* depth; uint32_t* anc; int32_t* bad; int32_t* tree_bad; float* part_o; float2* part_ml;
+  int32_t* depth; uint32_t* anc; int32_t* bad; int32_t* tree_bad; uint16_t* part_o; float2* part_ml;
   float* sk_o; float2* sk_ml; int32_t* sk_cnt;
   AttnPlan plan;
   size_t bytes;
@@ -156,7 +156,7 @@ AttnLayout layout_attn(const spec_attn_args* a, void* ws) {
     l.sk_o = c.take<float>((size_t)sms * 2 * kSkRows * a->head_dim);
   } else if (a->dtype == SPEC_DTYPE_BF16) {
     const size_t rows = (size_t)B * N * a->num_q_heads;
-    l.part_o = c.take<float>(rows * l.plan.n_split * a->head_dim);
+    l.part_o = c.take<uint16_t>(rows * l.plan.n_split * a->head_dim);
     l.part_ml = c.take<float2>(rows * l.plan.n_split);
   }
   l.bytes = c.off;
@@ -196,7 +196,7 @@ struct VerifyLayout {
   float4* part; int* part_idx;
   float *rmax, *rlse, *rent, *rgap, *clog; int32_t* rarg;
   float* logits; float* rbuf; int32_t* inv; int32_t* map_bad; int32_t* counters;
-  int R, n_vt, BN, BNV, n_nc, cpc, n_parts;
+  int R, n_vt, BN, BNV, n_nc, cpc, n_parts, pair;
   size_t bytes;
 };
 
@@ -209,10 +209,20 @@ VerifyLayout layout_verify(const spec_verify_args* a, void* ws) {
   l.n_nc = (l.R + l.BN - 1) / l.BN;
   const int sms = num_sms_current();
   // BN == 128: tree rows on the MMA M side, BNV vocabulary entries per tile; else vocabulary
-  // on M in tiles of 128 and BN tree rows on N
-  l.BNV = (l.BN == 128) ? lmhead_rows_bnv(l.n_nc, sms) : 128;
-  const int tiles = (a->vocab + l.BNV - 1) / l.BNV;
-  l.cpc = sms / l.n_nc;
+  // on M in tiles of 128 and BN tree rows on N.  Above 128 rows (bf16) CTA pairs take 256 rows per
+  // MMA, 256 vocabulary entries per tile, cpc clusters per row pair.
+  l.pair = (a->dtype == SPEC_DTYPE_BF16 && l.BN == 128 && l.R > kLmPairMinRows) ? 1 : 0;
+  int tiles;
+  if (l.pair) {
+    l.n_nc = (l.R + 255) / 256;
+    l.BNV = 256;
+    tiles = (a->vocab + 255) / 256;
+    l.cpc = (sms / 2) / l.n_nc;
+  } else {
+    l.BNV = (l.BN == 128) ? lmhead_rows_bnv(l.n_nc, sms) : 128;
+    tiles = (a->vocab + l.BNV - 1) / l.BNV;
+    l.cpc = sms / l.n_nc;
+  }
   if (l.cpc < 1) l.cpc = 1;
   if (l.cpc > tiles) l.cpc = tiles;
   // statistics records per row: one per CTA of the row's chunk (bf16), one per tile (fp32)
@@ -412,6 +422,7 @@ spec_status verify_accept_impl(const spec_verify_args* a, void* workspace, size_
   LmParams lp;
   std::memset(&lp, 0, sizeof(lp));
   lp.R = l.R; lp.V = V; lp.Hd = Hd; lp.n_vt = l.n_vt; lp.n_nc = l.n_nc; lp.BN = l.BN; lp.BNV = l.BNV; lp.cpc = l.cpc;
+  lp.pair = l.pair;
   lp.inv_tau = inv_tau;
   lp.part = l.part;
   lp.part_idx = l.part_idx;
@@ -424,7 +435,7 @@ spec_status verify_accept_impl(const spec_verify_args* a, void* workspace, size_
     const cuuint64_t dW[2] = {(cuuint64_t)Hd, (cuuint64_t)V};
     const cuuint64_t dH[2] = {(cuuint64_t)Hd, (cuuint64_t)l.R};
     const cuuint64_t str[1] = {(cuuint64_t)Hd * 2};
-    const cuuint32_t bW[2] = {64, (cuuint32_t)l.BNV};
+    const cuuint32_t bW[2] = {64, (cuuint32_t)(l.pair ? l.BNV / 2 : l.BNV)};  // a pair CTA loads half a tile
     const cuuint32_t bH[2] = {64, (cuuint32_t)l.BN};
     if (!make_map_bf16(&tmW, a->lm_head_weight, 2, dW, str, bW) ||
         !make_map_bf16(&tmH, a->hidden_states, 2, dH, str, bH))

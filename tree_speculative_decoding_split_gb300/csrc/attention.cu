@@ -5,8 +5,8 @@
 // "EAGLE-3とMedusaで実装するSpeculative Decoding実践ガイド", section "並列検証"); each tree node
 // attends only to its ancestors and itself (tech-tldr "多トークン予測（Medusa・EAGLE）", section
 // "ツリー検証"; qiita, section "Tree Attention").  Each split of the bf16 kernel writes a normalised
-// partial (o, running max in log2 units, sum); the merge kernel combines them per output row with
-// warp shuffles and writes O and the natural-log LSE.
+// partial (bf16 o, running max in log2 units, sum); the merge kernel combines them per output row
+// with warp shuffles and writes O and the natural-log LSE.
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -60,13 +60,16 @@ __global__ void __launch_bounds__(256) attn_merge_bf16_kernel(const AttnParams p
       const int s = s0 + k;
       ws[k] = __shfl_sync(0xffffffffu, w, s & 31);
       if (s < p.n_split && ws[k] > 0.f) {
-        const float* src = p.part_o + (orow * p.n_split + s) * D + lane * EPL;
+        const uint16_t* src = p.part_o + (orow * p.n_split + s) * D + lane * EPL;
         if constexpr (EPL == 4) {
-          const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-          v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+          const uint2 t = __ldcg(reinterpret_cast<const uint2*>(src));
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
+          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
+          v[k][0] = a.x; v[k][1] = a.y; v[k][2] = b.x; v[k][3] = b.y;
         } else {
-          const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-          v[k][0] = t.x; v[k][1] = t.y;
+          const uint32_t t = __ldcg(reinterpret_cast<const unsigned int*>(src));
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t));
+          v[k][0] = a.x; v[k][1] = a.y;
         }
       } else {
         ws[k] = 0.f;

@@ -24,7 +24,7 @@
 //              (exact: P and the running sum use the same stale maximum).
 // Every CTA validates the tree; the CTAs of the split that holds the tree keys (the prefix split
 // containing slot L, which then also covers [L, L + n)) build the ancestor bits by pointer
-// jumping.  Each split writes a normalised partial (o, running max, sum), merged by the merge
+// jumping.  Each split writes a normalised partial (bf16 o, running max, sum), merged by the merge
 // kernel.
 
 #include "common.cuh"
@@ -626,20 +626,24 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       tc_fence_after();
       if (valid) p.part_ml[orow * p.n_split + split] = make_float2(m_run, l_run);
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      // the normalised partial row in bf16: its rounding (2^-9 relative) is far inside the output
+      // tolerance, and it halves what the merge reads
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld_x32(tO + c * 32, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(srow + (c * 32 + j) * 4) =
-              make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
-                          __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+        for (int j = 0; j < 32; j += 8)
+          *reinterpret_cast<uint4*>(srow + (c * 32 + j) * 2) =
+              make_uint4(pack_bf16x2(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv),
+                         pack_bf16x2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv),
+                         pack_bf16x2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv),
+                         pack_bf16x2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv));
       }
       if (valid) {
         fence_proxy_async_smem();  // the staged row (generic stores) becomes visible to the copy
-        bulk_store_row(p.part_o + (orow * p.n_split + split) * D, srow, D * 4);
+        bulk_store_row(p.part_o + (orow * p.n_split + split) * D, srow, D * 2);
         bulk_wait_read();
       }
     } else {

@@ -28,7 +28,7 @@ struct AttnParams {
   const uint32_t* anc;      // fp32 path: ancestor bits from the tree-prep kernel
   const int32_t* bad;       // fp32 path: per-request verdict of the tree-prep kernel
   const int32_t* parent;    // [B][N]
-  float* part_o;     // [B*N*Hq][n_split][d]
+  uint16_t* part_o;  // [B*N*Hq][n_split][d] normalised partial rows, bf16 bits
   float2* part_ml;   // [B*N*Hq][n_split] (running max in log2 units, sum)
   int B, N, Hq, Hkv, G, W, d;
   long long L_cap;
@@ -78,6 +78,7 @@ struct LmParams {
   int BN;
   int cpc;         // CTAs per node chunk (grid = cpc * n_nc); records per row of the tc kernel
   int BNV;         // rows-on-M kernel (BN == 128): vocabulary entries per tile (128 or 256)
+  int pair;        // CTA-pair kernel: n_nc counts 256-row pairs, cpc clusters per pair, 256-entry tiles
   float inv_tau;
   float4* part;    // [slot][R] {max, sumexp, sumexp*y, second max}
   int* part_idx;   // [slot][R] argmax
@@ -88,6 +89,8 @@ struct LmParams {
 };
 int lmhead_pick_bn(int R);
 int lmhead_rows_bnv(int n_nc, int num_sms);
+// The CTA-pair kernel takes more than this many tree rows (bf16).
+constexpr int kLmPairMinRows = 128;
 size_t lmhead_smem_bytes(int BN);
 cudaError_t launch_lmhead_bf16(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p,
                                int num_sms, cudaStream_t stream);

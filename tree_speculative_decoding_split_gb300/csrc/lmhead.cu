@@ -16,10 +16,12 @@
 // tiles, and keeps one running record per row in shared memory across its tiles, so it writes
 // one record per row at the end (about 150 records per row in total, merged by the row
 // finalisation kernel).  Full fp32 logits go to HBM only when the caller needs them (rejection
-// sampling), written once from the same epilogue.
+// sampling), written once from the same epilogue.  Larger batches put the tree rows on M instead:
+// 128 rows per CTA (65..128 rows), or 256 rows per MMA over a pair of CTAs (more than 128 rows).
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tc_ptx.cuh"
 
 namespace spectree {
 
@@ -29,74 +31,9 @@ constexpr int kBM = 128;  // vocabulary rows per tile (MMA M)
 constexpr int kBK = 64;   // hidden elements per stage (one 128-byte swizzle atom of bf16)
 constexpr int kLmThreads = 192;
 
-// ---- tcgen05 / TMEM wrappers ----------------------------------------------------------------
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// D[tmem] (+)= A[smem] . B[smem]^T, both K-major, bf16 -> fp32.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-        "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with 128-byte swizzle:
-// rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset
-  d |= (uint64_t)1 << 46;            // version
-  d |= (uint64_t)2 << 61;            // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
+// Shared-memory descriptor of a K-major tile written by TMA with 128-byte swizzle: 128-byte rows,
+// 8-row groups 1024 bytes apart (the leading byte offset is unused for this layout).
+__device__ __forceinline__ uint64_t sdesc_k(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
 
 // Vocabulary-on-M kernel: four 64-element k atoms per pipeline stage, so that every W row is read
 // 512 contiguous bytes at a time (measured on the 63-row, 128256 x 4096 head: 177.4 us with one
@@ -206,7 +143,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---- MMA issuer ----
-      constexpr uint32_t idesc = idesc_bf16(kBM, BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, 0);
       uint32_t it = 0;
       int lu = 0;
       bool ok = true;
@@ -227,8 +164,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           tc_fence_after();
           const int na = min(C::kAtoms, n_atoms - kb * C::kAtoms);
           for (int at = 0; at < na; ++at) {
-            const uint64_t ad = sdesc_sw128(smem_u32(sA + st * C::kStageA + at * C::kAtomA));
-            const uint64_t bd = sdesc_sw128(smem_u32(sB + st * C::kStageB + at * C::kAtomB));
+            const uint64_t ad = sdesc_k(smem_u32(sA + st * C::kStageA + at * C::kAtomA));
+            const uint64_t bd = sdesc_k(smem_u32(sB + st * C::kStageB + at * C::kAtomB));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
               umma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | at | kk) != 0);
@@ -433,7 +370,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---- MMA issuer ----
-      constexpr uint32_t idesc = idesc_bf16(kBM, BNV);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BNV, 0);
       uint32_t it = 0;
       int lu = 0;
       bool ok = true;
@@ -452,8 +389,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_sw128(smem_u32(sA + st * C::kStageA));
-          const uint64_t bd = sdesc_sw128(smem_u32(sB + st * C::kStageB));
+          const uint64_t ad = sdesc_k(smem_u32(sA + st * C::kStageA));
+          const uint64_t bd = sdesc_k(smem_u32(sB + st * C::kStageB));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
@@ -555,6 +492,223 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+// ---- CTA-pair orientation (cta_group::2): 256 tree rows per MMA over two SMs ---------------------
+// Used above 128 tree rows.  A cluster of two CTAs computes 256-row x 256-vocabulary tiles with one
+// pair MMA: each CTA stages its own 128 tree rows and its half (128 entries) of the vocabulary tile,
+// so a 64-wide k stage is 32 KB per SM instead of 48 KB and six stages fit where four did.  The
+// even CTA's MMA warp issues the MMAs and multicasts each commit to both CTAs' barriers; both
+// CTAs' TMA loads count on the even CTA's stage barrier; each CTA's epilogue drains its own tensor
+// memory (its 128 rows) as in the rows-on-M kernel and signals the even CTA when a buffer is free.
+// Cluster c owns row pair rc = c % n_nc and vocabulary tiles slot, slot + cpc, ... (slot = c / n_nc).
+struct LmPairCfg {
+  static constexpr int kN = 256;                  // vocabulary entries per pair tile (MMA N)
+  static constexpr int kStageA = kBM * kBK * 2;   // this CTA's 128 tree rows x 64 hidden
+  static constexpr int kStageB = (kN / 2) * kBK * 2;  // this CTA's half of the vocabulary tile
+  static constexpr int kStage = kStageA + kStageB;
+  static constexpr int kStages = 6;
+  static constexpr uint32_t kTmemCols = 2 * kN;   // double-buffered accumulators
+  static constexpr int kSmem = 1024 + kStages * kStage + 256;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
+    lmhead_tc_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                          const LmParams p) {
+  using C = LmPairCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + C::kStages * C::kStageA;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kStages * C::kStage);
+  uint64_t* full = bars;                  // [stage] both CTAs' tiles landed (used in the even CTA)
+  uint64_t* empty = bars + C::kStages;    // [stage] the pair MMA consumed the stage (each CTA)
+  uint64_t* tfull = empty + C::kStages;   // [buffer] accumulator ready (each CTA)
+  uint64_t* tempty = tfull + 2;           // [buffer] both CTAs drained it (used in the even CTA)
+  uint64_t* drained = tempty + 2;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int n_kb = p.Hd / kBK;
+  const int cl = blockIdx.x >> 1;
+  const int rc = cl % p.n_nc, slot = cl / p.n_nc;
+  const int n_vt = (p.V + C::kN - 1) / C::kN;
+  if (blockIdx.x == 0 && threadIdx.x < 32)
+    for (int i = threadIdx.x; i < p.n_counters; i += 32) p.counters[i] = 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(drained, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&s_tmem, C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrival or completion
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer (both CTAs): this CTA's tree rows and half vocabulary tile ----
+      const uint64_t pol_h = l2_policy_evict_last();
+      const uint64_t pol_w = (p.n_nc > 1) ? l2_policy_evict_last() : l2_policy_evict_first();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int vt = slot; vt < n_vt && ok; vt += p.cpc) {
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % C::kStages;
+          if (!mbar_wait_bounded(&empty[st], ((it / C::kStages) & 1) ^ 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[st], 2 * C::kStage);  // both CTAs' bytes
+          const uint32_t fb = cluster_addr(&full[st], 0);
+          tma_load_2d_pair(sA + st * C::kStageA, &tmH, fb, kb * kBK, rc * 2 * kBM + (int)rank * kBM, pol_h);
+          tma_load_2d_pair(sB + st * C::kStageB, &tmW, fb, kb * kBK, vt * C::kN + (int)rank * (C::kN / 2), pol_w);
+        }
+      }
+      if (!ok) {
+        s_abort = 1;
+        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---- MMA issuer (even CTA): 256 x 256 x 16 pair MMAs ----
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, C::kN, 0);
+      uint32_t it = 0;
+      int lu = 0;
+      bool ok = true;
+      for (int vt = slot; vt < n_vt && ok; vt += p.cpc, ++lu) {
+        const int a = lu & 1;
+        if (!mbar_wait_bounded(&tempty[a], ((lu >> 1) & 1) ^ 1, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(a * C::kN);
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % C::kStages;
+          if (!mbar_wait_bounded(&full[st], (it / C::kStages) & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_k(smem_u32(sA + st * C::kStageA));
+          const uint64_t bd = sdesc_k(smem_u32(sB + st * C::kStageB));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+          umma_commit_pair(&empty[st], 3);  // the stage is free in both CTAs
+        }
+        if (ok) umma_commit_pair(&tfull[a], 3);
+      }
+      if (!ok) {
+        s_abort = 1;
+        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+      }
+      umma_commit_pair(drained, 1);
+      mbar_wait_bounded(drained, 0, nullptr);
+    }
+  } else {
+    // ---- epilogue (both CTAs): thread (q, lane) owns tree row 256 rc + 128 rank + 32 q + lane ----
+    const int q = warp & 3;
+    const int n = rc * 2 * kBM + (int)rank * kBM + q * 32 + lane;
+    const bool nvalid = n < p.R;
+    constexpr float kLog2e = 1.4426950408889634f;
+    float m1 = -INFINITY, m2 = -INFINITY, s = 0.f, t = 0.f;
+    int i1 = 0x7fffffff;
+    bool failed = false;
+    int lu = 0;
+    for (int vt = slot; vt < n_vt; vt += p.cpc, ++lu) {
+      const int a = lu & 1;
+      if (!mbar_wait_bounded(&tfull[a], (lu >> 1) & 1, &s_abort)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < C::kN / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * C::kN + cc * 32), r);
+        tmem_ld_wait();
+        const int vbase = vt * C::kN + cc * 32;
+        if (p.logits && nvalid) {
+          float* dst = p.logits + (size_t)n * p.V + vbase;
+          if (vbase + 32 <= p.V && ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(dst + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+          } else {
+            for (int j = 0; j < 32; ++j)
+              if (vbase + j < p.V) dst[j] = __uint_as_float(r[j]);
+          }
+        }
+        const float m_prev = m1;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float y = (vbase + j < p.V) ? __uint_as_float(r[j]) * p.inv_tau : -INFINITY;
+          if (y > m1) {
+            m2 = m1;
+            m1 = y;
+            i1 = vbase + j;
+          } else if (y > m2) {
+            m2 = y;
+          }
+        }
+        if (m1 > -INFINITY) {
+          const float scale = (m_prev > -INFINITY) ? exp2f((m_prev - m1) * kLog2e) : 0.f;
+          s *= scale;
+          t *= scale;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (vbase + j < p.V) {  // entries past the vocabulary contribute nothing (0 * -inf is NaN)
+              const float y = __uint_as_float(r[j]) * p.inv_tau;
+              const float e = exp2f((y - m1) * kLog2e);
+              s += e;
+              t = fmaf(e, y, t);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_addr(&tempty[a], 0));
+    }
+    if (failed) {
+      if (lane == 0) {
+        s_abort = 1;
+        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
+      }
+    } else if (nvalid) {
+      p.part[(size_t)slot * p.R + n] = make_float4(m1, s, t, m2);
+      p.part_idx[(size_t)slot * p.R + n] = i1;
+    }
+  }
+
+  __syncthreads();
+  // Both CTAs finish here together: every remote arrival has landed and the even CTA's MMAs have
+  // completed before either releases shared or tensor memory.  (After a timeout the copies still in
+  // flight land within the bounded waits of the peer's producer or issuer.)
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, C::kTmemCols);
 }
 
 // ---- fp32 path ------------------------------------------------------------------------------
@@ -668,8 +822,18 @@ static cudaError_t launch_lm_rows(const CUtensorMap* tmW, const CUtensorMap* tmH
   return cudaGetLastError();
 }
 
+static cudaError_t launch_lm_pair(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p,
+                                  cudaStream_t stream) {
+  const int smem = LmPairCfg::kSmem;
+  cudaError_t err = cudaFuncSetAttribute(lmhead_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  lmhead_tc_pair_kernel<<<2 * p.cpc * p.n_nc, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lmhead_bf16(const CUtensorMap* tmW, const CUtensorMap* tmH, const LmParams& p, int num_sms,
                                cudaStream_t stream) {
+  if (p.pair) return launch_lm_pair(tmW, tmH, p, stream);
   switch (p.BN) {
     case 32: return launch_lm<32>(tmW, tmH, p, num_sms, stream);
     case 64: return launch_lm<64>(tmW, tmH, p, num_sms, stream);
