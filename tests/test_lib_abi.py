@@ -164,20 +164,26 @@ def test_workspace_queries_are_host_only(L):
 
 
 def test_attention_split_plan_from_the_workspace_query(L):
-    """The key-split count shows in the workspace (fp32 partials per split).  A batch of 32
+    """The key-split count shows in the workspace (bf16 partials per split).  A batch of 32
     4096-token prefixes (256 CTAs of 65 key tiles fill more than one round of SMs) runs one split
     per KV head; a single 2048-token request is cut into 4-tile splits so that its 16 row groups
-    reach every SM."""
+    reach every SM.  Batches of 8 or 16 such prefixes stay unsplit too: one round that leaves
+    SMs idle beats two filled rounds plus the merge by more than 15 %.  Eight 8192-token
+    capacities with 127-node trees take three splits: the filling grid is preferred, since
+    requests shorter than the capacity make it cheaper than estimated."""
     fake = ctypes.c_void_p(1 << 20)
 
-    def splits(B, L_cap):
-        a = st.AttnArgs(dtype=1, batch=B, n_max=63, num_q_heads=32, num_kv_heads=8, head_dim=128,
+    def splits(B, L_cap, N=63):
+        a = st.AttnArgs(dtype=1, batch=B, n_max=N, num_q_heads=32, num_kv_heads=8, head_dim=128,
                         kv_capacity=L_cap, q=fake, k_cache=fake, v_cache=fake, prefix_len=fake,
                         n_nodes=fake, parent=fake, out=fake)
-        rows = B * 63 * 32
+        rows = B * N * 32
         ws = L.spec_tree_attention_workspace(ctypes.byref(a))
         return ws // (rows * (128 * 2 + 8))  # bf16 partial rows + (max, sum); everything else is far smaller
 
     assert splits(32, 4096 + 63) == 1
     assert splits(1, 2048 + 63) == 9
+    assert splits(16, 4096 + 63) == 1
+    assert splits(8, 4096 + 63) == 1
+    assert splits(8, 8192 + 127, N=127) == 3
 

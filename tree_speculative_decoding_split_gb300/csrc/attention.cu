@@ -159,13 +159,16 @@ AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_s
   pl.n_rg = (N * G + rows_cta - 1) / rows_cta;
   const long long base = (long long)B * Hkv * pl.n_rg;
   // Key splits.  A CTA costs about kFixedTiles key tiles of fixed work (tree checks, prologue,
-  // epilogue) plus its key tiles, and the CTAs run one per SM in rounds; prefix lengths are only
-  // known on the device, so the estimate takes every request at L_cap.  Among chunks of 4 or
-  // more key tiles (at most 16K keys, at most 31 splits) take the one with the smallest
-  // estimated time, preferring grids that fill at least one round.  When that fills at most two
-  // rounds, take the most splits (up to twice as many) whose estimate is within 10 %: with few
-  // rounds, requests shorter than L_cap would leave SMs idle unless the work is cut finer.
-  constexpr long long kFixedTiles = 7;
+  // epilogue) plus its key tiles, and the CTAs run one per SM in rounds; more than one split adds
+  // the merge kernel, about kMergeTiles.  Prefix lengths are only known on the device, so the
+  // estimate takes every request at L_cap.  Among chunks of 4 or more key tiles (at most 16K
+  // keys, at most 31 splits) take the one with the smallest estimated time, preferring grids that
+  // fill at least one round; a grid that leaves SMs idle in its only round wins only when its
+  // estimate is lower by more than 15 % (requests shorter than L_cap shrink the filling grids'
+  // real time, not its).  When the pick takes at most two rounds, take the most splits (up to
+  // twice as many) whose estimate is within 10 %: with few rounds, requests shorter than L_cap
+  // would leave SMs idle unless the work is cut finer.
+  constexpr long long kFixedTiles = 7, kMergeTiles = 4;
   struct Cand {
     long long chunk, np, cost, rounds;
     bool fills;
@@ -180,7 +183,8 @@ AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_s
     const long long np = (L_cap + chunk - 1) / chunk;
     const long long ctas = base * np;
     const long long rounds = (ctas + num_sms - 1) / num_sms;
-    const Cand c = {chunk, np, rounds * (kFixedTiles + chunk / kKT), rounds, ctas >= num_sms};
+    const Cand c = {chunk, np, rounds * (kFixedTiles + chunk / kKT) + (np > 1 ? kMergeTiles : 0), rounds,
+                    ctas >= num_sms};
     if (nc > 0 && cand[nc - 1].np == np)
       cand[nc - 1] = c;  // same split count with a smaller chunk
     else
@@ -188,11 +192,12 @@ AttnPlan plan_attention(int B, int N, int G, int Hkv, long long L_cap, int num_s
   }
   long long best_chunk = -1, best_np = 0;
   if (nc > 0) {
-    int bi = 0;
-    for (int i = 1; i < nc; ++i)
-      if ((cand[i].fills && !cand[bi].fills) ||
-          (cand[i].fills == cand[bi].fills && cand[i].cost < cand[bi].cost))
-        bi = i;
+    int bf = -1, bn = -1;  // cheapest filling grid, cheapest other grid
+    for (int i = 0; i < nc; ++i) {
+      int& bx = cand[i].fills ? bf : bn;
+      if (bx < 0 || cand[i].cost < cand[bx].cost) bx = i;
+    }
+    const int bi = (bf < 0 || (bn >= 0 && cand[bn].cost * 115 < cand[bf].cost * 100)) ? bn : bf;
     int pick = bi;
     if (cand[bi].rounds <= 2)
       for (int i = 0; i < nc; ++i)

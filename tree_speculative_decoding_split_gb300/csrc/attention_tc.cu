@@ -144,6 +144,110 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   const int rows_total = p.N * p.G;
   const int row0 = rg * kRowsCta;
 
+  // Split s covers keys [s * chunk, (s + 1) * chunk); the split holding key L (the first tree
+  // slot) also takes every tree key, [L, L + n), and the splits after it have none.  (A request
+  // that fails the checks below gets a range too; its CTAs only wait for their loads and leave.)
+  const int n_keys = (n < 1 || n > p.N) ? 0 : n;
+  const int s_tree = (int)(L / p.chunk) < p.n_split - 1 ? (int)(L / p.chunk) : p.n_split - 1;
+  const bool tail = (split == s_tree);   // this CTA's keys include the tree
+  const long long kb = (long long)split * p.chunk;
+  const long long ke = split < s_tree ? kb + p.chunk : (tail ? L + n_keys : kb);
+  // Paged KV: tiles start on 64-key boundaries of the logical slots (so that a tile never
+  // straddles a block of >= 64 slots, and a block of fewer slots fills whole 16-row groups of
+  // the swizzled tile); keys below kb are masked.  Contiguous: tiles start at kb.
+  const bool paged = p.table != nullptr;
+  const long long t0 = paged ? (kb & ~(long long)(kKT - 1)) : kb;
+  const int T = ke > kb ? (int)((ke - t0 + kKT - 1) / kKT) : 0;
+  // paged: this CTA's block-table entries (-1 beyond the table), staged for the producer below
+  const int blk0 = paged ? (int)(t0 >> p.bs_shift) : 0;
+  const int nblk = paged ? (int)(((t0 + (long long)T * kKT - 1) >> p.bs_shift) - blk0 + 1) : 0;
+  const bool tbl_staged = nblk <= kMaxBlkCta;
+
+  // K/V tile t of this split -> ring stage t % kStages (the caller has made that stage free)
+  auto issue_tile = [&](int t) {
+    const int st = t % kStages;
+    const long long key = t0 + (long long)t * kKT;
+    mbar_arrive_expect_tx(&full[st], 2 * C::kTile);
+    if (!paged) {
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128, &tmK, &full[st], c * 64, (int)key, bg);
+        tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128, &tmV, &full[st], c * 64, (int)key, bg);
+      }
+    } else {
+      // boxes of min(bs, 64) rows; a slot beyond the table, or an entry out of range, reads
+      // from outside the pool map (zero fill)
+      const int rows = p.bs < kKT ? p.bs : kKT;
+      const long long zlim = (long long)p.num_blocks * p.Hkv;
+      for (int i = 0; i < kKT / rows; ++i) {
+        const long long pos = key + (long long)i * rows;
+        int y = 0, z = (int)zlim;
+        if (pos < p.L_cap) {
+          const int lb = (int)(pos >> p.bs_shift);
+          const int blk = tbl_staged ? s_blk[lb - blk0] : p.table[(size_t)b * p.max_blocks + lb];
+          const long long zz = (long long)blk * p.Hkv + g;
+          if (blk >= 0 && zz < zlim) {
+            y = (int)(pos & (p.bs - 1));
+            z = (int)zz;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmK, &full[st], c * 64, y, z);
+          tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmV, &full[st], c * 64, y, z);
+        }
+      }
+    }
+  };
+  // Q (TMA path) and the first kStages K/V tiles (every stage starts free).  Contiguous caches
+  // send them before the tree checks and the ancestor bits, which then overlap the loads; paged
+  // pools send them once the block-table entries are staged.
+  const int pre = T < kStages ? T : kStages;
+  auto issue_first = [&]() {
+    if (T == 0) return;
+    if (p.q_tma) {
+      // box (64 dims, G heads, 128 / G nodes) = 128 rows (node, head) in row order, swizzled
+      // like the MMA's A operand; rows past the last node read as zeros
+      mbar_arrive_expect_tx(qfull, kGroups * C::kQ);
+      const int npg = kGR / p.G;  // nodes per group
+#pragma unroll
+      for (int a = 0; a < kGroups; ++a)
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d_plain(sQ + a * C::kQ + c * kGR * 128, &tmQ, qfull, c * 64, g * p.G, (row0 / p.G) + a * npg, b);
+    }
+    for (int t = 0; t < pre; ++t) issue_tile(t);
+    s_issued = pre;
+  };
+  const bool early = !paged;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kGroups);  // one P V commit per group's issuer
+    }
+    for (int a = 0; a < kGroups; ++a) {
+      mbar_init(&sfull[a], 1);
+      mbar_init(&sfree[a], 4);
+      mbar_init(&pfull[2 * a], 4);
+      mbar_init(&pfull[2 * a + 1], 4);
+      mbar_init(&ofull[2 * a], 1);
+      mbar_init(&ofull[2 * a + 1], 1);
+    }
+    for (int a = 0; a < kGroups; ++a) mbar_init(&drained[a], 1);
+    mbar_init(qfull, 1);
+    s_abort = 0;
+    s_issued = 0;
+    s_consumed = 0;
+    fence_mbar_init();
+    if (early) issue_first();
+  }
+  // a CTA that leaves before its tile loop lets its early loads land first (tid 0 issued them)
+  auto drain_first = [&]() {
+    if (tid != 0 || !early || T == 0) return;
+    for (int u = 0; u < s_issued; ++u) mbar_wait_bounded(&full[u], 0, nullptr);
+    if (p.q_tma) mbar_wait_bounded(qfull, 0, nullptr);
+  };
+
   // ---- tree checks, done by every CTA of the request (same verdict everywhere) ----
   int bad_tree = (n < 1 || n > p.N) ? 1 : 0, bad_cap = 0;
   if (!bad_tree) {
@@ -173,19 +277,9 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   if (err) {  // the merge kernel (or, with one split, this CTA) zeroes this request's outputs
     if (tid == 0 && rg == 0 && split == 0 && g == 0) set_status(p.dev_status, err);
     if (p.direct) zero_rows();
+    drain_first();
     return;
   }
-  // Split s covers keys [s * chunk, (s + 1) * chunk); the split holding key L (the first tree
-  // slot) also takes every tree key, [L, L + n), and the splits after it have none.
-  const int s_tree = (int)(L / p.chunk) < p.n_split - 1 ? (int)(L / p.chunk) : p.n_split - 1;
-  const bool tail = (split == s_tree);   // this CTA's keys include the tree
-  const long long kb = (long long)split * p.chunk;
-  const long long ke = split < s_tree ? kb + p.chunk : (tail ? L + n : kb);
-  // Paged KV: tiles start on 64-key boundaries of the logical slots (so that a tile never
-  // straddles a block of >= 64 slots, and a block of fewer slots fills whole 16-row groups of
-  // the swizzled tile); keys below kb are masked.  Contiguous: tiles start at kb.
-  const bool paged = p.table != nullptr;
-  const long long t0 = paged ? (kb & ~(long long)(kKT - 1)) : kb;
   if (paged && tail) {  // every tree-split CTA of the request checks its whole table (same verdict)
     const long long used = (L + n + p.bs - 1) >> p.bs_shift;
     int badt = 0;
@@ -203,7 +297,6 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       return;
     }
   }
-  const int T = ke > kb ? (int)((ke - t0 + kKT - 1) / kKT) : 0;
   if (T == 0) {  // no keys here: the merge skips this split
     if (p.direct) {
       zero_rows();
@@ -267,35 +360,11 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       sAnc[c] = word;
     }
   }
-  // paged: this CTA's block-table entries (-1 beyond the table), staged for the producer
-  const int blk0 = paged ? (int)(t0 >> p.bs_shift) : 0;
-  const int nblk = paged ? (int)(((t0 + (long long)T * kKT - 1) >> p.bs_shift) - blk0 + 1) : 0;
-  const bool tbl_staged = nblk <= kMaxBlkCta;
   if (paged && tbl_staged)
     for (int j = tid; j < nblk; j += kTcThreads) {
       const int lb = blk0 + j;
       s_blk[j] = lb < p.max_blocks ? p.table[(size_t)b * p.max_blocks + lb] : -1;
     }
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kGroups);  // one P V commit per group's issuer
-    }
-    for (int a = 0; a < kGroups; ++a) {
-      mbar_init(&sfull[a], 1);
-      mbar_init(&sfree[a], 4);
-      mbar_init(&pfull[2 * a], 4);
-      mbar_init(&pfull[2 * a + 1], 4);
-      mbar_init(&ofull[2 * a], 1);
-      mbar_init(&ofull[2 * a + 1], 1);
-    }
-    for (int a = 0; a < kGroups; ++a) mbar_init(&drained[a], 1);
-    mbar_init(qfull, 1);
-    s_abort = 0;
-    s_issued = 0;
-    s_consumed = 0;
-    fence_mbar_init();
-  }
   if (warp == 1) {
     tmem_alloc(&s_tmem, C::kTmemCols);
     tmem_relinquish();
@@ -304,59 +373,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   __syncthreads();  // barriers initialised, block-table entries staged
   tc_fence_after();
 
-  // K/V tile t of this split -> ring stage t % kStages (the caller has made that stage free)
-  auto issue_tile = [&](int t) {
-    const int st = t % kStages;
-    const long long key = t0 + (long long)t * kKT;
-    mbar_arrive_expect_tx(&full[st], 2 * C::kTile);
-    if (!paged) {
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128, &tmK, &full[st], c * 64, (int)key, bg);
-        tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128, &tmV, &full[st], c * 64, (int)key, bg);
-      }
-    } else {
-      // boxes of min(bs, 64) rows; a slot beyond the table, or an entry out of range, reads
-      // from outside the pool map (zero fill)
-      const int rows = p.bs < kKT ? p.bs : kKT;
-      const long long zlim = (long long)p.num_blocks * p.Hkv;
-      for (int i = 0; i < kKT / rows; ++i) {
-        const long long pos = key + (long long)i * rows;
-        int y = 0, z = (int)zlim;
-        if (pos < p.L_cap) {
-          const int lb = (int)(pos >> p.bs_shift);
-          const int blk = tbl_staged ? s_blk[lb - blk0] : p.table[(size_t)b * p.max_blocks + lb];
-          const long long zz = (long long)blk * p.Hkv + g;
-          if (blk >= 0 && zz < zlim) {
-            y = (int)(pos & (p.bs - 1));
-            z = (int)zz;
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmK, &full[st], c * 64, y, z);
-          tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmV, &full[st], c * 64, y, z);
-        }
-      }
-    }
-  };
-  // Q (TMA path) and the first kStages K/V tiles go out now (every stage starts free).
-  const int pre = T < kStages ? T : kStages;
-  if (warp == 0 && lane == 0) {
-    if (p.q_tma) {
-      // box (64 dims, G heads, 128 / G nodes) = 128 rows (node, head) in row order, swizzled
-      // like the MMA's A operand; rows past the last node read as zeros
-      mbar_arrive_expect_tx(qfull, kGroups * C::kQ);
-      const int npg = kGR / p.G;  // nodes per group
-#pragma unroll
-      for (int a = 0; a < kGroups; ++a)
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d_plain(sQ + a * C::kQ + c * kGR * 128, &tmQ, qfull, c * 64, g * p.G, (row0 / p.G) + a * npg, b);
-    }
-    for (int t = 0; t < pre; ++t) issue_tile(t);
-    s_issued = pre;
-  }
+  if (!early && warp == 0 && lane == 0) issue_first();
 
   if (!p.q_tma) {
     // ---- Q rows -> shared memory in the K-major 128-byte-swizzle layout of the MMA A operand ----
