@@ -48,6 +48,7 @@ KERNEL_SOURCES = {
     "attn_merge_bf16_kernel": ["attention.cu", "common.cuh"],
     "lmhead_tc_kernel": ["lmhead.cu", "tc_ptx.cuh", "common.cuh"],
     "lmhead_tc_rows_kernel": ["lmhead.cu", "tc_ptx.cuh", "common.cuh"],
+    "lmhead_tc_pair_kernel": ["lmhead.cu", "tc_ptx.cuh", "common.cuh"],
     "compact_kv_kernel": ["compact.cu", "compact.cuh", "common.cuh"],
 }
 
@@ -447,7 +448,10 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
     hbm, tc, tc_sus, peak_kind = _peaks()
     lm_med = statistics.median(lm_ms)
     attn_med = statistics.median(attn_ms)
-    lm_kernel = "lmhead_tc_rows_kernel" if case.B * case.N > 64 else "lmhead_tc_kernel"
+    # the LM-head kernel the library picks for this many tree rows (bf16): vocabulary on M up to
+    # 64 rows, rows on M up to 128, CTA pairs above
+    R = case.B * case.N
+    lm_kernel = "lmhead_tc_pair_kernel" if R > 128 else ("lmhead_tc_rows_kernel" if R > 64 else "lmhead_tc_kernel")
     rf_attn = _roofline("attn_sk_kernel" if stream_k else "attn_tc_kernel", w["attn_flops"], w["attn_kernel_bytes"], attn_med, hbm, tc, peak_kind,
                         case.name)
     rf_lm = _roofline(lm_kernel, w["lm_flops"], w["lm_kernel_bytes"], lm_med, hbm, tc, peak_kind, case.name)
