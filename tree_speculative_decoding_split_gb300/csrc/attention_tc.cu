@@ -163,14 +163,16 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   const int nblk = paged ? (int)(((t0 + (long long)T * kKT - 1) >> p.bs_shift) - blk0 + 1) : 0;
   const bool tbl_staged = nblk <= kMaxBlkCta;
 
-  // K/V tile t of this split -> ring stage t % kStages (the caller has made that stage free)
-  auto issue_tile = [&](int t) {
+  // K/V tile t of this split -> ring stage t % kStages (the caller has made that stage free and
+  // armed the stage's barrier for 2 * kTile bytes): the loads that lane `ln` of `nl` cooperating
+  // lanes issues -- a d-chunk of a contiguous tile, or a box of a paged one with its block-table
+  // lookup (one thread issuing a paged tile's 16 copies and 4 lookups in turn was the slowest step
+  // of the loop with blocks of 16 slots; one lane per copy was no faster than one per box)
+  auto tile_loads = [&](int t, int ln, int nl) {
     const int st = t % kStages;
     const long long key = t0 + (long long)t * kKT;
-    mbar_arrive_expect_tx(&full[st], 2 * C::kTile);
     if (!paged) {
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
+      for (int c = ln; c < D / 64; c += nl) {
         tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128, &tmK, &full[st], c * 64, (int)key, bg);
         tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128, &tmV, &full[st], c * 64, (int)key, bg);
       }
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       // from outside the pool map (zero fill)
       const int rows = p.bs < kKT ? p.bs : kKT;
       const long long zlim = (long long)p.num_blocks * p.Hkv;
-      for (int i = 0; i < kKT / rows; ++i) {
+      for (int i = ln; i < kKT / rows; i += nl) {
         const long long pos = key + (long long)i * rows;
         int y = 0, z = (int)zlim;
         if (pos < p.L_cap) {
@@ -198,6 +200,11 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         }
       }
     }
+  };
+  // one thread: arm the stage's barrier, then every load of the tile
+  auto issue_tile = [&](int t) {
+    mbar_arrive_expect_tx(&full[t % kStages], 2 * C::kTile);
+    tile_loads(t, 0, 1);
   };
   // Q (TMA path) and the first kStages K/V tiles (every stage starts free).  Contiguous caches
   // send them before the tree checks and the ancestor bits, which then overlap the loads; paged
@@ -408,22 +415,25 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---- TMA producer (tiles pre .. T-1) ----
-      bool ok = true;
-      for (int t = pre; t < T && ok; ++t) {
-        const int st = t % kStages;
-        if (!mbar_wait_bounded(&empty[st], ((t / kStages) & 1) ^ 1, &s_abort)) {
-          ok = false;
-          break;
-        }
-        issue_tile(t);
-        s_issued = t + 1;
+    // ---- TMA producer (tiles pre .. T-1): lane 0 waits for the stage and arms its barrier, then
+    // the warp's lanes issue the tile's loads side by side ----
+    bool ok = true;
+    for (int t = pre; t < T; ++t) {
+      const int st = t % kStages;
+      const bool got = lane == 0 ? mbar_wait_bounded(&empty[st], ((t / kStages) & 1) ^ 1, &s_abort) : true;
+      if (!__shfl_sync(0xffffffffu, got, 0)) {
+        ok = false;
+        break;
       }
-      if (!ok) {
-        s_abort = 1;
-        set_status(p.dev_status, SPEC_ERR_TIMEOUT);
-      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], 2 * C::kTile);
+      __syncwarp();
+      tile_loads(t, lane, 32);
+      __syncwarp();
+      if (lane == 0) s_issued = t + 1;
+    }
+    if (!ok && lane == 0) {
+      s_abort = 1;
+      set_status(p.dev_status, SPEC_ERR_TIMEOUT);
     }
   } else if (warp == 1 || warp >= 2 + 4 * kGroups) {
     // ---- MMA issuers: group 0 on warp 1, group g > 0 on warp 1 + 4 * kGroups + g ----
