@@ -575,11 +575,10 @@ def medusa_expand(head_logits, topo_parent, topo_rank, topk, root_token=None, wo
     return outputs
 
 
-def eagle_expand(logp, frontier_score, topk, next_k, frontier_valid=None, frontier_cand=None, outputs=None,
-                 cand_stride=0, workspace=None, dev_status=None, stream=None):
-    """One layer of the dynamic draft tree (spec_eagle_expand).  logp float32 [B][F][Vd];
-    frontier_score float32 [B][F].  ``outputs`` may pass views into stacked [B][layers][C]
-    buffers together with ``cand_stride``.  Returns a dict of tensors."""
+def eagle_expand_args(logp, frontier_score, topk, next_k, frontier_valid=None, frontier_cand=None, outputs=None,
+                      cand_stride=0):
+    """Build the C argument struct for eagle_expand (tensors are validated here); returns
+    (args, outputs dict)."""
     torch = _torch()
     _need(logp, "logp", torch.float32)
     dev = logp.device
@@ -601,6 +600,17 @@ def eagle_expand(logp, frontier_score, topk, next_k, frontier_valid=None, fronti
                         cand_token=_vp(outputs["token"].data_ptr()), cand_score=_vp(outputs["score"].data_ptr()),
                         cand_parent=_vp(outputs["parent"].data_ptr()), next_index=_ptr(outputs["next_index"]),
                         next_score=_ptr(outputs["next_score"]))
+    return a, outputs
+
+
+def eagle_expand(logp, frontier_score, topk, next_k, frontier_valid=None, frontier_cand=None, outputs=None,
+                 cand_stride=0, workspace=None, dev_status=None, stream=None):
+    """One layer of the dynamic draft tree (spec_eagle_expand).  logp float32 [B][F][Vd];
+    frontier_score float32 [B][F].  ``outputs`` may pass views into stacked [B][layers][C]
+    buffers together with ``cand_stride``.  Returns a dict of tensors."""
+    a, outputs = eagle_expand_args(logp, frontier_score, topk, next_k, frontier_valid, frontier_cand, outputs,
+                                   cand_stride)
+    dev = logp.device
     L = lib()
     need = L.spec_eagle_expand_workspace(ctypes.byref(a))
     if need == 0:
@@ -611,9 +621,9 @@ def eagle_expand(logp, frontier_score, topk, next_k, frontier_valid=None, fronti
     return outputs
 
 
-def eagle_tree(score, token, parent, n_max, draft_to_target=None, root_token=None, dev_status=None, stream=None):
-    """The draft tree from stacked candidates [B][layers][C] (spec_eagle_tree).  Returns a dict:
-    parent [B][N], tokens [B][N], n_nodes [B], node_cand [B][N]."""
+def eagle_tree_args(score, token, parent, n_max, draft_to_target=None, root_token=None):
+    """Build the C argument struct for eagle_tree (tensors are validated here); returns (args,
+    outputs dict)."""
     torch = _torch()
     _need(score, "score", torch.float32)
     dev = score.device
@@ -635,6 +645,14 @@ def eagle_tree(score, token, parent, n_max, draft_to_target=None, root_token=Non
                       token=_ptr(token), parent=_ptr(parent), draft_to_target=_ptr(draft_to_target),
                       root_token=_ptr(root_token), tree_parent=_ptr(out["parent"]), tree_token=_ptr(out["tokens"]),
                       n_nodes=_ptr(out["n_nodes"]), node_cand=_ptr(out["node_cand"]))
+    return a, out
+
+
+def eagle_tree(score, token, parent, n_max, draft_to_target=None, root_token=None, dev_status=None, stream=None):
+    """The draft tree from stacked candidates [B][layers][C] (spec_eagle_tree).  Returns a dict:
+    parent [B][N], tokens [B][N], n_nodes [B], node_cand [B][N]."""
+    a, out = eagle_tree_args(score, token, parent, n_max, draft_to_target, root_token)
+    dev = score.device
     st = _status_buffer(dev_status, dev)
     _check(lib().spec_eagle_tree(ctypes.byref(a), _ptr(st), _stream(stream)), "spec_eagle_tree")
     return out

@@ -4,10 +4,11 @@
 // 2's top-2 = 18 paths) along a predefined topology ("Medusa Tree", 63 / 127 / 255 nodes).  A
 // node at depth d >= 1 with rank r carries the r-th best token of head d - 1.
 //
-// K5a: per (request, head, vocabulary chunk) top-k by k rounds of block-wide argmax over 64-bit
-// order keys (value, then the lower token id) held in registers.  K5b: per request, the chunk
-// candidates of every head merge into the head's top-k, the topology is validated and every
-// node's token is looked up.
+// K5a: per (request, head, vocabulary chunk) top-k over 64-bit order keys (value, then the lower
+// token id) held in registers: every warp takes its own top-k by k rounds of a warp-wide maximum
+// below the previous winner, then one warp merges the warps' candidates the same way.  K5b: per request, the chunk
+// candidates of every head merge into the head's top-k (one warp per head, the heads side by
+// side), the topology is validated and every node's token is looked up.
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -45,19 +46,12 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long x)
   return x;
 }
 
-// Largest key below `below` over the block (0 when there is none); every thread gets it.
-__device__ __forceinline__ unsigned long long block_max_below(const unsigned long long* keys, int n,
-                                                              unsigned long long below,
-                                                              unsigned long long* s_red) {
+// Largest of `n` keys below `below` over the warp (0 when there is none); every lane gets it.
+__device__ __forceinline__ unsigned long long warp_max_below(const unsigned long long* keys, int n,
+                                                             unsigned long long below) {
   unsigned long long m = 0ull;
   for (int e = 0; e < n; ++e)
     if (keys[e] < below && keys[e] > m) m = keys[e];
-  m = warp_max_u64(m);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) s_red[warp] = m;
-  __syncthreads();
-  m = (lane < (int)(blockDim.x >> 5)) ? s_red[lane] : 0ull;
   return warp_max_u64(m);
 }
 
@@ -65,7 +59,8 @@ __device__ __forceinline__ unsigned long long block_max_below(const unsigned lon
 
 // K5a: grid (n_chunks, B * K).  Writes k keys per (row, chunk), best first (0 = none).
 __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const MedusaParams p) {
-  __shared__ unsigned long long s_red[kMxThreads / 32];
+  constexpr int kWarps = kMxThreads / 32;
+  __shared__ unsigned long long s_cand[kWarps * kMaxTopk];  // [warp][rank]
   const int chunk = blockIdx.x, row = blockIdx.y;  // row = b * K + head
   const int v0 = chunk * p.chunk;
   const int v1 = min(p.V, v0 + p.chunk);
@@ -83,17 +78,32 @@ __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const Med
     }
     keys[e] = in ? topk_key(f, v) : 0ull;
   }
-  unsigned long long* out = p.cand + ((size_t)row * p.n_chunks + chunk) * p.k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned long long below = ~0ull;
-  for (int r = 0; r < p.k; ++r) {
-    below = block_max_below(keys, kMxEpt, below, s_red);
-    if (threadIdx.x == 0) out[r] = below;  // 0 once the chunk is exhausted
+  for (int r = 0; r < p.k; ++r) {  // this warp's top-k
+    below = warp_max_below(keys, kMxEpt, below);
+    if (lane == 0) s_cand[warp * kMaxTopk + r] = below;  // 0 once the warp's keys are exhausted
+  }
+  __syncthreads();
+  if (warp == 0) {  // the chunk's top-k among the warps' candidates (kWarps * k <= 256)
+    constexpr int kPer = kWarps * kMaxTopk / 32;
+    unsigned long long c[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int j = lane + 32 * e, w = j / kMaxTopk, r = j % kMaxTopk;
+      c[e] = (r < p.k) ? s_cand[w * kMaxTopk + r] : 0ull;
+    }
+    unsigned long long* out = p.cand + ((size_t)row * p.n_chunks + chunk) * p.k;
+    below = ~0ull;
+    for (int r = 0; r < p.k; ++r) {
+      below = warp_max_below(c, kPer, below);
+      if (lane == 0) out[r] = below;  // 0 once the chunk is exhausted
+    }
   }
 }
 
 // K5b: one CTA per request.
-__global__ void __launch_bounds__(kMxThreads) medusa_expand_kernel(const MedusaParams p) {
-  __shared__ unsigned long long s_red[kMxThreads / 32];
+__global__ void __launch_bounds__(kMxThreads, 1) medusa_expand_kernel(const MedusaParams p) {
   __shared__ int s_top[kMaxHeads * kMaxTopk];
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_depth[kMaxNodes];
@@ -122,21 +132,22 @@ __global__ void __launch_bounds__(kMxThreads) medusa_expand_kernel(const MedusaP
     }
   }
   bad = __syncthreads_or(bad);
-  // every head's top-k from the chunk candidates (k rounds of block argmax each)
+  // every head's top-k from its chunk candidates: one warp per head, k rounds of a warp-wide
+  // maximum below the previous winner (the candidates are re-read from L1 each round), so the
+  // heads proceed side by side with no block barrier
   const int nc = p.n_chunks * p.k;
-  for (int h = 0; h < p.K; ++h) {
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int h = warp; h < p.K; h += kMxThreads / 32) {
     const unsigned long long* c = p.cand + (size_t)(b * p.K + h) * nc;
-    constexpr int kPer = kMedusaMergeCands / kMxThreads;
-    unsigned long long keys[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int j = tid + e * kMxThreads;
-      keys[e] = (j < nc) ? c[j] : 0ull;
-    }
     unsigned long long below = ~0ull;
     for (int r = 0; r < p.k; ++r) {
-      below = block_max_below(keys, kPer, below, s_red);
-      if (tid == 0) {
+      unsigned long long m = 0ull;
+      for (int j = lane; j < nc; j += 32) {
+        const unsigned long long x = c[j];
+        if (x < below && x > m) m = x;
+      }
+      below = warp_max_u64(m);
+      if (lane == 0) {
         const int tok = below ? key_token(below) : -1;
         s_top[h * kMaxTopk + r] = tok;
         if (p.topk_index) p.topk_index[((size_t)b * p.K + h) * p.k + r] = tok;
