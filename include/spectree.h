@@ -416,11 +416,16 @@ spec_status spec_eagle_tree(const spec_eagle_tree_args* args, int32_t* dev_statu
  * prefix -- not how they are launched.  At batch 1 the round is a handful of short kernels
  * around the LM head, so per-call host work and launch gaps are a visible share of it.)
  *
- * spec_round_create captures, in this order, spec_tree_attention(attn, attn_workspace),
- * spec_verify_accept(verify, verify_workspace) and spec_compact_kv(compact) into a CUDA graph
- * and instantiates it; when `compact` names the verification's outputs (same path, accept_len,
- * path_cap and batch) the last two are captured as spec_verify_accept_compact.  Any of the three
- * may be NULL to leave that call out; at least one must be given.
+ * spec_round_create captures spec_tree_attention(attn, attn_workspace), spec_verify_accept(verify,
+ * verify_workspace) and spec_compact_kv(compact) into a CUDA graph and instantiates it.  With
+ * both `attn` and `verify` given, the two run as parallel branches of the graph (they read
+ * disjoint inputs; the LM head then overlaps the attention's split merge and its last CTAs) and
+ * the compaction follows both, since it rewrites K/V rows the attention reads.  Without `attn`,
+ * a `compact` that names the verification's outputs (same path, accept_len, path_cap and batch)
+ * is captured with it as spec_verify_accept_compact.  Any of the three may be NULL to leave that
+ * call out; at least one must be given.  Because of the branches, `attn` and `verify` must not
+ * share output or workspace buffers, and the attention's out / lse must not alias the
+ * verification's inputs.
  *   - Everything in the argument structs is frozen at creation: device pointers, shapes,
  *     scalars (rule, temperature, eps, delta, seed), dev_status and the optional timing events.
  *     The CONTENTS of the device buffers are read when the round runs, so a serving loop refills

@@ -25,26 +25,53 @@ extern "C" spec_status spec_round_create(const spec_attn_args* attn, void* attn_
   // lazily initialised launch state is set up outside the capture
   if (verify && verify->rule == SPEC_RULE_REJECTION) spectree::prepare_rejection_launch();
 
-  cudaStream_t s = nullptr;
-  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return SPEC_ERR_CUDA;
+  // Tree attention and the verification read disjoint inputs, so with both present they are
+  // captured as parallel branches (a second stream forked from and joined back into the capture):
+  // the LM head then runs beside the split merge and fills SMs as the attention's last CTAs
+  // drain.  The compaction rewrites K/V rows the attention reads, so it follows both branches and
+  // is folded into the acceptance kernels only when the round has no attention call.
+  const bool branch = attn && verify;
+  cudaStream_t s = nullptr, s2 = nullptr;
+  cudaEvent_t e_fork = nullptr, e_join = nullptr;
+  auto release = [&]() {
+    if (s) cudaStreamDestroy(s);
+    if (s2) cudaStreamDestroy(s2);
+    if (e_fork) cudaEventDestroy(e_fork);
+    if (e_join) cudaEventDestroy(e_join);
+  };
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
+      (branch && (cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking) != cudaSuccess ||
+                  cudaEventCreateWithFlags(&e_fork, cudaEventDisableTiming) != cudaSuccess ||
+                  cudaEventCreateWithFlags(&e_join, cudaEventDisableTiming) != cudaSuccess))) {
+    release();
+    cudaGetLastError();
+    return SPEC_ERR_CUDA;
+  }
   if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
-    cudaStreamDestroy(s);
+    release();
     cudaGetLastError();
     return SPEC_ERR_CUDA;
   }
   spec_status st = SPEC_OK;
-  if (attn) st = spec_tree_attention(attn, attn_workspace, attn_workspace_bytes, dev_status, s);
+  if (branch && (cudaEventRecord(e_fork, s) != cudaSuccess || cudaStreamWaitEvent(s2, e_fork, 0) != cudaSuccess))
+    st = SPEC_ERR_CUDA;
+  if (st == SPEC_OK && attn) st = spec_tree_attention(attn, attn_workspace, attn_workspace_bytes, dev_status, s);
   // a compaction of the verification's own outputs is folded into the acceptance kernels
-  const bool fuse = verify && compact && compact->path == verify->path && compact->accept_len == verify->accept_len &&
-                    compact->path_cap == verify->path_cap && compact->batch == verify->batch;
+  const bool fuse = !branch && verify && compact && compact->path == verify->path &&
+                    compact->accept_len == verify->accept_len && compact->path_cap == verify->path_cap &&
+                    compact->batch == verify->batch;
   if (st == SPEC_OK && fuse)
     st = spec_verify_accept_compact(verify, verify_workspace, verify_workspace_bytes, compact, dev_status, s);
   else if (st == SPEC_OK && verify)
-    st = spec_verify_accept(verify, verify_workspace, verify_workspace_bytes, dev_status, s);
+    st = spec_verify_accept(verify, verify_workspace, verify_workspace_bytes, dev_status, branch ? s2 : s);
+  // the join is captured even after a failure, so that the capture ends cleanly
+  if (branch && (cudaEventRecord(e_join, s2) != cudaSuccess || cudaStreamWaitEvent(s, e_join, 0) != cudaSuccess) &&
+      st == SPEC_OK)
+    st = SPEC_ERR_CUDA;
   if (st == SPEC_OK && compact && !fuse) st = spec_compact_kv(compact, dev_status, s);
   cudaGraph_t graph = nullptr;
   const cudaError_t end = cudaStreamEndCapture(s, &graph);  // always ends the capture
-  cudaStreamDestroy(s);
+  release();
   if (st != SPEC_OK || end != cudaSuccess || !graph) {
     if (graph) cudaGraphDestroy(graph);
     cudaGetLastError();
