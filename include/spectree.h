@@ -453,9 +453,15 @@ spec_status spec_round_launch(const spec_round* round, void* stream);
 void spec_round_destroy(spec_round* round);
 
 /* One round end to end from host memory: the step's inputs are copied in, the round runs, and
- * its results are copied out, all enqueued on `stream` in that order by one call.  (Deployment
- * convenience, like the round itself: the pages describe what a round computes, not where its
- * inputs come from.)
+ * its results are copied out, all enqueued by one call and complete in `stream` order.
+ * (Deployment convenience, like the round itself: the pages describe what a round computes, not
+ * where its inputs come from.)  When the round has both tree attention and verification, a copy
+ * whose destination lies wholly inside a buffer only the verification reads (hidden_states,
+ * tokens, lm_head_weight, draft_probs) goes to a stream of the round's own: it starts after
+ * everything already enqueued on `stream`, carries the verification beside the attention, and
+ * rejoins `stream` before the compaction and the result copies.  Every other input copy, and
+ * every output copy, is on `stream`.  Those verification-only buffers must therefore not overlap
+ * any buffer the attention reads.
  *
  * Each spec_host_copy moves `rows` rows of `row_bytes` bytes; row r starts at
  * host + r * host_pitch and at device + r * device_pitch (pitches are ignored when rows == 1).

@@ -12,7 +12,93 @@
 struct spec_round {
   cudaGraph_t graph;
   cudaGraphExec_t exec;
+  // Host-buffer launches: the three calls also as graphs of their own, so that the copies that
+  // feed only the verification run on `side` beside the attention (null when the round lacks
+  // the attention or the verification, or when they could not be made).
+  cudaGraph_t g_part[3];
+  cudaGraphExec_t x_part[3];  // attention, verification, compaction (or null)
+  cudaStream_t side;
+  cudaEvent_t e_fork, e_join;
+  uintptr_t vonly[4][2];      // [lo, hi) of the buffers only the verification reads
+  int n_vonly;
 };
+
+namespace {
+
+// One call captured into a graph of its own (null exec on failure).
+template <typename F>
+void capture_part(F call, cudaGraph_t* g, cudaGraphExec_t* x) {
+  *g = nullptr;
+  *x = nullptr;
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return;
+  if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+    const spec_status st = call(s);
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamEndCapture(s, &graph) == cudaSuccess && graph && st == SPEC_OK &&
+        cudaGraphInstantiate(x, graph, 0) == cudaSuccess) {
+      *g = graph;
+    } else {
+      if (graph) cudaGraphDestroy(graph);
+      *x = nullptr;
+    }
+  }
+  cudaStreamDestroy(s);
+  cudaGetLastError();
+}
+
+void release_parts(spec_round* r) {
+  for (int i = 0; i < 3; ++i) {
+    if (r->x_part[i]) cudaGraphExecDestroy(r->x_part[i]);
+    if (r->g_part[i]) cudaGraphDestroy(r->g_part[i]);
+    r->x_part[i] = nullptr;
+    r->g_part[i] = nullptr;
+  }
+  if (r->side) cudaStreamDestroy(r->side);
+  if (r->e_fork) cudaEventDestroy(r->e_fork);
+  if (r->e_join) cudaEventDestroy(r->e_join);
+  r->side = nullptr;
+  r->e_fork = r->e_join = nullptr;
+}
+
+// The split launch state for a round with attention and verification; left empty (the host
+// launch then copies everything before the round's graph) if any part cannot be made.
+void make_parts(spec_round* r, const spec_attn_args* attn, void* attn_ws, size_t attn_ws_bytes,
+                const spec_verify_args* verify, void* verify_ws, size_t verify_ws_bytes,
+                const spec_compact_args* compact, int32_t* dev_status) {
+  capture_part([&](cudaStream_t s) { return spec_tree_attention(attn, attn_ws, attn_ws_bytes, dev_status, s); },
+               &r->g_part[0], &r->x_part[0]);
+  capture_part([&](cudaStream_t s) { return spec_verify_accept(verify, verify_ws, verify_ws_bytes, dev_status, s); },
+               &r->g_part[1], &r->x_part[1]);
+  if (compact)
+    capture_part([&](cudaStream_t s) { return spec_compact_kv(compact, dev_status, s); }, &r->g_part[2],
+                 &r->x_part[2]);
+  bool ok = r->x_part[0] && r->x_part[1] && (!compact || r->x_part[2]) &&
+            cudaStreamCreateWithFlags(&r->side, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&r->e_fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&r->e_join, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    release_parts(r);
+    cudaGetLastError();
+    return;
+  }
+  const size_t es = verify->dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  const size_t rows = (size_t)verify->batch * verify->n_max;
+  auto add = [&](const void* p, size_t bytes) {
+    if (!p || !bytes) return;
+    r->vonly[r->n_vonly][0] = reinterpret_cast<uintptr_t>(p);
+    r->vonly[r->n_vonly][1] = reinterpret_cast<uintptr_t>(p) + bytes;
+    ++r->n_vonly;
+  };
+  add(verify->hidden_states, rows * verify->hidden * es);
+  add(verify->tokens, rows * sizeof(int32_t));
+  add(verify->lm_head_weight, (size_t)verify->vocab * verify->hidden * es);
+  if (verify->rule == SPEC_RULE_REJECTION)
+    add(verify->draft_probs, rows * (size_t)(verify->draft_vocab > 0 ? verify->draft_vocab : verify->vocab) *
+                                 sizeof(float));
+}
+
+}  // namespace
 
 extern "C" spec_status spec_round_create(const spec_attn_args* attn, void* attn_workspace,
                                          size_t attn_workspace_bytes, const spec_verify_args* verify,
@@ -83,12 +169,17 @@ extern "C" spec_status spec_round_create(const spec_attn_args* attn, void* attn_
     cudaGetLastError();
     return SPEC_ERR_CUDA;
   }
-  spec_round* r = new (std::nothrow) spec_round{graph, exec};
+  spec_round* r = new (std::nothrow) spec_round{};
   if (!r) {
     cudaGraphExecDestroy(exec);
     cudaGraphDestroy(graph);
     return SPEC_ERR_CUDA;
   }
+  r->graph = graph;
+  r->exec = exec;
+  if (branch)
+    make_parts(r, attn, attn_workspace, attn_workspace_bytes, verify, verify_workspace, verify_workspace_bytes,
+               compact, dev_status);
   *out = r;
   return SPEC_OK;
 }
@@ -132,9 +223,31 @@ extern "C" spec_status spec_round_launch_host(const spec_round* round, const spe
   if (st != SPEC_OK) return st;
   if (!round) return SPEC_ERR_INVALID_ARGUMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  for (int32_t i = 0; i < n_inputs; ++i)
-    if (enqueue_copy(inputs[i], true, s) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (cudaGraphLaunch(round->exec, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (round->x_part[0]) {
+    // Copies into buffers that only the verification reads go on the side stream, which then
+    // runs the verification beside the attention; the compaction and the result copies follow
+    // both.  The side stream starts after everything enqueued on `s` so far (the previous
+    // round included), so no copy overwrites a buffer still being read.
+    auto verify_only = [&](const spec_host_copy& c) {
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(c.device);
+      const uintptr_t hi = lo + (c.rows > 1 ? (size_t)(c.rows - 1) * c.device_pitch : 0) + c.row_bytes;
+      for (int k = 0; k < round->n_vonly; ++k)
+        if (lo >= round->vonly[k][0] && hi <= round->vonly[k][1]) return true;
+      return false;
+    };
+    if (cudaEventRecord(round->e_fork, s) != cudaSuccess || cudaStreamWaitEvent(round->side, round->e_fork, 0) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    for (int32_t i = 0; i < n_inputs; ++i)
+      if (enqueue_copy(inputs[i], true, verify_only(inputs[i]) ? round->side : s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (cudaGraphLaunch(round->x_part[0], s) != cudaSuccess || cudaGraphLaunch(round->x_part[1], round->side) != cudaSuccess ||
+        cudaEventRecord(round->e_join, round->side) != cudaSuccess || cudaStreamWaitEvent(s, round->e_join, 0) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (round->x_part[2] && cudaGraphLaunch(round->x_part[2], s) != cudaSuccess) return SPEC_ERR_CUDA;
+  } else {
+    for (int32_t i = 0; i < n_inputs; ++i)
+      if (enqueue_copy(inputs[i], true, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (cudaGraphLaunch(round->exec, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  }
   for (int32_t i = 0; i < n_outputs; ++i)
     if (enqueue_copy(outputs[i], false, s) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
@@ -142,6 +255,7 @@ extern "C" spec_status spec_round_launch_host(const spec_round* round, const spe
 
 extern "C" void spec_round_destroy(spec_round* round) {
   if (!round) return;
+  release_parts(round);
   cudaGraphExecDestroy(round->exec);
   cudaGraphDestroy(round->graph);
   delete round;
