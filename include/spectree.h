@@ -198,6 +198,10 @@ typedef struct spec_verify_args {
   void* timing_begin;             /* optional cudaEvent_t recorded on `stream` right before the
                                      LM-head kernel; NULL = none */
   void* timing_end;               /* optional cudaEvent_t recorded right after it */
+  void* draft_ready;              /* REJECTION, optional cudaEvent_t: the rejection walk (the only
+                                     reader of draft_probs) waits for it, so the distributions may
+                                     still be arriving while the LM head runs; NULL = none.  Inside
+                                     a stream capture the wait is captured as an external one. */
 } spec_verify_args;
 
 /* Bytes of workspace spec_verify_accept needs for these shapes (0 on invalid args).  The

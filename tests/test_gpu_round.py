@@ -191,3 +191,69 @@ def test_round_from_host_buffers_matches_the_device_round():
     assert torch.equal(res_nl, ref_nl.cpu())
     assert torch.equal(t["k"].view(torch.int16), ref_k.view(torch.int16))
     r.close()
+
+
+def test_host_round_steps_back_to_back():
+    """Three spec_round_launch_host steps enqueued without a synchronisation in between, their
+    inputs alternating between two variants (different hidden states and draft distributions):
+    every step's results equal a device round on that step's inputs, so no step's copies overtake
+    the previous step's readers (the verification's inputs and the draft distributions travel on
+    streams of the round's own)."""
+    d = H.dev()
+    case = _case("rejection", 21)
+    t = H.to_device(case, d)
+    aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"])
+    va, outs = st.verify_args(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], case.rule, case.tau,
+                              case.eps, case.delta, case.seed, t["draft"], t["map"], path_cap=case.N)
+    ca, src, nl = st.compact_args(t["k"], t["v"], t["prefix_len"], outs["path"], outs["accept_len"])
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    r = st.Round(aa, va, ca, dev_status=status)
+    fresh = H.to_device(case, d)
+    keys = ("q", "hidden", "tokens", "parent", "draft")
+    var_a = {k: fresh[k].clone() for k in keys}
+    var_b = {k: fresh[k].clone() for k in keys}
+    var_b["hidden"] = (var_b["hidden"].float() * -0.75).to(var_b["hidden"].dtype)
+    var_b["draft"] = torch.roll(var_b["draft"], shifts=1, dims=-1)
+
+    def reset_caches():
+        t["k"].copy_(fresh["k"])
+        t["v"].copy_(fresh["v"])
+
+    refs = []
+    for var in (var_a, var_b):  # device rounds on each variant
+        reset_caches()
+        for k in keys:
+            t[k].copy_(var[k])
+        r.launch()
+        torch.cuda.synchronize()
+        refs.append(({k: v.clone() for k, v in outs.items()}, nl.clone()))
+    reset_caches()
+    for k in keys:
+        t[k].zero_()
+    n = int(case.n_nodes.max())
+    Lp = [int(x) for x in case.prefix_len]
+    tree_rows = []
+    for b in range(case.B):
+        for name in ("k", "v"):
+            rows = fresh[name][b, :, Lp[b]: Lp[b] + n].contiguous().cpu().pin_memory()
+            tree_rows.append((rows, t[name][b, :, Lp[b]: Lp[b] + n]))
+    host_vars = [{k: v[k].cpu().pin_memory() for k in keys} for v in (var_a, var_b)]
+    order = (0, 1, 0)
+    results = []
+    for step, vi in enumerate(order):  # the descriptors hold raw pointers: everything stays referenced
+        ins = [st.host_copy(host_vars[vi][k], t[k]) for k in keys]
+        ins += [st.host_copy(rows, dst, rows=case.Hkv) for rows, dst in tree_rows]
+        res = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+        res_nl = torch.empty(nl.shape, dtype=nl.dtype).pin_memory()
+        outs_c = [st.host_copy(res[k], outs[k]) for k in res] + [st.host_copy(res_nl, nl)]
+        r.launch_host(ins, outs_c)
+        results.append((vi, res, res_nl))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for vi, res, res_nl in results:
+        ref, ref_nl = refs[vi]
+        for k in res:
+            assert torch.equal(res[k], ref[k].cpu()), (vi, k)
+        assert torch.equal(res_nl, ref_nl.cpu()), vi
+    assert any(not torch.equal(refs[0][0][k], refs[1][0][k]) for k in refs[0][0]), "variants should differ"
+    r.close()

@@ -55,7 +55,7 @@ class VerifyArgs(ctypes.Structure):
                 ("parent", _vp), ("n_nodes", _vp), ("draft_probs", _vp), ("draft_to_target", _vp),
                 ("accept_len", _vp), ("path", _vp), ("bonus_token", _vp), ("margin_count", _vp),
                 ("bonus_margin", _vp), ("row_max", _vp), ("row_lse", _vp), ("row_entropy", _vp),
-                ("row_argmax", _vp), ("timing_begin", _vp), ("timing_end", _vp)]
+                ("row_argmax", _vp), ("timing_begin", _vp), ("timing_end", _vp), ("draft_ready", _vp)]
 
 
 class CompactArgs(ctypes.Structure):

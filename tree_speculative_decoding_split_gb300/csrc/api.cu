@@ -481,6 +481,13 @@ spec_status verify_accept_impl(const spec_verify_args* a, void* workspace, size_
   fp.counters = l.counters;
   fp.acc = ap;
   launch_row_finalize(fp, stream);
+  if (a->rule == SPEC_RULE_REJECTION && a->draft_ready) {  // the walk is the first reader of draft_probs
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (cudaStreamWaitEvent(stream, static_cast<cudaEvent_t>(a->draft_ready),
+                            cs == cudaStreamCaptureStatusActive ? cudaEventWaitExternal : 0) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+  }
   if (a->rule == SPEC_RULE_REJECTION && launch_accept(ap, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -19,8 +19,19 @@ struct spec_round {
   cudaGraphExec_t x_part[3];  // attention, verification, compaction (or null)
   cudaStream_t side;
   cudaEvent_t e_fork, e_join;
-  uintptr_t vonly[4][2];      // [lo, hi) of the buffers only the verification reads
+  uintptr_t vonly[3][2];      // [lo, hi) of the buffers only the verification reads (but draft_probs)
   int n_vonly;
+  // Rejection with draft distributions: their copies run on `side_d` beside the LM head, and
+  // the verification is issued as direct calls whose rejection walk waits for e_draft (a wait
+  // with well-defined host-order semantics, recorded afresh every launch).
+  bool direct_verify;
+  spec_verify_args vargs;     // the round's verification arguments, draft_ready = e_draft
+  void* vws;
+  size_t vws_bytes;
+  int32_t* dev_status;
+  cudaStream_t side_d;
+  cudaEvent_t e_draft;
+  uintptr_t draft[2];
 };
 
 namespace {
@@ -55,10 +66,13 @@ void release_parts(spec_round* r) {
     r->g_part[i] = nullptr;
   }
   if (r->side) cudaStreamDestroy(r->side);
+  if (r->side_d) cudaStreamDestroy(r->side_d);
   if (r->e_fork) cudaEventDestroy(r->e_fork);
   if (r->e_join) cudaEventDestroy(r->e_join);
-  r->side = nullptr;
-  r->e_fork = r->e_join = nullptr;
+  if (r->e_draft) cudaEventDestroy(r->e_draft);
+  r->side = r->side_d = nullptr;
+  r->e_fork = r->e_join = r->e_draft = nullptr;
+  r->direct_verify = false;
 }
 
 // The split launch state for a round with attention and verification; left empty (the host
@@ -93,9 +107,21 @@ void make_parts(spec_round* r, const spec_attn_args* attn, void* attn_ws, size_t
   add(verify->hidden_states, rows * verify->hidden * es);
   add(verify->tokens, rows * sizeof(int32_t));
   add(verify->lm_head_weight, (size_t)verify->vocab * verify->hidden * es);
-  if (verify->rule == SPEC_RULE_REJECTION)
-    add(verify->draft_probs, rows * (size_t)(verify->draft_vocab > 0 ? verify->draft_vocab : verify->vocab) *
-                                 sizeof(float));
+  if (verify->rule == SPEC_RULE_REJECTION && verify->draft_probs && !verify->draft_ready &&
+      cudaStreamCreateWithFlags(&r->side_d, cudaStreamNonBlocking) == cudaSuccess &&
+      cudaEventCreateWithFlags(&r->e_draft, cudaEventDisableTiming) == cudaSuccess) {
+    r->direct_verify = true;
+    r->vargs = *verify;
+    r->vargs.draft_ready = r->e_draft;
+    r->vws = verify_ws;
+    r->vws_bytes = verify_ws_bytes;
+    r->dev_status = dev_status;
+    r->draft[0] = reinterpret_cast<uintptr_t>(verify->draft_probs);
+    r->draft[1] = r->draft[0] + rows * (size_t)verify->draft_vocab * sizeof(float);
+  } else if (verify->rule == SPEC_RULE_REJECTION && verify->draft_probs) {
+    add(verify->draft_probs, rows * (size_t)verify->draft_vocab * sizeof(float));
+  }
+  cudaGetLastError();
 }
 
 }  // namespace
@@ -228,19 +254,38 @@ extern "C" spec_status spec_round_launch_host(const spec_round* round, const spe
     // runs the verification beside the attention; the compaction and the result copies follow
     // both.  The side stream starts after everything enqueued on `s` so far (the previous
     // round included), so no copy overwrites a buffer still being read.
-    auto verify_only = [&](const spec_host_copy& c) {
-      const uintptr_t lo = reinterpret_cast<uintptr_t>(c.device);
-      const uintptr_t hi = lo + (c.rows > 1 ? (size_t)(c.rows - 1) * c.device_pitch : 0) + c.row_bytes;
-      for (int k = 0; k < round->n_vonly; ++k)
-        if (lo >= round->vonly[k][0] && hi <= round->vonly[k][1]) return true;
-      return false;
+    auto extent = [](const spec_host_copy& c, uintptr_t& lo, uintptr_t& hi) {
+      lo = reinterpret_cast<uintptr_t>(c.device);
+      hi = lo + (c.rows > 1 ? (size_t)(c.rows - 1) * c.device_pitch : 0) + c.row_bytes;
     };
-    if (cudaEventRecord(round->e_fork, s) != cudaSuccess || cudaStreamWaitEvent(round->side, round->e_fork, 0) != cudaSuccess)
+    // 0: the caller's stream; 1: the verification's stream; 2: the draft distributions' stream
+    auto route = [&](const spec_host_copy& c) {
+      uintptr_t lo, hi;
+      extent(c, lo, hi);
+      if (round->direct_verify && lo >= round->draft[0] && hi <= round->draft[1]) return 2;
+      for (int k = 0; k < round->n_vonly; ++k)
+        if (lo >= round->vonly[k][0] && hi <= round->vonly[k][1]) return 1;
+      return 0;
+    };
+    if (cudaEventRecord(round->e_fork, s) != cudaSuccess || cudaStreamWaitEvent(round->side, round->e_fork, 0) != cudaSuccess ||
+        (round->direct_verify && cudaStreamWaitEvent(round->side_d, round->e_fork, 0) != cudaSuccess))
       return SPEC_ERR_CUDA;
-    for (int32_t i = 0; i < n_inputs; ++i)
-      if (enqueue_copy(inputs[i], true, verify_only(inputs[i]) ? round->side : s) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (cudaGraphLaunch(round->x_part[0], s) != cudaSuccess || cudaGraphLaunch(round->x_part[1], round->side) != cudaSuccess ||
-        cudaEventRecord(round->e_join, round->side) != cudaSuccess || cudaStreamWaitEvent(s, round->e_join, 0) != cudaSuccess)
+    for (int32_t i = 0; i < n_inputs; ++i) {
+      const int q = route(inputs[i]);
+      if (enqueue_copy(inputs[i], true, q == 0 ? s : (q == 1 ? round->side : round->side_d)) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    }
+    // the draft distributions are complete once e_draft (recorded after their copies, before the
+    // walk's wait is enqueued) completes
+    if (round->direct_verify && cudaEventRecord(round->e_draft, round->side_d) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (cudaGraphLaunch(round->x_part[0], s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (round->direct_verify) {
+      const spec_status vs = spec_verify_accept(&round->vargs, round->vws, round->vws_bytes, round->dev_status, round->side);
+      if (vs != SPEC_OK) return vs;
+    } else if (cudaGraphLaunch(round->x_part[1], round->side) != cudaSuccess) {
+      return SPEC_ERR_CUDA;
+    }
+    if (cudaEventRecord(round->e_join, round->side) != cudaSuccess || cudaStreamWaitEvent(s, round->e_join, 0) != cudaSuccess)
       return SPEC_ERR_CUDA;
     if (round->x_part[2] && cudaGraphLaunch(round->x_part[2], s) != cudaSuccess) return SPEC_ERR_CUDA;
   } else {
