@@ -476,7 +476,9 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
                    "statistic": "median over the timed steps"},
         "e2e": {"value": job_rate(world, w["nodes"], e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "call": "spec_round_launch_host: pinned host inputs copied in, the round, results copied out"},
+                "call": ("spec_round_launch_host: pinned host inputs copied in (those only the verification "
+                         "reads on the round's own streams, beside the attention), the round, results copied out; "
+                         "every step's copies are inside the timed region")},
         # the graph runs attention and verification as parallel branches, so its compaction is a
         # launch of its own, as in the direct calls
         "gpu_launches": K * _launches_per_step(case, n_split, stream_k, False),
