@@ -160,3 +160,47 @@ def test_paged_compaction_bit_exact(dtype, bs):
     after = tk.view(torch.int16).cpu().numpy() if bf else tk.cpu().numpy()
     was = before.view(torch.int16).cpu().numpy() if bf else before.cpu().numpy()
     assert (oracle.gather_paged(after, table[:1], bs, L_cap) == oracle.gather_paged(was, table[:1], bs, L_cap)).all()
+
+
+def test_paged_round_matches_direct_calls():
+    """The captured round on a paged pool -- tree attention and verification as parallel branches,
+    compaction after both -- gives the three direct calls' outputs and pool, bit for bit (the
+    compaction rewrites pool rows the attention reads, so it must not overtake it)."""
+    d = H.dev()
+    rng = np.random.default_rng(5)
+    parents = [T.random_bfs_tree(rng, 40, 6)[0] for _ in range(3)]
+    case = make_case(dtype="bf16", Hq=8, Hkv=2, d=128, Hd=64, V=16, prefix_len=[500, 7, 1300], parents=parents,
+                     tokens=("rank", 0.95), N=40, seed=11, rng=rng)  # drafts close to the target: paths accepted
+    table, pk, pv = _pool(case, 32, rng)
+
+    def fresh():
+        t = H.to_device(case, d)
+        return t, H.tensor(pk, d, True), H.tensor(pv, d, True), H.tensor(table, d)
+
+    # the direct calls
+    t, tk, tv, tab = fresh()
+    out, lse = st.tree_attention(t["q"], tk, tv, t["prefix_len"], t["n_nodes"], t["parent"], block_table=tab)
+    outs = st.verify_accept(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], "greedy", path_cap=case.N)
+    src, nl = st.compact_kv(tk, tv, t["prefix_len"], outs["path"], outs["accept_len"], block_table=tab)
+    torch.cuda.synchronize()
+    ref = {"out": out.clone(), "lse": lse.clone(), "src": src.clone(), "nl": nl.clone(), "k": tk.clone(),
+           "v": tv.clone(), **{k: v.clone() for k, v in outs.items()}}
+    # the round on a fresh copy of everything
+    t, tk, tv, tab = fresh()
+    aa, out, lse = st.attn_args(t["q"], tk, tv, t["prefix_len"], t["n_nodes"], t["parent"], block_table=tab)
+    va, outs = st.verify_args(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], "greedy",
+                              path_cap=case.N)
+    ca, src, nl = st.compact_args(tk, tv, t["prefix_len"], outs["path"], outs["accept_len"], block_table=tab)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    r = st.Round(aa, va, ca, dev_status=status)
+    r.launch()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = {"out": out, "lse": lse, "src": src, "nl": nl, "k": tk, "v": tv, **outs}
+    for k, v in ref.items():
+        a, b = got[k], v
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), k
+    assert int(ref["accept_len"].max().item()) >= 1, "no request accepted a node: the compaction was not exercised"
+    r.close()
