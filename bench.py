@@ -295,13 +295,21 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
     dev = torch.device("cuda", local)
     case = make_config_case(cfg, seed=seed)
     t = _device_tensors(case, dev)
+    t["draft_rows"] = None
+    if case.draft_probs is not None:
+        # a drafter has distributions only for the nodes it expanded: pass those rows compactly
+        from gen import compact_draft
+        rows, index = compact_draft(case.draft_probs, case.parent, case.n_nodes)
+        t["draft"] = torch.from_numpy(rows).to(dev)
+        t["draft_rows"] = torch.from_numpy(index).to(dev)
     stream = torch.cuda.current_stream()
     sp = ctypes.c_void_p(stream.cuda_stream)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"])
     va, outs = st.verify_args(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], case.rule, case.tau,
-                              case.eps, case.delta, case.seed, t["draft"], t["map"], path_cap=case.N)
+                              case.eps, case.delta, case.seed, t["draft"], t["map"], path_cap=case.N,
+                              draft_rows=t["draft_rows"])
     ca, src_slot, new_len = st.compact_args(t["k"], t["v"], t["prefix_len"], outs["path"], outs["accept_len"])
     need_a = L.spec_tree_attention_workspace(ctypes.byref(aa))
     need_v = L.spec_verify_accept_workspace(ctypes.byref(va))
@@ -384,8 +392,8 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
     n_tree = int(case.n_nodes.max())
     Lp = [int(x) for x in case.prefix_len]
     step_inputs = ["q", "hidden", "tokens", "parent", "n_nodes", "prefix_len"]
-    if t["draft"] is not None:  # rejection sampling: the draft distributions arrive with every step
-        step_inputs.append("draft")
+    if t["draft"] is not None:  # rejection sampling: the expanded nodes' draft distributions and
+        step_inputs += ["draft", "draft_rows"]  # their row index arrive with every step
     host = {k: t[k].cpu().pin_memory() for k in step_inputs}
     ins = [st.host_copy(host[k], t[k]) for k in step_inputs]
     for b in range(case.B):  # the tree's new K/V rows, one strided copy per request and cache
@@ -469,6 +477,9 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
                    "tree_nodes": [int(x) for x in case.n_nodes][:8], "q_heads": case.Hq, "kv_heads": case.Hkv,
                    "head_dim": case.d, "hidden": case.Hd, "vocab": case.V, "rule": case.rule, "temperature": case.tau,
                    "eps": case.eps, "delta": case.delta, "parallelism": f"replicas x{world}",
+                   "draft_distributions": (None if t["draft"] is None else
+                                           f"{t['draft'].shape[0]} rows (the expanded nodes') of "
+                                           f"{t['draft'].shape[1]} fp32, indexed by draft_rows [B][N]"),
                    "l2": "flushed before every step (256 MB write, then read)",
                    "launch": ("one CUDA-graph launch of the captured round per step (spec_round_launch; "
                               "tree attention and verification as parallel branches, compaction after both)"
@@ -476,9 +487,10 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
                    "statistic": "median over the timed steps"},
         "e2e": {"value": job_rate(world, w["nodes"], e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "call": ("spec_round_launch_host: pinned host inputs copied in (those only the verification "
-                         "reads on the round's own streams, beside the attention), the round, results copied out; "
-                         "every step's copies are inside the timed region")},
+                "call": ("spec_round_launch_host: pinned host inputs copied in group after group (the "
+                         "verification's on the round's own stream, then the attention's, then the draft "
+                         "distributions beside the LM head), the round, results copied out; every step's copies "
+                         "are inside the timed region")},
         # the graph runs attention and verification as parallel branches, so its compaction is a
         # launch of its own, as in the direct calls
         "gpu_launches": K * _launches_per_step(case, n_split, stream_k, False),

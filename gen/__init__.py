@@ -15,5 +15,5 @@ candidates.
 
 from .bf16 import f32_to_bf16_bits, bf16_bits_to_f32, bf16_bits_to_f64  # noqa: F401
 from .configs import CONFIGS, config_by_id  # noqa: F401
-from .inputs import Case, make_config_case, make_case  # noqa: F401
+from .inputs import Case, compact_draft, make_config_case, make_case  # noqa: F401
 from . import trees  # noqa: F401

@@ -281,3 +281,19 @@ def make_config_case(cfg_id, seed=0):
                      seed=seed, tokens=spec["tokens"], name=spec["name"], rng=rng)
     case.meta["config"] = cfg_id
     return case
+
+
+def compact_draft(draft_probs, parent, n_nodes, rng=None):
+    """The draft distributions of the nodes that have children, as a compact [rows][Vd] array and
+    a [B][N] row index (-1 for nodes without children): the layout a dynamic drafter produces,
+    since it expands only some nodes.  ``rng`` shuffles the row order (a layout check for tests)."""
+    B, N = parent.shape
+    keys = sorted({(b, int(parent[b, c])) for b in range(B) for c in range(1, int(n_nodes[b]))})
+    if rng is not None:
+        keys = [keys[i] for i in rng.permutation(len(keys))]
+    index = np.full((B, N), -1, dtype=np.int32)
+    rows = np.zeros((max(len(keys), 1), draft_probs.shape[-1]), dtype=np.float32)
+    for r, (b, e) in enumerate(keys):
+        index[b, e] = r
+        rows[r] = draft_probs[b, e]
+    return rows, index

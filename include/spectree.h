@@ -59,7 +59,8 @@ typedef int32_t spec_status;
 #define SPEC_ERR_WORKSPACE_TOO_SMALL 3 /* host: workspace_bytes below the *_workspace() query */
 #define SPEC_ERR_BAD_TREE 4           /* device: parent array is not a valid rooted tree */
 #define SPEC_ERR_CUDA 5               /* host: a CUDA runtime call failed (launch, attribute) */
-#define SPEC_ERR_BAD_TOKEN 6          /* device: token or draft map entry outside the vocabulary */
+#define SPEC_ERR_BAD_TOKEN 6          /* device: token or draft map entry outside the vocabulary,
+                                         or a node with children without a draft row */
 #define SPEC_ERR_CAPACITY 7           /* device: prefix_len + n_nodes > L_cap, or a path longer
                                          than path_cap */
 #define SPEC_ERR_TIMEOUT 8            /* device: a bounded wait in a kernel ran out */
@@ -184,7 +185,8 @@ typedef struct spec_verify_args {
   const int32_t* tokens;          /* [B][N] target-vocab ids (entry 0 unused) */
   const int32_t* parent;          /* [B][N] */
   const int32_t* n_nodes;         /* [B] */
-  const float* draft_probs;       /* REJECTION: [B][N][Vd]; row e = distribution of e's children */
+  const float* draft_probs;       /* REJECTION: [B][N][Vd]; row e = distribution of e's children
+                                     (compact [n_draft_rows][Vd] with draft_rows, below) */
   const int32_t* draft_to_target; /* REJECTION: [Vd] injective map into [0, V), or NULL */
   int32_t* accept_len;            /* out [B] */
   int32_t* path;                  /* out [B][path_cap], -1 padded */
@@ -202,6 +204,14 @@ typedef struct spec_verify_args {
                                      reader of draft_probs) waits for it, so the distributions may
                                      still be arriving while the LM head runs; NULL = none.  Inside
                                      a stream capture the wait is captured as an external one. */
+  const int32_t* draft_rows;      /* REJECTION, optional [B][N]: with it, draft_probs is a compact
+                                     [n_draft_rows][Vd] array and node e's distribution is row
+                                     draft_rows[b][e]; nodes without children may hold -1.  A
+                                     dynamic tree expands only some of its nodes (the EAGLE-2
+                                     reading of tech-tldr, section "ツリー検証"), so only their rows
+                                     need to exist and travel.  NULL = draft_probs is [B][N][Vd]. */
+  int32_t n_draft_rows;           /* rows of draft_probs when draft_rows != NULL (>= 1) */
+  int32_t reserved1;              /* must be 0 */
 } spec_verify_args;
 
 /* Bytes of workspace spec_verify_accept needs for these shapes (0 on invalid args).  The
@@ -465,7 +475,10 @@ void spec_round_destroy(spec_round* round);
  * everything already enqueued on `stream`, carries the verification beside the attention, and
  * rejoins `stream` before the compaction and the result copies.  Every other input copy, and
  * every output copy, is on `stream`.  Those verification-only buffers must therefore not overlap
- * any buffer the attention reads.
+ * any buffer the attention reads.  The input copies run group after group, each with the whole
+ * host link: the verification's first (its LM head is issued before the attention), then those
+ * on `stream`, then the draft distributions (and with draft_rows, the compact rows), which only
+ * the rejection walk at the end of the verification reads.
  *
  * Each spec_host_copy moves `rows` rows of `row_bytes` bytes; row r starts at
  * host + r * host_pitch and at device + r * device_pitch (pitches are ignored when rows == 1).

@@ -3,7 +3,7 @@
 import numpy as np
 
 import oracle
-from gen import make_case, trees as T
+from gen import compact_draft, make_case, trees as T
 from gen.bf16 import bf16_bits_to_f32, f32_to_bf16_bits
 
 
@@ -54,3 +54,24 @@ def test_make_case_deterministic_and_shaped():
     for bb in range(2):
         for c in range(1, a.n_nodes[bb]):
             assert a.draft_probs[bb, a.parent[bb, c], a.tokens[bb, c]] > 0
+
+
+def test_compact_draft_keeps_exactly_the_expanded_rows():
+    rng = np.random.default_rng(3)
+    parents = [T.random_bfs_tree(rng, 20, 4)[0], T.chain_tree(5), np.array([-1], dtype=np.int32)]
+    N, Vd = 20, 7
+    parent = np.full((3, N), -1, dtype=np.int32)
+    for b, p in enumerate(parents):
+        parent[b, : len(p)] = p
+    n_nodes = np.array([len(p) for p in parents])
+    full = rng.random((3, N, Vd)).astype(np.float32)
+    rows, index = compact_draft(full, parent, n_nodes, rng=rng)
+    expanded = {(b, int(parent[b, c])) for b in range(3) for c in range(1, n_nodes[b])}
+    assert rows.shape == (len(expanded), Vd)
+    assert sorted(index[index >= 0].tolist()) == list(range(len(expanded)))
+    for b in range(3):
+        for e in range(N):
+            if (b, e) in expanded:
+                assert (rows[index[b, e]] == full[b, e]).all()
+            else:
+                assert index[b, e] == -1

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import tree_speculative_decoding_split_gb300 as st
-from gen import make_case, trees as T
+from gen import compact_draft, make_case, trees as T
 import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
@@ -256,4 +256,53 @@ def test_host_round_steps_back_to_back():
             assert torch.equal(res[k], ref[k].cpu()), (vi, k)
         assert torch.equal(res_nl, ref_nl.cpu()), vi
     assert any(not torch.equal(refs[0][0][k], refs[1][0][k]) for k in refs[0][0]), "variants should differ"
+    r.close()
+
+
+def test_host_round_with_compact_draft_rows():
+    """The host-buffer round with the draft distributions of the expanded nodes only (compact
+    [rows][Vd] plus a [B][N] row index, both copied from the host): the same results as the
+    device round over the full [B][N][Vd] layout."""
+    d = H.dev()
+    case = _case("rejection", 23)
+    t = H.to_device(case, d)
+    aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"])
+    va, outs = st.verify_args(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], case.rule, case.tau,
+                              case.eps, case.delta, case.seed, t["draft"], t["map"], path_cap=case.N)
+    ca, src, nl = st.compact_args(t["k"], t["v"], t["prefix_len"], outs["path"], outs["accept_len"])
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    r = st.Round(aa, va, ca, dev_status=status)
+    r.launch()
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in outs.items()}
+    ref_k, ref_nl = t["k"].clone(), nl.clone()
+    r.close()
+
+    rows, index = compact_draft(case.draft_probs, case.parent, case.n_nodes, rng=np.random.default_rng(4))
+    t2 = H.to_device(case, d)
+    t2["rows"], t2["index"] = H.tensor(rows, d), H.tensor(index, d)
+    aa, out, lse = st.attn_args(t2["q"], t2["k"], t2["v"], t2["prefix_len"], t2["n_nodes"], t2["parent"])
+    va, outs = st.verify_args(t2["hidden"], t2["W"], t2["tokens"], t2["parent"], t2["n_nodes"], case.rule, case.tau,
+                              case.eps, case.delta, case.seed, t2["rows"], t2["map"], path_cap=case.N,
+                              draft_rows=t2["index"])
+    ca, src, nl = st.compact_args(t2["k"], t2["v"], t2["prefix_len"], outs["path"], outs["accept_len"])
+    r = st.Round(aa, va, ca, dev_status=status)
+    keys = ("q", "hidden", "tokens", "parent", "rows", "index")
+    host = {k: t2[k].cpu().pin_memory() for k in keys}
+    for k in keys:
+        t2[k].zero_()
+    for v in outs.values():
+        v.fill_(-7)
+    ins = [st.host_copy(host[k], t2[k]) for k in keys]
+    res = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    res_nl = torch.empty(nl.shape, dtype=nl.dtype).pin_memory()
+    outs_c = [st.host_copy(res[k], outs[k]) for k in res] + [st.host_copy(res_nl, nl)]
+    torch.cuda.synchronize()
+    r.launch_host(ins, outs_c)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for k in res:
+        assert torch.equal(res[k], ref[k].cpu()), k
+    assert torch.equal(res_nl, ref_nl.cpu())
+    assert torch.equal(t2["k"].view(torch.int16), ref_k.view(torch.int16))
     r.close()

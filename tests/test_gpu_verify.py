@@ -2,9 +2,11 @@
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
-from gen import make_case, make_config_case, trees as T
+import tree_speculative_decoding_split_gb300 as st
+from gen import compact_draft, make_case, make_config_case, trees as T
 import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
@@ -198,3 +200,80 @@ def test_up_to_64_rows_vocab_on_m(rule):
     H.check_row_stats(case, got, _rows(case))
     pad = [(b, i) for b in range(case.B) for i in range(case.n_nodes[b], case.N)]
     assert all(got["row_argmax"][b, i] == -1 for b, i in pad)
+
+
+def _verify_compact(case, t, rows, index, status=None):
+    d = t["hidden"].device
+    status = torch.zeros(1, dtype=torch.int32, device=d) if status is None else status
+    res = st.verify_accept(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], case.rule, case.tau,
+                           case.eps, case.delta, case.seed, draft_probs=H.tensor(rows, d),
+                           draft_to_target=t["map"], dev_status=status, draft_rows=H.tensor(index, d))
+    torch.cuda.synchronize()
+    out = {k: v.cpu().numpy() for k, v in res.items()}
+    out["status"] = int(status.item())
+    return out
+
+
+_VERIFY_OUT = ("accept_len", "path", "bonus_token", "margin_count", "bonus_margin")
+
+
+@pytest.mark.parametrize("V", [5000, 300001])
+def test_compact_draft_rows_match_the_full_layout(V):
+    """Draft distributions given only for the expanded nodes (a compact [rows][Vd] array in
+    shuffled order plus a [B][N] row index): the cluster walk (V 5000) and the single-CTA walk
+    (V above 8 x 32768) decide exactly as with the full [B][N][Vd] layout, and match the oracle."""
+    d = H.dev()
+    rng = np.random.default_rng(V + 7)
+    parents = [T.random_bfs_tree(rng, 40, 5)[0], T.chain_tree(12), T.random_bfs_tree(rng, 40, 3)[0]]
+    case = make_case(dtype="bf16", Hq=4, Hkv=1, d=64, Hd=128, V=V, prefix_len=[4] * 3, parents=parents,
+                     rule="rejection", tau=0.9, seed=V + 3, tokens=("iid", 0.8, 0.4), rng=rng)
+    t = H.to_device(case, d)
+    full = H.gpu_verify(case, t, hooks=False)
+    rows, index = compact_draft(case.draft_probs, case.parent, case.n_nodes, rng=rng)
+    assert rows.shape[0] < case.B * case.N
+    got = _verify_compact(case, t, rows, index)
+    assert got["status"] == 0 and full["status"] == 0
+    for k in _VERIFY_OUT:
+        assert (got[k] == full[k]).all(), k
+    c = H.check_verify(case, got, H.oracle_verify(case))
+    assert c.exact + c.excluded == case.B
+
+
+def test_compact_draft_rows_on_the_eagle3_b32_workload():
+    """The B32 EAGLE-3-shaped workload (mapped 32000-token draft vocabulary) with only the
+    expanded nodes' draft rows: the same decisions as the full [B][N][Vd] layout, from a draft
+    buffer an eighth of its size."""
+    d = H.dev()
+    case = H.config_case(4, 2)
+    t = H.to_device(case, d)
+    full = H.gpu_verify(case, t, hooks=False)
+    rows, index = compact_draft(case.draft_probs, case.parent, case.n_nodes, rng=np.random.default_rng(1))
+    assert rows.shape[0] * 4 < case.B * case.N
+    got = _verify_compact(case, t, rows, index)
+    assert got["status"] == 0 and full["status"] == 0
+    for k in _VERIFY_OUT:
+        assert (got[k] == full[k]).all(), k
+
+
+def test_missing_draft_row_zeroes_only_that_request():
+    """A node with children whose draft row index is -1 (or past the compact array): SPEC_ERR_BAD_TOKEN,
+    that request's outputs zeroed, the others decided as usual."""
+    d = H.dev()
+    rng = np.random.default_rng(77)
+    parents = [T.random_bfs_tree(rng, 30, 4)[0] for _ in range(3)]
+    case = make_case(dtype="bf16", Hq=4, Hkv=1, d=64, Hd=128, V=3000, prefix_len=[4] * 3, parents=parents,
+                     rule="rejection", tau=0.9, seed=12, tokens=("iid", 0.8, 0.4), rng=rng)
+    t = H.to_device(case, d)
+    full = H.gpu_verify(case, t, hooks=False)
+    rows, index = compact_draft(case.draft_probs, case.parent, case.n_nodes)
+    for bad in (-1, rows.shape[0]):
+        idx = index.copy()
+        e = int(case.parent[1, int(case.n_nodes[1]) - 1])  # an expanded node of request 1
+        idx[1, e] = bad
+        got = _verify_compact(case, t, rows, idx)
+        assert got["status"] == 6
+        assert got["accept_len"][1] == 0 and got["bonus_token"][1] == -1
+        assert got["path"][1][0] == 0 and (got["path"][1][1:] == -1).all()
+        for b in (0, 2):
+            for k in ("accept_len", "path", "bonus_token"):
+                assert (got[k][b] == full[k][b]).all(), (b, k)

@@ -55,7 +55,8 @@ class VerifyArgs(ctypes.Structure):
                 ("parent", _vp), ("n_nodes", _vp), ("draft_probs", _vp), ("draft_to_target", _vp),
                 ("accept_len", _vp), ("path", _vp), ("bonus_token", _vp), ("margin_count", _vp),
                 ("bonus_margin", _vp), ("row_max", _vp), ("row_lse", _vp), ("row_entropy", _vp),
-                ("row_argmax", _vp), ("timing_begin", _vp), ("timing_end", _vp), ("draft_ready", _vp)]
+                ("row_argmax", _vp), ("timing_begin", _vp), ("timing_end", _vp), ("draft_ready", _vp),
+                ("draft_rows", _vp), ("n_draft_rows", ctypes.c_int32), ("reserved1", ctypes.c_int32)]
 
 
 class CompactArgs(ctypes.Structure):
@@ -289,8 +290,12 @@ def tree_attention(q, k_cache, v_cache, prefix_len, n_nodes, parent, out=None, l
 
 
 def verify_args(hidden, weight, tokens, parent, n_nodes, rule, temperature=0.0, eps=0.09, delta=0.3,
-                seed=0, draft_probs=None, draft_to_target=None, path_cap=None, hooks=False, outputs=None):
-    """Build the C argument struct for verify_accept; returns (args, outputs dict)."""
+                seed=0, draft_probs=None, draft_to_target=None, path_cap=None, hooks=False, outputs=None,
+                draft_rows=None):
+    """Build the C argument struct for verify_accept; returns (args, outputs dict).
+
+    ``draft_probs`` is [B][N][Vd], or with ``draft_rows`` (int32 [B][N], -1 for nodes without
+    children) a compact [rows][Vd] array holding only the expanded nodes' distributions."""
     torch = _torch()
     _need(hidden, "hidden")
     dev = hidden.device
@@ -310,6 +315,12 @@ def verify_args(hidden, weight, tokens, parent, n_nodes, rule, temperature=0.0, 
         Vd = draft_probs.shape[-1]
     if draft_to_target is not None:
         _need(draft_to_target, "draft_to_target", torch.int32, dev)
+    n_draft_rows = 0
+    if draft_rows is not None:
+        _need(draft_rows, "draft_rows", torch.int32, dev)
+        if draft_probs is None or draft_probs.dim() != 2 or tuple(draft_rows.shape) != (B, N):
+            raise ValueError("draft_rows [B][N] goes with a compact draft_probs [rows][Vd]")
+        n_draft_rows = draft_probs.shape[0]
     if outputs is None:
         outputs = dict(
             accept_len=torch.empty(B, dtype=torch.int32, device=dev),
@@ -332,16 +343,17 @@ def verify_args(hidden, weight, tokens, parent, n_nodes, rule, temperature=0.0, 
                    bonus_token=_ptr(o["bonus_token"]), margin_count=_ptr(o.get("margin_count")),
                    bonus_margin=_ptr(o.get("bonus_margin")), row_max=_ptr(o.get("row_max")),
                    row_lse=_ptr(o.get("row_lse")), row_entropy=_ptr(o.get("row_entropy")),
-                   row_argmax=_ptr(o.get("row_argmax")))
+                   row_argmax=_ptr(o.get("row_argmax")), draft_rows=_ptr(draft_rows), n_draft_rows=n_draft_rows,
+                   reserved1=0)
     return a, outputs
 
 
 def verify_accept(hidden, weight, tokens, parent, n_nodes, rule, temperature=0.0, eps=0.09, delta=0.3, seed=0,
                   draft_probs=None, draft_to_target=None, path_cap=None, hooks=False, workspace=None,
-                  dev_status=None, stream=None, outputs=None):
+                  dev_status=None, stream=None, outputs=None, draft_rows=None):
     """LM head + acceptance + longest path (see spec_verify_accept).  Returns a dict of tensors."""
     a, outputs = verify_args(hidden, weight, tokens, parent, n_nodes, rule, temperature, eps, delta, seed,
-                             draft_probs, draft_to_target, path_cap, hooks, outputs)
+                             draft_probs, draft_to_target, path_cap, hooks, outputs, draft_rows)
     L = lib()
     need = L.spec_verify_accept_workspace(ctypes.byref(a))
     if need == 0:

@@ -62,11 +62,22 @@ __device__ int load_and_validate(const AcceptParams& p, int b, int* s_par, int* 
       if (s_tok) s_tok[c] = tok;
       if (c == 0 ? par != -1 : (par < 0 || par >= c)) bad_tree = 1;
       if (c > 0 && (tok < 0 || tok >= p.V)) bad_tok = 1;
+      if (c > 0 && p.draft_rows && par >= 0 && par < c) {  // a parent's draft row must exist
+        const int dr = p.draft_rows[(size_t)b * p.N + par];
+        if (dr < 0 || dr >= p.n_draft_rows) bad_tok = 1;
+      }
     }
   }
   bad_tree = __syncthreads_or(bad_tree);
   bad_tok = __syncthreads_or(bad_tok);
   return bad_tree ? SPEC_ERR_BAD_TREE : (bad_tok ? SPEC_ERR_BAD_TOKEN : 0);
+}
+
+// Node e's draft distribution (rejection): row b * N + e, or the compact row draft_rows[b][e].
+// Called only for nodes with children, whose rows load_and_validate has checked.
+__device__ __forceinline__ const float* draft_row(const AcceptParams& p, int b, int e) {
+  const size_t r = p.draft_rows ? (size_t)p.draft_rows[(size_t)b * p.N + e] : (size_t)b * p.N + e;
+  return p.draft + r * (size_t)p.Vd;
 }
 
 // Writes path = root .. e (depth(e) + 1 entries), -1 beyond.
@@ -349,8 +360,7 @@ __device__ void rejection_block_walk(const AcceptParams& p) {
   float S = 1.f;         // sum of Rb[cur]
   int e = 0, dep = 0, margins = 0;
 
-  auto draft_at = [&](int node, int v) -> float {
-    const float* row = p.draft + (rb + node) * (size_t)p.Vd;
+  auto draft_at = [&](const float* row, int v) -> float {
     if (p.inv_map) {
       const int j = p.inv_map[v];
       return j >= 0 ? row[j] : 0.f;
@@ -370,13 +380,14 @@ __device__ void rejection_block_walk(const AcceptParams& p) {
     const size_t erow = rb + e;
     const float* lg = p.logits + erow * (size_t)V;
     const float lse_e = p.rlse[erow];
+    const float* de = nk > 0 ? draft_row(p, b, e) : nullptr;
     bool moved = false;
     for (int k = 0; k < nk; ++k) {
       const int c = s_kids[k];
       if (tid == 0) {
         const int x = s_tok[c];
         const float u = accept_uniform(p.seed, (uint32_t)b, (uint32_t)c, 0u);
-        const float Dx = draft_at(e, x);
+        const float Dx = draft_at(de, x);
         const float Rx = lazy ? expf(lg[x] * p.inv_tau - lse_e) : Rb[cur][x] / S;
         const float a = (Dx > 0.f) ? fminf(1.f, Rx / Dx) : (Rx > 0.f ? 1.f : 0.f);
         if (fabsf(u - a) < kMargin) ++margins;
@@ -398,7 +409,7 @@ __device__ void rejection_block_walk(const AcceptParams& p) {
       float part = 0.f;
       for (int v = tid; v < V; v += blockDim.x) {
         const float r = lazy ? expf(lg[v] * p.inv_tau - lse_e) : Rc[v] * invS;
-        const float nv = fmaxf(r - draft_at(e, v), 0.f);
+        const float nv = fmaxf(r - draft_at(de, v), 0.f);
         Rn[v] = nv;
         part += nv;
       }
@@ -573,19 +584,20 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
   bool moved = true;
 
   while (moved) {
-    // ---- arrive at node e: r <- T_e, s_D <- D_e (this slice) ----
+    // ---- arrive at node e: r <- T_e, s_D <- D_e (this slice; a leaf has no D_e) ----
+    const int c_first = next_child(s_kids, e, -1);
     {
       const size_t erow = rb + e;
       const float* lg = p.logits + erow * (size_t)V + base;
-      const float* drow = p.draft + erow * (size_t)p.Vd;
-      if (p.inv_map) {  // draft indices first (asynchronously, into s_D), then the gathers
+      const float* drow = c_first >= 0 ? draft_row(p, b, e) : nullptr;
+      if (drow && p.inv_map) {  // draft indices first (asynchronously, into s_D), then the gathers
 #pragma unroll
         for (int j = 0; j < kRcEpt; ++j) {
           const int li = j * kRcThreads + tid;
           if (li < Lc) cp_async_4(s_D + li, p.inv_map + base + li);
         }
         asm volatile("cp.async.commit_group;\n" ::: "memory");
-      } else {
+      } else if (drow) {
 #pragma unroll
         for (int j = 0; j < kRcEpt; ++j) {
           const int li = j * kRcThreads + tid;
@@ -598,7 +610,7 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
         const int li = j * kRcThreads + tid;
         r[j] = (li < Lc) ? __ldg(lg + li) : 0.f;
       }
-      if (p.inv_map) {
+      if (drow && p.inv_map) {
         cp_async_wait_all();
 #pragma unroll
         for (int j = 0; j < kRcEpt; ++j) {
@@ -623,13 +635,13 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
       cp_async_wait_all();  // each thread reads back only the entries it copied
     }
     moved = false;
-    int c = next_child(s_kids, e, -1);
+    int c = c_first;
     if (c < 0) break;  // a leaf: the bonus is drawn from T_e
     // the first child sees R = T_e: every CTA evaluates R[x] and D[x] itself
     const size_t erow = rb + e;
     {
       const int x = s_tok[c];
-      const float* drow = p.draft + erow * (size_t)p.Vd;
+      const float* drow = draft_row(p, b, e);
       float rx = target_prob(__ldg(p.logits + erow * (size_t)V + x), p.inv_tau, p.rlse[erow]);
       float dx;
       if (p.inv_map) {

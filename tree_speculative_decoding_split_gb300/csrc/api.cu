@@ -168,7 +168,8 @@ AttnLayout layout_attn(const spec_attn_args* a, void* ws) {
 spec_status check_verify(const spec_verify_args* a) {
   if (!a) return SPEC_ERR_INVALID_ARGUMENT;
   if (a->dtype != SPEC_DTYPE_F32 && a->dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
-  if (a->batch < 1 || a->n_max < 1 || a->hidden < 1 || a->vocab < 2 || a->path_cap < 1 || a->reserved0 != 0)
+  if (a->batch < 1 || a->n_max < 1 || a->hidden < 1 || a->vocab < 2 || a->path_cap < 1 || a->reserved0 != 0 ||
+      a->reserved1 != 0)
     return SPEC_ERR_INVALID_ARGUMENT;
   if (a->n_max > SPEC_MAX_NODES) return SPEC_ERR_UNSUPPORTED;
   if (a->dtype == SPEC_DTYPE_BF16 && a->hidden % 64) return SPEC_ERR_UNSUPPORTED;
@@ -186,6 +187,7 @@ spec_status check_verify(const spec_verify_args* a) {
     if (!a->draft_probs || a->draft_vocab < 1) return SPEC_ERR_INVALID_ARGUMENT;
     if (!a->draft_to_target && a->draft_vocab != a->vocab) return SPEC_ERR_INVALID_ARGUMENT;
     if (a->draft_vocab > a->vocab) return SPEC_ERR_INVALID_ARGUMENT;
+    if (a->draft_rows && a->n_draft_rows < 1) return SPEC_ERR_INVALID_ARGUMENT;
   }
   const long long R = (long long)a->batch * a->n_max;
   if (R > 0x7fffffffLL / 2 || (long long)a->vocab * R > (1LL << 40)) return SPEC_ERR_UNSUPPORTED;
@@ -462,6 +464,10 @@ spec_status verify_accept_impl(const spec_verify_args* a, void* workspace, size_
   ap.tokens = a->tokens; ap.parent = a->parent; ap.n_nodes = a->n_nodes;
   ap.rmax = l.rmax; ap.rlse = l.rlse; ap.rent = l.rent; ap.rgap = l.rgap; ap.rarg = l.rarg; ap.clog = l.clog;
   ap.logits = l.logits; ap.draft = a->draft_probs; ap.inv_map = l.inv; ap.map_bad = l.map_bad; ap.rbuf = l.rbuf;
+  if (a->rule == SPEC_RULE_REJECTION && a->draft_rows) {
+    ap.draft_rows = a->draft_rows;
+    ap.n_draft_rows = a->n_draft_rows;
+  }
   ap.accept_len = a->accept_len; ap.path = a->path; ap.bonus = a->bonus_token;
   ap.margin_count = a->margin_count; ap.bonus_margin = a->bonus_margin;
   ap.dev_status = dev_status;
@@ -528,7 +534,7 @@ const char* spec_status_string(spec_status s) {
     case SPEC_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than the *_workspace() query";
     case SPEC_ERR_BAD_TREE: return "parent array is not a valid rooted, topologically ordered tree";
     case SPEC_ERR_CUDA: return "CUDA runtime error";
-    case SPEC_ERR_BAD_TOKEN: return "token or draft-map entry outside the vocabulary";
+    case SPEC_ERR_BAD_TOKEN: return "token or draft-map entry outside the vocabulary, or a missing draft row";
     case SPEC_ERR_CAPACITY: return "KV capacity or path capacity exceeded";
     case SPEC_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
     default: return "unknown status";

@@ -63,25 +63,8 @@ struct AttnTcCfg {
   static_assert(kRowsCta * kORow <= NG * kQ + 2 * kStages * kTile, "O staging does not fit");
 };
 
-// 2^x with the special-function unit's approximation (PTX ex2.approx.ftz: about 2 ulp; results
-// below the normal range flush to 0).  P is rounded to bf16 right after, so this is ample.
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ uint32_t sw128_off(int r, int ch, int rows) {
   return (uint32_t)((ch >> 3) * rows * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ void tma_load_4d_plain(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                                  int z, int w) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
 }
 
 // One row of the output partial (fp32) from shared memory to global memory by the bulk-copy
@@ -93,15 +76,6 @@ __device__ __forceinline__ void bulk_store_row(void* gdst, const void* ssrc, uin
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
-__device__ __forceinline__ void tma_load_3d_plain(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                                  int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 
 }  // namespace
 
@@ -173,8 +147,8 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     const long long key = t0 + (long long)t * kKT;
     if (!paged) {
       for (int c = ln; c < D / 64; c += nl) {
-        tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128, &tmK, &full[st], c * 64, (int)key, bg);
-        tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128, &tmV, &full[st], c * 64, (int)key, bg);
+        tma_load_3d(sK + st * C::kTile + c * kKT * 128, &tmK, &full[st], c * 64, (int)key, bg);
+        tma_load_3d(sV + st * C::kTile + c * kKT * 128, &tmV, &full[st], c * 64, (int)key, bg);
       }
     } else {
       // boxes of min(bs, 64) rows; a slot beyond the table, or an entry out of range, reads
@@ -195,8 +169,8 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d_plain(sK + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmK, &full[st], c * 64, y, z);
-          tma_load_3d_plain(sV + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmV, &full[st], c * 64, y, z);
+          tma_load_3d(sK + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmK, &full[st], c * 64, y, z);
+          tma_load_3d(sV + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmV, &full[st], c * 64, y, z);
         }
       }
     }
@@ -221,7 +195,7 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
       for (int a = 0; a < kGroups; ++a)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d_plain(sQ + a * C::kQ + c * kGR * 128, &tmQ, qfull, c * 64, g * p.G, (row0 / p.G) + a * npg, b);
+          tma_load_4d(sQ + a * C::kQ + c * kGR * 128, &tmQ, qfull, c * 64, g * p.G, (row0 / p.G) + a * npg, b);
     }
     for (int t = 0; t < pre; ++t) issue_tile(t);
     s_issued = pre;

@@ -125,7 +125,9 @@ struct AcceptParams {
   const float* rmax; const float* rlse; const float* rent; const float* rgap;
   const int32_t* rarg; const float* clog;
   const float* logits;         // [R][V] (rejection)
-  const float* draft;          // [B][N][Vd] (rejection)
+  const float* draft;          // [B][N][Vd], or [n_draft_rows][Vd] with draft_rows (rejection)
+  const int32_t* draft_rows;   // [B][N] node -> row of draft, or nullptr (row b * N + e)
+  int n_draft_rows;
   const int32_t* inv_map;      // [V] target -> draft index, -1 if unmapped; nullptr = identity
   const int32_t* map_bad;      // non-zero when the draft map is invalid
   float* rbuf;                 // [B][2][V] residual buffers (rejection)

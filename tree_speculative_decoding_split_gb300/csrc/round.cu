@@ -19,7 +19,8 @@ struct spec_round {
   cudaGraphExec_t x_part[3];  // attention, verification, compaction (or null)
   cudaStream_t side;
   cudaEvent_t e_fork, e_join;
-  uintptr_t vonly[3][2];      // [lo, hi) of the buffers only the verification reads (but draft_probs)
+  cudaEvent_t e_vin, e_ain;   // the verification's / the attention's input copies are done
+  uintptr_t vonly[5][2];      // [lo, hi) of the buffers only the verification reads (but draft_probs)
   int n_vonly;
   // Rejection with draft distributions: their copies run on `side_d` beside the LM head, and
   // the verification is issued as direct calls whose rejection walk waits for e_draft (a wait
@@ -70,8 +71,10 @@ void release_parts(spec_round* r) {
   if (r->e_fork) cudaEventDestroy(r->e_fork);
   if (r->e_join) cudaEventDestroy(r->e_join);
   if (r->e_draft) cudaEventDestroy(r->e_draft);
+  if (r->e_vin) cudaEventDestroy(r->e_vin);
+  if (r->e_ain) cudaEventDestroy(r->e_ain);
   r->side = r->side_d = nullptr;
-  r->e_fork = r->e_join = r->e_draft = nullptr;
+  r->e_fork = r->e_join = r->e_draft = r->e_vin = r->e_ain = nullptr;
   r->direct_verify = false;
 }
 
@@ -90,7 +93,9 @@ void make_parts(spec_round* r, const spec_attn_args* attn, void* attn_ws, size_t
   bool ok = r->x_part[0] && r->x_part[1] && (!compact || r->x_part[2]) &&
             cudaStreamCreateWithFlags(&r->side, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&r->e_fork, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&r->e_join, cudaEventDisableTiming) == cudaSuccess;
+            cudaEventCreateWithFlags(&r->e_join, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&r->e_vin, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&r->e_ain, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
     release_parts(r);
     cudaGetLastError();
@@ -107,6 +112,9 @@ void make_parts(spec_round* r, const spec_attn_args* attn, void* attn_ws, size_t
   add(verify->hidden_states, rows * verify->hidden * es);
   add(verify->tokens, rows * sizeof(int32_t));
   add(verify->lm_head_weight, (size_t)verify->vocab * verify->hidden * es);
+  const bool compact_draft = verify->rule == SPEC_RULE_REJECTION && verify->draft_rows;
+  if (compact_draft) add(verify->draft_rows, rows * sizeof(int32_t));
+  const size_t draft_bytes = (compact_draft ? (size_t)verify->n_draft_rows : rows) * verify->draft_vocab * sizeof(float);
   if (verify->rule == SPEC_RULE_REJECTION && verify->draft_probs && !verify->draft_ready &&
       cudaStreamCreateWithFlags(&r->side_d, cudaStreamNonBlocking) == cudaSuccess &&
       cudaEventCreateWithFlags(&r->e_draft, cudaEventDisableTiming) == cudaSuccess) {
@@ -117,9 +125,9 @@ void make_parts(spec_round* r, const spec_attn_args* attn, void* attn_ws, size_t
     r->vws_bytes = verify_ws_bytes;
     r->dev_status = dev_status;
     r->draft[0] = reinterpret_cast<uintptr_t>(verify->draft_probs);
-    r->draft[1] = r->draft[0] + rows * (size_t)verify->draft_vocab * sizeof(float);
+    r->draft[1] = r->draft[0] + draft_bytes;
   } else if (verify->rule == SPEC_RULE_REJECTION && verify->draft_probs) {
-    add(verify->draft_probs, rows * (size_t)verify->draft_vocab * sizeof(float));
+    add(verify->draft_probs, draft_bytes);
   }
   cudaGetLastError();
 }
@@ -254,6 +262,11 @@ extern "C" spec_status spec_round_launch_host(const spec_round* round, const spe
     // runs the verification beside the attention; the compaction and the result copies follow
     // both.  The side stream starts after everything enqueued on `s` so far (the previous
     // round included), so no copy overwrites a buffer still being read.
+    // The copy groups take the host link one after another rather than sharing it, so that each
+    // consumer starts as early as it can: the verification's inputs first (its LM head is
+    // issued first and holds the SMs it needs; the attention fills the rest and follows), then
+    // the attention's inputs, then the draft distributions, which only the rejection walk at
+    // the end of the verification reads.
     auto extent = [](const spec_host_copy& c, uintptr_t& lo, uintptr_t& hi) {
       lo = reinterpret_cast<uintptr_t>(c.device);
       hi = lo + (c.rows > 1 ? (size_t)(c.rows - 1) * c.device_pitch : 0) + c.row_bytes;
@@ -267,24 +280,30 @@ extern "C" spec_status spec_round_launch_host(const spec_round* round, const spe
         if (lo >= round->vonly[k][0] && hi <= round->vonly[k][1]) return 1;
       return 0;
     };
-    if (cudaEventRecord(round->e_fork, s) != cudaSuccess || cudaStreamWaitEvent(round->side, round->e_fork, 0) != cudaSuccess ||
-        (round->direct_verify && cudaStreamWaitEvent(round->side_d, round->e_fork, 0) != cudaSuccess))
+    if (cudaEventRecord(round->e_fork, s) != cudaSuccess || cudaStreamWaitEvent(round->side, round->e_fork, 0) != cudaSuccess)
       return SPEC_ERR_CUDA;
-    for (int32_t i = 0; i < n_inputs; ++i) {
-      const int q = route(inputs[i]);
-      if (enqueue_copy(inputs[i], true, q == 0 ? s : (q == 1 ? round->side : round->side_d)) != cudaSuccess)
-        return SPEC_ERR_CUDA;
-    }
+    auto copies = [&](int group, cudaStream_t on) {
+      for (int32_t i = 0; i < n_inputs; ++i)
+        if (route(inputs[i]) == group && enqueue_copy(inputs[i], true, on) != cudaSuccess) return false;
+      return true;
+    };
+    if (!copies(1, round->side) || cudaEventRecord(round->e_vin, round->side) != cudaSuccess ||
+        cudaStreamWaitEvent(s, round->e_vin, 0) != cudaSuccess || !copies(0, s))
+      return SPEC_ERR_CUDA;
+    if (round->direct_verify &&
+        (cudaEventRecord(round->e_ain, s) != cudaSuccess || cudaStreamWaitEvent(round->side_d, round->e_ain, 0) != cudaSuccess ||
+         !copies(2, round->side_d)))
+      return SPEC_ERR_CUDA;
     // the draft distributions are complete once e_draft (recorded after their copies, before the
     // walk's wait is enqueued) completes
     if (round->direct_verify && cudaEventRecord(round->e_draft, round->side_d) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (cudaGraphLaunch(round->x_part[0], s) != cudaSuccess) return SPEC_ERR_CUDA;
     if (round->direct_verify) {
       const spec_status vs = spec_verify_accept(&round->vargs, round->vws, round->vws_bytes, round->dev_status, round->side);
       if (vs != SPEC_OK) return vs;
     } else if (cudaGraphLaunch(round->x_part[1], round->side) != cudaSuccess) {
       return SPEC_ERR_CUDA;
     }
+    if (cudaGraphLaunch(round->x_part[0], s) != cudaSuccess) return SPEC_ERR_CUDA;
     if (cudaEventRecord(round->e_join, round->side) != cudaSuccess || cudaStreamWaitEvent(s, round->e_join, 0) != cudaSuccess)
       return SPEC_ERR_CUDA;
     if (round->x_part[2] && cudaGraphLaunch(round->x_part[2], s) != cudaSuccess) return SPEC_ERR_CUDA;
