@@ -95,3 +95,28 @@ def test_expanded_tree_feeds_typical_acceptance():
     ref = H.oracle_verify(case)
     c = H.check_verify(case, out, ref)
     assert c.exact + c.excluded == 2
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("topk_heads", [(12, 8, 3), (8, 5, 3)])
+def test_plateaus_and_constant_rows(dtype, topk_heads):
+    """Rows whose top values tie over hundreds of entries: a constant head (every chunk takes the
+    per-warp register path, since more keys reach the threshold than shared memory gathers), a
+    head with a 700-entry plateau at its maximum, and a random head; k above 8 (threshold from
+    the threads' maxima) and k = 8 (from the warps' maxima)."""
+    rng = np.random.default_rng(11)
+    B, V = 2, 128256
+    k = max(topk_heads)
+    x = rng.standard_normal((B, 3, V)).astype(np.float32)
+    x[:, 0] = 0.5
+    x[:, 1, 4000:4700] = 9.0
+    x[1, 1, 70001:70301] = 9.0
+    xs = BF.f32_to_bf16_bits(x) if dtype == "bf16" else x
+    parent, rank = st.medusa_topology(topk_heads, 60)
+    got = _run(xs, dtype, parent, rank, k)
+    assert got["status"] == 0
+    xf = BF.bf16_bits_to_f64(xs) if dtype == "bf16" else xs.astype(np.float64)
+    tokens, idx = oracle.medusa_expand(xf, parent, rank, k)
+    assert (got["topk_index"] == idx).all()
+    assert (got["tokens"] == tokens).all()
+    assert idx[0, 0].tolist() == list(range(k))  # a constant row: the lowest ids

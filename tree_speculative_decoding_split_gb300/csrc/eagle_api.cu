@@ -42,7 +42,7 @@ spec_status spec_eagle_expand(const spec_eagle_expand_args* a, void* workspace, 
   m.B = a->batch; m.K = a->frontier; m.V = a->draft_vocab; m.N = 1; m.k = a->topk;
   m.is_bf16 = 0;
   m.n_chunks = eagle_chunks(a->draft_vocab);
-  m.chunk = (a->draft_vocab + m.n_chunks - 1) / m.n_chunks;
+  m.chunk = spectree::topk_chunk_len(a->draft_vocab, m.n_chunks);
   m.logits = a->logp;
   m.cand = static_cast<unsigned long long*>(workspace);
   m.dev_status = dev_status;

@@ -186,6 +186,7 @@ struct MedusaParams {
   int32_t* dev_status;
 };
 int medusa_chunks(int B, int K, int V, int k, int num_sms);
+int topk_chunk_len(int V, int n_chunks);
 void launch_medusa(const MedusaParams& p, cudaStream_t stream);
 // K5a alone: per-row chunk top-k keys of p.logits [p.B * p.K][p.V] into p.cand.
 void launch_row_topk_chunks(const MedusaParams& p, cudaStream_t stream);

@@ -5,10 +5,11 @@
 // node at depth d >= 1 with rank r carries the r-th best token of head d - 1.
 //
 // K5a: per (request, head, vocabulary chunk) top-k over 64-bit order keys (value, then the lower
-// token id) held in registers: every warp takes its own top-k by k rounds of a warp-wide maximum
-// below the previous winner, then one warp merges the warps' candidates the same way.  K5b: per request, the chunk
-// candidates of every head merge into the head's top-k (one warp per head, the heads side by
-// side), the topology is validated and every node's token is looked up.
+// token id) held in registers: a threshold taken from the threads' own maxima narrows the chunk
+// to a few candidates, whose top-k one warp takes by k rounds of a warp-wide maximum below the
+// previous winner.  K5b: per request, the chunk candidates of every head merge into the head's
+// top-k (one warp per head, the heads side by side), the topology is validated and every node's
+// token is looked up.
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -55,49 +56,161 @@ __device__ __forceinline__ unsigned long long warp_max_below(const unsigned long
   return warp_max_u64(m);
 }
 
-}  // namespace
-
-// K5a: grid (n_chunks, B * K).  Writes k keys per (row, chunk), best first (0 = none).
-__global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const MedusaParams p) {
-  constexpr int kWarps = kMxThreads / 32;
-  __shared__ unsigned long long s_cand[kWarps * kMaxTopk];  // [warp][rank]
-  const int chunk = blockIdx.x, row = blockIdx.y;  // row = b * K + head
-  const int v0 = chunk * p.chunk;
-  const int v1 = min(p.V, v0 + p.chunk);
-  unsigned long long keys[kMxEpt];
+// The kMxEpt keys of this thread in the chunk [v0, v1) of logits row `row` (0 for entries past
+// the chunk).  With rows and chunk starts on 16-byte boundaries a thread reads 16-byte vectors
+// (8 bf16 or 4 fp32 neighbours each); otherwise single entries, the threads side by side.
+__device__ __forceinline__ void load_keys(const MedusaParams& p, int row, int v0, int v1,
+                                          unsigned long long (&keys)[kMxEpt]) {
+  const int tid = threadIdx.x;
+  const size_t rb = (size_t)row * p.V;
+  const bool aligned = (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0;
+  if (p.is_bf16 && aligned && (p.V & 7) == 0 && (p.chunk & 7) == 0) {
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.logits) + rb;
+#pragma unroll
+    for (int h = 0; h < kMxEpt / 8; ++h) {
+      const int base = v0 + (h * kMxThreads + tid) * 8;
+      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      if (base + 8 <= v1) u = *reinterpret_cast<const uint4*>(x + base);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float f = __uint_as_float((i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16));
+        keys[h * 8 + i] = base + 8 <= v1 ? topk_key(f, base + i) : 0ull;
+      }
+    }
+    return;
+  }
+  if (!p.is_bf16 && aligned && (p.V & 3) == 0 && (p.chunk & 3) == 0) {
+    const float* x = static_cast<const float*>(p.logits) + rb;
+#pragma unroll
+    for (int h = 0; h < kMxEpt / 4; ++h) {
+      const int base = v0 + (h * kMxThreads + tid) * 4;
+      float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (base + 4 <= v1) u = *reinterpret_cast<const float4*>(x + base);
+      const float f[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) keys[h * 4 + i] = base + 4 <= v1 ? topk_key(f[i], base + i) : 0ull;
+    }
+    return;
+  }
 #pragma unroll
   for (int e = 0; e < kMxEpt; ++e) {
-    const int v = v0 + e * kMxThreads + (int)threadIdx.x;
+    const int v = v0 + e * kMxThreads + tid;
     float f = 0.f;
-    bool in = v < v1;
+    const bool in = v < v1;
     if (in) {
       if (p.is_bf16)
-        f = __bfloat162float(static_cast<const __nv_bfloat16*>(p.logits)[(size_t)row * p.V + v]);
+        f = __bfloat162float(static_cast<const __nv_bfloat16*>(p.logits)[rb + v]);
       else
-        f = static_cast<const float*>(p.logits)[(size_t)row * p.V + v];
+        f = static_cast<const float*>(p.logits)[rb + v];
     }
     keys[e] = in ? topk_key(f, v) : 0ull;
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+}
+
+}  // namespace
+
+// K5a: grid (n_chunks, B * K).  Writes k keys per (row, chunk), best first (0 = none).
+// The chunk's top k by a threshold T with at least k distinct keys at or above it, so that the
+// chunk's top k all reach it: for k <= 8 the k-th largest of the eight warps' maxima (every
+// thread finds it among those eight), above that the k-th largest of the threads' own maxima
+// (warp 0, k rounds of a warp-wide maximum below the previous winner).  The keys that reach T --
+// a few times k of them on the benchmark's rows -- are gathered in shared memory and each finds
+// its rank by counting the larger ones; ranks below k are the result.  When more than kMxThreads
+// keys reach T (a chunk of many equal values) every warp instead takes its own top k from
+// registers by warp-wide rounds and warp 0 merges the warps' candidates.  Either way the result
+// is the top k of one strict order (value, then the lower token id).
+__global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const MedusaParams p) {
+  constexpr int kWarps = kMxThreads / 32;
+  constexpr int kPer = kMxThreads / 32;  // keys per lane when warp 0 scans kMxThreads of them
+  __shared__ unsigned long long s_keys[kMxThreads];         // thread maxima, then the candidates
+  __shared__ unsigned long long s_wmax[kWarps];
+  __shared__ unsigned long long s_cand[kWarps * kMaxTopk];  // fallback: [warp][rank]
+  __shared__ unsigned long long s_thr;
+  __shared__ int s_n;
+  const int chunk = blockIdx.x, row = blockIdx.y;  // row = b * K + head
+  const int v0 = chunk * p.chunk;
+  const int v1 = min(p.V, v0 + p.chunk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned long long keys[kMxEpt];
+  load_keys(p, row, v0, v1, keys);
+  unsigned long long mx = 0ull;
+#pragma unroll
+  for (int e = 0; e < kMxEpt; ++e) mx = keys[e] > mx ? keys[e] : mx;
+  const bool small_k = p.k <= kWarps;
+  if (small_k) {
+    const unsigned long long wm = warp_max_u64(mx);
+    if (lane == 0) s_wmax[warp] = wm;
+  } else {
+    s_keys[tid] = mx;
+  }
+  if (tid == 0) s_n = 0;
+  __syncthreads();
+  unsigned long long thr;
+  if (small_k) {  // the k-th largest of the warp maxima (0 when fewer than k warps hold a key)
+    // the largest warp maximum with at least k of them at or above it
+    unsigned long long w[kWarps];
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) w[i] = s_wmax[i];
+    thr = 0ull;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+      int ge = 0;
+#pragma unroll
+      for (int j = 0; j < kWarps; ++j) ge += w[j] >= w[i];
+      if (ge >= p.k && w[i] > thr) thr = w[i];
+    }
+  } else {  // the k-th largest thread maximum (0 when fewer than k threads hold a key)
+    if (warp == 0) {
+      unsigned long long c[kPer];
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) c[e] = s_keys[lane + 32 * e];
+      unsigned long long below = ~0ull;
+      for (int r = 0; r < p.k; ++r) below = warp_max_below(c, kPer, below);
+      if (lane == 0) s_thr = below;
+    }
+    __syncthreads();  // every read of the maxima is done: s_keys now collects the candidates
+    thr = s_thr;
+  }
+#pragma unroll
+  for (int e = 0; e < kMxEpt; ++e)
+    if (keys[e] != 0ull && keys[e] >= thr) {
+      const int i = atomicAdd(&s_n, 1);
+      if (i < kMxThreads) s_keys[i] = keys[e];
+    }
+  __syncthreads();
+  const int n = s_n;
+  unsigned long long* out = p.cand + ((size_t)row * p.n_chunks + chunk) * p.k;
+  if (n <= kMxThreads) {
+    if (tid < n) {  // keys are distinct, so the ranks are
+      const unsigned long long c = s_keys[tid];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += s_keys[j] > c;
+      if (rank < p.k) out[rank] = c;
+    } else if (tid < p.k) {
+      out[tid] = 0ull;  // fewer than k keys in the chunk
+    }
+    return;
+  }
+  // many keys tie at the threshold: per-warp top k from registers, then warp 0 merges
   unsigned long long below = ~0ull;
-  for (int r = 0; r < p.k; ++r) {  // this warp's top-k
+  for (int r = 0; r < p.k; ++r) {
     below = warp_max_below(keys, kMxEpt, below);
     if (lane == 0) s_cand[warp * kMaxTopk + r] = below;  // 0 once the warp's keys are exhausted
   }
   __syncthreads();
   if (warp == 0) {  // the chunk's top-k among the warps' candidates (kWarps * k <= 256)
-    constexpr int kPer = kWarps * kMaxTopk / 32;
-    unsigned long long c[kPer];
+    constexpr int kPerC = kWarps * kMaxTopk / 32;
+    unsigned long long c[kPerC];
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) {
+    for (int e = 0; e < kPerC; ++e) {
       const int j = lane + 32 * e, w = j / kMaxTopk, r = j % kMaxTopk;
       c[e] = (r < p.k) ? s_cand[w * kMaxTopk + r] : 0ull;
     }
-    unsigned long long* out = p.cand + ((size_t)row * p.n_chunks + chunk) * p.k;
     below = ~0ull;
     for (int r = 0; r < p.k; ++r) {
-      below = warp_max_below(c, kPer, below);
-      if (lane == 0) out[r] = below;  // 0 once the chunk is exhausted
+      below = warp_max_below(c, kPerC, below);
+      if (lane == 0) out[r] = below;
     }
   }
 }
@@ -181,6 +294,14 @@ int medusa_chunks(int B, int K, int V, int k, int num_sms) {
   if (want > cap) want = cap;
   if (want < min_chunks) want = min_chunks;
   return want < 1 ? 1 : want;
+}
+
+// Entries per chunk for n_chunks chunks of a V-entry row: rounded up to 8 entries so that chunk
+// starts stay on 16-byte boundaries (vector loads); at most kMxThreads * kMxEpt whenever n_chunks
+// covers the row at that length.  Trailing chunks may be short or empty.
+int topk_chunk_len(int V, int n_chunks) {
+  const int len = (V + n_chunks - 1) / n_chunks;
+  return (len + 7) & ~7;
 }
 
 void launch_row_topk_chunks(const MedusaParams& p, cudaStream_t stream) {

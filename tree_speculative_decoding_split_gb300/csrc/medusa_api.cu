@@ -53,7 +53,7 @@ spec_status spec_medusa_expand(const spec_medusa_args* a, void* workspace, size_
   p.B = a->batch; p.K = a->num_heads; p.V = a->vocab; p.N = a->n_nodes; p.k = a->topk;
   p.is_bf16 = a->dtype == SPEC_DTYPE_BF16;
   p.n_chunks = spectree::medusa_chunks(p.B, p.K, p.V, p.k, num_sms_here());
-  p.chunk = (p.V + p.n_chunks - 1) / p.n_chunks;
+  p.chunk = spectree::topk_chunk_len(p.V, p.n_chunks);
   const size_t need = (size_t)p.B * p.K * p.n_chunks * p.k * sizeof(unsigned long long);
   if (workspace_bytes < need) return SPEC_ERR_WORKSPACE_TOO_SMALL;
   p.logits = a->head_logits;
