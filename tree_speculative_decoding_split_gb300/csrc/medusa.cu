@@ -22,16 +22,14 @@ constexpr int kMxThreads = 256;
 constexpr int kMxEpt = 16;  // vocabulary entries per thread in K5a (chunk <= 4096)
 
 // Order key: larger is better.  Values order as floats (-0 = +0, NaN below -inf); equal values
-// order by the lower token id.
-__device__ __forceinline__ unsigned long long topk_key(float f, int v) {
-  uint32_t u;
-  if (f != f) {
-    u = 0u;
-  } else {
-    const uint32_t b = __float_as_uint(f == 0.f ? 0.f : f);
-    u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    if (u == 0u) u = 1u;  // keep 0 for NaN
-  }
+// order by the lower token id.  The upper half (order_u) alone orders the values.
+__device__ __forceinline__ uint32_t order_u(float f) {
+  if (f != f) return 0u;
+  const uint32_t b = __float_as_uint(f == 0.f ? 0.f : f);
+  const uint32_t u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return u == 0u ? 1u : u;  // keep 0 for NaN
+}
+__device__ __forceinline__ unsigned long long order_key(uint32_t u, int v) {
   return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)v);
 }
 __device__ __forceinline__ int key_token(unsigned long long k) {
@@ -56,128 +54,130 @@ __device__ __forceinline__ unsigned long long warp_max_below(const unsigned long
   return warp_max_u64(m);
 }
 
-// The kMxEpt keys of this thread in the chunk [v0, v1) of logits row `row` (0 for entries past
-// the chunk).  With rows and chunk starts on 16-byte boundaries a thread reads 16-byte vectors
-// (8 bf16 or 4 fp32 neighbours each); otherwise single entries, the threads side by side.
-__device__ __forceinline__ void load_keys(const MedusaParams& p, int row, int v0, int v1,
-                                          unsigned long long (&keys)[kMxEpt]) {
+// Where this thread's entries lie in its chunk: with rows and chunk starts on 16-byte boundaries
+// a thread reads 16-byte vectors (8 bf16 or 4 fp32 neighbours each), the threads side by side;
+// otherwise single entries.  Entry e of thread t is token v0 + entry_offset(mode, t, e).
+enum { kLoadScalar = 0, kLoadVec4 = 4, kLoadVec8 = 8 };
+__device__ __forceinline__ int load_mode(const MedusaParams& p) {
+  const bool aligned = (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0;
+  if (p.is_bf16 && aligned && (p.V & 7) == 0 && (p.chunk & 7) == 0) return kLoadVec8;
+  if (!p.is_bf16 && aligned && (p.V & 3) == 0 && (p.chunk & 3) == 0) return kLoadVec4;
+  return kLoadScalar;
+}
+__device__ __forceinline__ int entry_offset(int mode, int t, int e) {
+  if (mode == kLoadVec8) return ((e >> 3) * kMxThreads + t) * 8 + (e & 7);
+  if (mode == kLoadVec4) return ((e >> 2) * kMxThreads + t) * 4 + (e & 3);
+  return e * kMxThreads + t;
+}
+
+// The order values (order_u) of this thread's kMxEpt entries in the chunk [v0, v1) of logits row
+// `row`; 0 for entries past the chunk (callers tell them from NaN by the token).
+__device__ __forceinline__ void load_order(const MedusaParams& p, int mode, int row, int v0, int v1,
+                                           uint32_t (&u)[kMxEpt]) {
   const int tid = threadIdx.x;
   const size_t rb = (size_t)row * p.V;
-  const bool aligned = (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0;
-  if (p.is_bf16 && aligned && (p.V & 7) == 0 && (p.chunk & 7) == 0) {
+  if (mode == kLoadVec8) {
     const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.logits) + rb;
 #pragma unroll
     for (int h = 0; h < kMxEpt / 8; ++h) {
-      const int base = v0 + (h * kMxThreads + tid) * 8;
-      uint4 u = make_uint4(0u, 0u, 0u, 0u);
-      if (base + 8 <= v1) u = *reinterpret_cast<const uint4*>(x + base);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      const int base = v0 + entry_offset(mode, tid, h * 8);
+      const bool in = base + 8 <= v1;  // v1 is a multiple of 8 here
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (in) w = *reinterpret_cast<const uint4*>(x + base);
+      const uint32_t q[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float f = __uint_as_float((i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16));
-        keys[h * 8 + i] = base + 8 <= v1 ? topk_key(f, base + i) : 0ull;
+        const float f = __uint_as_float((i & 1) ? (q[i >> 1] & 0xFFFF0000u) : (q[i >> 1] << 16));
+        u[h * 8 + i] = in ? order_u(f) : 0u;
       }
     }
     return;
   }
-  if (!p.is_bf16 && aligned && (p.V & 3) == 0 && (p.chunk & 3) == 0) {
+  if (mode == kLoadVec4) {
     const float* x = static_cast<const float*>(p.logits) + rb;
 #pragma unroll
     for (int h = 0; h < kMxEpt / 4; ++h) {
-      const int base = v0 + (h * kMxThreads + tid) * 4;
-      float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (base + 4 <= v1) u = *reinterpret_cast<const float4*>(x + base);
-      const float f[4] = {u.x, u.y, u.z, u.w};
+      const int base = v0 + entry_offset(mode, tid, h * 4);
+      const bool in = base + 4 <= v1;  // v1 is a multiple of 4 here
+      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (in) w = *reinterpret_cast<const float4*>(x + base);
+      const float f[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) keys[h * 4 + i] = base + 4 <= v1 ? topk_key(f[i], base + i) : 0ull;
+      for (int i = 0; i < 4; ++i) u[h * 4 + i] = in ? order_u(f[i]) : 0u;
     }
     return;
   }
 #pragma unroll
   for (int e = 0; e < kMxEpt; ++e) {
-    const int v = v0 + e * kMxThreads + tid;
-    float f = 0.f;
-    const bool in = v < v1;
-    if (in) {
-      if (p.is_bf16)
-        f = __bfloat162float(static_cast<const __nv_bfloat16*>(p.logits)[rb + v]);
-      else
-        f = static_cast<const float*>(p.logits)[rb + v];
-    }
-    keys[e] = in ? topk_key(f, v) : 0ull;
+    const int v = v0 + entry_offset(mode, tid, e);
+    u[e] = 0u;
+    if (v < v1)
+      u[e] = order_u(p.is_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.logits)[rb + v])
+                               : static_cast<const float*>(p.logits)[rb + v]);
   }
 }
 
 }  // namespace
 
 // K5a: grid (n_chunks, B * K).  Writes k keys per (row, chunk), best first (0 = none).
-// The chunk's top k by a threshold T with at least k distinct keys at or above it, so that the
-// chunk's top k all reach it: for k <= 8 the k-th largest of the eight warps' maxima (every
-// thread finds it among those eight), above that the k-th largest of the threads' own maxima
-// (warp 0, k rounds of a warp-wide maximum below the previous winner).  The keys that reach T --
-// a few times k of them on the benchmark's rows -- are gathered in shared memory and each finds
-// its rank by counting the larger ones; ranks below k are the result.  When more than kMxThreads
-// keys reach T (a chunk of many equal values) every warp instead takes its own top k from
-// registers by warp-wide rounds and warp 0 merges the warps' candidates.  Either way the result
-// is the top k of one strict order (value, then the lower token id).
+// The chunk's top k by a threshold T on the order values with at least k entries at or above it,
+// so that the chunk's top k all reach it.  With j = ceil(k / 8), every warp finds the j-th
+// largest of its threads' maxima (counting repeats: a warp-wide maximum and a ballot per round),
+// and T is the ceil(k / j)-th largest of those eight, so that ceil(k / j) warps hold j entries
+// each at or above it.  The entries that reach T -- a few times k of them on the benchmark's rows
+// -- become 64-bit keys in shared memory and each finds its rank by counting the larger ones;
+// ranks below k are the result.  When more than kMxThreads entries reach T (a chunk of many
+// equal values) every warp instead takes its own top k from registers by k rounds of a
+// warp-wide maximum below the previous winner, and warp 0 merges the warps' candidates.  Either
+// way the result is the top k of one strict order (value, then the lower token id).
 __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const MedusaParams p) {
   constexpr int kWarps = kMxThreads / 32;
-  constexpr int kPer = kMxThreads / 32;  // keys per lane when warp 0 scans kMxThreads of them
-  __shared__ unsigned long long s_keys[kMxThreads];         // thread maxima, then the candidates
-  __shared__ unsigned long long s_wmax[kWarps];
+  __shared__ unsigned long long s_keys[kMxThreads];         // the candidates
+  __shared__ uint32_t s_wv[kWarps];
   __shared__ unsigned long long s_cand[kWarps * kMaxTopk];  // fallback: [warp][rank]
-  __shared__ unsigned long long s_thr;
   __shared__ int s_n;
   const int chunk = blockIdx.x, row = blockIdx.y;  // row = b * K + head
   const int v0 = chunk * p.chunk;
   const int v1 = min(p.V, v0 + p.chunk);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  unsigned long long keys[kMxEpt];
-  load_keys(p, row, v0, v1, keys);
-  unsigned long long mx = 0ull;
+  const int mode = load_mode(p);
+  uint32_t u[kMxEpt];
+  load_order(p, mode, row, v0, v1, u);
+  uint32_t um = 0u;
 #pragma unroll
-  for (int e = 0; e < kMxEpt; ++e) mx = keys[e] > mx ? keys[e] : mx;
-  const bool small_k = p.k <= kWarps;
-  if (small_k) {
-    const unsigned long long wm = warp_max_u64(mx);
-    if (lane == 0) s_wmax[warp] = wm;
-  } else {
-    s_keys[tid] = mx;
+  for (int e = 0; e < kMxEpt; ++e) um = max(um, u[e]);
+  // the warp's j-th largest thread maximum, repeats counted (0 once the maxima run out)
+  const int j = (p.k + kWarps - 1) / kWarps;
+  uint32_t wv = 0u, prev = 0xFFFFFFFFu;
+  for (int have = 0, r = 0; r < j && have < j; ++r) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, um < prev ? um : 0u);
+    have += __popc(__ballot_sync(0xffffffffu, um == m));
+    wv = m;
+    prev = m;
+    if (m == 0u) break;
   }
+  if (lane == 0) s_wv[warp] = wv;
   if (tid == 0) s_n = 0;
   __syncthreads();
-  unsigned long long thr;
-  if (small_k) {  // the k-th largest of the warp maxima (0 when fewer than k warps hold a key)
-    // the largest warp maximum with at least k of them at or above it
-    unsigned long long w[kWarps];
+  // T: the largest warp value with at least ceil(k / j) of the eight at or above it
+  const int need = (p.k + j - 1) / j;
+  uint32_t thr = 0u;
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i) w[i] = s_wmax[i];
-    thr = 0ull;
+  for (int i = 0; i < kWarps; ++i) {
+    const uint32_t w = s_wv[i];
+    int ge = 0;
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i) {
-      int ge = 0;
-#pragma unroll
-      for (int j = 0; j < kWarps; ++j) ge += w[j] >= w[i];
-      if (ge >= p.k && w[i] > thr) thr = w[i];
-    }
-  } else {  // the k-th largest thread maximum (0 when fewer than k threads hold a key)
-    if (warp == 0) {
-      unsigned long long c[kPer];
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) c[e] = s_keys[lane + 32 * e];
-      unsigned long long below = ~0ull;
-      for (int r = 0; r < p.k; ++r) below = warp_max_below(c, kPer, below);
-      if (lane == 0) s_thr = below;
-    }
-    __syncthreads();  // every read of the maxima is done: s_keys now collects the candidates
-    thr = s_thr;
+    for (int q = 0; q < kWarps; ++q) ge += s_wv[q] >= w;
+    if (ge >= need && w > thr) thr = w;
   }
 #pragma unroll
-  for (int e = 0; e < kMxEpt; ++e)
-    if (keys[e] != 0ull && keys[e] >= thr) {
+  for (int e = 0; e < kMxEpt; ++e) {
+    const int v = v0 + entry_offset(mode, tid, e);
+    if (v < v1 && u[e] >= thr) {
       const int i = atomicAdd(&s_n, 1);
-      if (i < kMxThreads) s_keys[i] = keys[e];
+      if (i < kMxThreads) s_keys[i] = order_key(u[e], v);
     }
+  }
   __syncthreads();
   const int n = s_n;
   unsigned long long* out = p.cand + ((size_t)row * p.n_chunks + chunk) * p.k;
@@ -185,14 +185,20 @@ __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const Med
     if (tid < n) {  // keys are distinct, so the ranks are
       const unsigned long long c = s_keys[tid];
       int rank = 0;
-      for (int j = 0; j < n; ++j) rank += s_keys[j] > c;
+      for (int q = 0; q < n; ++q) rank += s_keys[q] > c;
       if (rank < p.k) out[rank] = c;
     } else if (tid < p.k) {
-      out[tid] = 0ull;  // fewer than k keys in the chunk
+      out[tid] = 0ull;  // fewer than k entries in the chunk
     }
     return;
   }
-  // many keys tie at the threshold: per-warp top k from registers, then warp 0 merges
+  // many entries tie at the threshold: per-warp top k from registers, then warp 0 merges
+  unsigned long long keys[kMxEpt];
+#pragma unroll
+  for (int e = 0; e < kMxEpt; ++e) {
+    const int v = v0 + entry_offset(mode, tid, e);
+    keys[e] = v < v1 ? order_key(u[e], v) : 0ull;
+  }
   unsigned long long below = ~0ull;
   for (int r = 0; r < p.k; ++r) {
     below = warp_max_below(keys, kMxEpt, below);
@@ -204,7 +210,7 @@ __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const Med
     unsigned long long c[kPerC];
 #pragma unroll
     for (int e = 0; e < kPerC; ++e) {
-      const int j = lane + 32 * e, w = j / kMaxTopk, r = j % kMaxTopk;
+      const int q = lane + 32 * e, w = q / kMaxTopk, r = q % kMaxTopk;
       c[e] = (r < p.k) ? s_cand[w * kMaxTopk + r] : 0ull;
     }
     below = ~0ull;
