@@ -29,6 +29,9 @@ __device__ __forceinline__ uint32_t order_u(float f) {
   const uint32_t u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
   return u == 0u ? 1u : u;  // keep 0 for NaN
 }
+__device__ __forceinline__ float order_value(uint32_t u) {  // the value order_u maps to u (u >= 1)
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
 __device__ __forceinline__ unsigned long long order_key(uint32_t u, int v) {
   return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)v);
 }
@@ -70,50 +73,48 @@ __device__ __forceinline__ int entry_offset(int mode, int t, int e) {
   return e * kMxThreads + t;
 }
 
-// The order values (order_u) of this thread's kMxEpt entries in the chunk [v0, v1) of logits row
-// `row`; 0 for entries past the chunk (callers tell them from NaN by the token).
-__device__ __forceinline__ void load_order(const MedusaParams& p, int mode, int row, int v0, int v1,
-                                           uint32_t (&u)[kMxEpt]) {
+// The values of this thread's kMxEpt entries in the chunk [v0, v1) of logits row `row`, as
+// floats; NaN for entries past the chunk (callers tell them from NaN logits by the token).
+__device__ __forceinline__ void load_vals(const MedusaParams& p, int mode, int row, int v0, int v1,
+                                          float (&x)[kMxEpt]) {
   const int tid = threadIdx.x;
   const size_t rb = (size_t)row * p.V;
+  const float nan = __uint_as_float(0x7FFFFFFFu);
   if (mode == kLoadVec8) {
-    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.logits) + rb;
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.logits) + rb;
 #pragma unroll
     for (int h = 0; h < kMxEpt / 8; ++h) {
       const int base = v0 + entry_offset(mode, tid, h * 8);
-      const bool in = base + 8 <= v1;  // v1 is a multiple of 8 here
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (in) w = *reinterpret_cast<const uint4*>(x + base);
+      uint4 w = make_uint4(0x7FFF7FFFu, 0x7FFF7FFFu, 0x7FFF7FFFu, 0x7FFF7FFFu);  // bf16 NaNs
+      if (base + 8 <= v1) w = *reinterpret_cast<const uint4*>(src + base);  // v1 is a multiple of 8 here
       const uint32_t q[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float f = __uint_as_float((i & 1) ? (q[i >> 1] & 0xFFFF0000u) : (q[i >> 1] << 16));
-        u[h * 8 + i] = in ? order_u(f) : 0u;
-      }
+      for (int i = 0; i < 8; ++i)
+        x[h * 8 + i] = __uint_as_float((i & 1) ? (q[i >> 1] & 0xFFFF0000u) : (q[i >> 1] << 16));
     }
     return;
   }
   if (mode == kLoadVec4) {
-    const float* x = static_cast<const float*>(p.logits) + rb;
+    const float* src = static_cast<const float*>(p.logits) + rb;
 #pragma unroll
     for (int h = 0; h < kMxEpt / 4; ++h) {
       const int base = v0 + entry_offset(mode, tid, h * 4);
-      const bool in = base + 4 <= v1;  // v1 is a multiple of 4 here
-      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (in) w = *reinterpret_cast<const float4*>(x + base);
-      const float f[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) u[h * 4 + i] = in ? order_u(f[i]) : 0u;
+      float4 w = make_float4(nan, nan, nan, nan);
+      if (base + 4 <= v1) w = *reinterpret_cast<const float4*>(src + base);  // v1 is a multiple of 4 here
+      x[h * 4 + 0] = w.x;
+      x[h * 4 + 1] = w.y;
+      x[h * 4 + 2] = w.z;
+      x[h * 4 + 3] = w.w;
     }
     return;
   }
 #pragma unroll
   for (int e = 0; e < kMxEpt; ++e) {
     const int v = v0 + entry_offset(mode, tid, e);
-    u[e] = 0u;
+    x[e] = nan;
     if (v < v1)
-      u[e] = order_u(p.is_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.logits)[rb + v])
-                               : static_cast<const float*>(p.logits)[rb + v]);
+      x[e] = p.is_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.logits)[rb + v])
+                       : static_cast<const float*>(p.logits)[rb + v];
   }
 }
 
@@ -141,11 +142,12 @@ __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const Med
   const int v1 = min(p.V, v0 + p.chunk);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mode = load_mode(p);
-  uint32_t u[kMxEpt];
-  load_order(p, mode, row, v0, v1, u);
-  uint32_t um = 0u;
+  float x[kMxEpt];
+  load_vals(p, mode, row, v0, v1, x);
+  float xm = x[0];
 #pragma unroll
-  for (int e = 0; e < kMxEpt; ++e) um = max(um, u[e]);
+  for (int e = 1; e < kMxEpt; ++e) xm = fmaxf(xm, x[e]);  // NaN only if every entry is NaN
+  const uint32_t um = order_u(xm);
   // the warp's j-th largest thread maximum, repeats counted (0 once the maxima run out)
   const int j = (p.k + kWarps - 1) / kWarps;
   uint32_t wv = 0u, prev = 0xFFFFFFFFu;
@@ -170,12 +172,16 @@ __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const Med
     for (int q = 0; q < kWarps; ++q) ge += s_wv[q] >= w;
     if (ge >= need && w > thr) thr = w;
   }
+  // order_u(x) >= thr exactly when x >= the value thr stands for (x not NaN); at thr = 0 every
+  // entry of the chunk, NaN included, is a candidate
+  const bool all = thr == 0u;
+  const float tf = order_value(thr);
 #pragma unroll
   for (int e = 0; e < kMxEpt; ++e) {
     const int v = v0 + entry_offset(mode, tid, e);
-    if (v < v1 && u[e] >= thr) {
+    if (v < v1 && (all || x[e] >= tf)) {
       const int i = atomicAdd(&s_n, 1);
-      if (i < kMxThreads) s_keys[i] = order_key(u[e], v);
+      if (i < kMxThreads) s_keys[i] = order_key(order_u(x[e]), v);
     }
   }
   __syncthreads();
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const Med
 #pragma unroll
   for (int e = 0; e < kMxEpt; ++e) {
     const int v = v0 + entry_offset(mode, tid, e);
-    keys[e] = v < v1 ? order_key(u[e], v) : 0ull;
+    keys[e] = v < v1 ? order_key(order_u(x[e]), v) : 0ull;
   }
   unsigned long long below = ~0ull;
   for (int r = 0; r < p.k; ++r) {
