@@ -482,15 +482,16 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
                                            f"{t['draft'].shape[1]} fp32, indexed by draft_rows [B][N]"),
                    "l2": "flushed before every step (256 MB write, then read)",
                    "launch": ("one CUDA-graph launch of the captured round per step (spec_round_launch; "
-                              "tree attention and verification as parallel branches, compaction after both)"
+                              "tree attention and verification as parallel branches, the longer one first, "
+                              "compaction after both)"
                               if a.mode == "graph" else "three C-ABI calls per step"),
                    "statistic": "median over the timed steps"},
         "e2e": {"value": job_rate(world, w["nodes"], e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "call": ("spec_round_launch_host: pinned host inputs copied in group after group (the "
-                         "verification's on the round's own stream, then the attention's, then the draft "
-                         "distributions beside the LM head), the round, results copied out; every step's copies "
-                         "are inside the timed region")},
+                "call": ("spec_round_launch_host: pinned host inputs copied in group after group (the longer "
+                         "branch's first -- the verification's go on the round's own stream --, then the other "
+                         "branch's, then the draft distributions beside the LM head), the round, results copied "
+                         "out; every step's copies are inside the timed region")},
         # the graph runs attention and verification as parallel branches, so its compaction is a
         # launch of its own, as in the direct calls
         "gpu_launches": K * _launches_per_step(case, n_split, stream_k, False),

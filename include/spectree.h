@@ -433,8 +433,10 @@ spec_status spec_eagle_tree(const spec_eagle_tree_args* args, int32_t* dev_statu
  * spec_round_create captures spec_tree_attention(attn, attn_workspace), spec_verify_accept(verify,
  * verify_workspace) and spec_compact_kv(compact) into a CUDA graph and instantiates it.  With
  * both `attn` and `verify` given, the two run as parallel branches of the graph (they read
- * disjoint inputs; the LM head then overlaps the attention's split merge and its last CTAs) and
- * the compaction follows both, since it rewrites K/V rows the attention reads.  Without `attn`,
+ * disjoint inputs), the one that the shapes make longer (FLOPs at the tensor rate against bytes
+ * at HBM bandwidth, keys taken at kv_capacity) captured first so that its kernels take the SMs
+ * and the other fills those left over; the compaction follows both, since it rewrites K/V rows
+ * the attention reads.  Without `attn`,
  * a `compact` that names the verification's outputs (same path, accept_len, path_cap and batch)
  * is captured with it as spec_verify_accept_compact.  Any of the three may be NULL to leave that
  * call out; at least one must be given.  Because of the branches, `attn` and `verify` must not
@@ -476,8 +478,8 @@ void spec_round_destroy(spec_round* round);
  * rejoins `stream` before the compaction and the result copies.  Every other input copy, and
  * every output copy, is on `stream`.  Those verification-only buffers must therefore not overlap
  * any buffer the attention reads.  The input copies run group after group, each with the whole
- * host link: the verification's first (its LM head is issued before the attention), then those
- * on `stream`, then the draft distributions (and with draft_rows, the compact rows), which only
+ * host link: the longer branch's first (that branch is also issued first, as in the graph), then
+ * the other's, then the draft distributions (and with draft_rows, the compact rows), which only
  * the rejection walk at the end of the verification reads.
  *
  * Each spec_host_copy moves `rows` rows of `row_bytes` bytes; row r starts at

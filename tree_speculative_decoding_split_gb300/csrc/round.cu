@@ -6,6 +6,8 @@
 
 #include <new>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -19,7 +21,8 @@ struct spec_round {
   cudaGraphExec_t x_part[3];  // attention, verification, compaction (or null)
   cudaStream_t side;
   cudaEvent_t e_fork, e_join;
-  cudaEvent_t e_vin, e_ain;   // the verification's / the attention's input copies are done
+  cudaEvent_t e_vin, e_ain;   // the first / the second group of input copies is done
+  bool verify_first;          // the verification is the longer branch: it is issued first
   uintptr_t vonly[5][2];      // [lo, hi) of the buffers only the verification reads (but draft_probs)
   int n_vonly;
   // Rejection with draft distributions: their copies run on `side_d` beside the LM head, and
@@ -132,6 +135,23 @@ void make_parts(spec_round* r, const spec_attn_args* attn, void* attn_ws, size_t
   cudaGetLastError();
 }
 
+// Rough device time of each branch from its shapes, for the order of the branches only: the
+// larger of its FLOPs at the tensor rate and its bytes at HBM bandwidth (nominal GB300 figures;
+// only the comparison matters).  The attention's keys are taken at the cache capacity.
+double attention_seconds(const spec_attn_args* a) {
+  const double rows = (double)a->batch * a->n_max * a->num_q_heads;
+  const double flops = 4.0 * a->head_dim * rows * (double)a->kv_capacity;
+  const double es = a->dtype == SPEC_DTYPE_BF16 ? 2.0 : 4.0;
+  const double bytes = 2.0 * es * a->batch * a->num_kv_heads * (double)a->kv_capacity * a->head_dim;
+  return std::max(flops / 2.0e15, bytes / 7.0e12);
+}
+double verification_seconds(const spec_verify_args* v) {
+  const double es = v->dtype == SPEC_DTYPE_BF16 ? 2.0 : 4.0;
+  const double flops = 2.0 * v->batch * v->n_max * (double)v->hidden * v->vocab;
+  const double bytes = es * (double)v->vocab * v->hidden;
+  return std::max(flops / 2.0e15, bytes / 7.0e12);
+}
+
 }  // namespace
 
 extern "C" spec_status spec_round_create(const spec_attn_args* attn, void* attn_workspace,
@@ -175,6 +195,11 @@ extern "C" spec_status spec_round_create(const spec_attn_args* attn, void* attn_
   spec_status st = SPEC_OK;
   if (branch && (cudaEventRecord(e_fork, s) != cudaSuccess || cudaStreamWaitEvent(s2, e_fork, 0) != cudaSuccess))
     st = SPEC_ERR_CUDA;
+  // The longer branch is captured (and so launched) first: its kernels take the SMs and the
+  // shorter branch fills those left over, rather than the long one waiting for them.
+  const bool verify_first = branch && verification_seconds(verify) >= attention_seconds(attn);
+  if (st == SPEC_OK && verify_first)
+    st = spec_verify_accept(verify, verify_workspace, verify_workspace_bytes, dev_status, s2);
   if (st == SPEC_OK && attn) st = spec_tree_attention(attn, attn_workspace, attn_workspace_bytes, dev_status, s);
   // a compaction of the verification's own outputs is folded into the acceptance kernels
   const bool fuse = !branch && verify && compact && compact->path == verify->path &&
@@ -182,7 +207,7 @@ extern "C" spec_status spec_round_create(const spec_attn_args* attn, void* attn_
                     compact->batch == verify->batch;
   if (st == SPEC_OK && fuse)
     st = spec_verify_accept_compact(verify, verify_workspace, verify_workspace_bytes, compact, dev_status, s);
-  else if (st == SPEC_OK && verify)
+  else if (st == SPEC_OK && verify && !verify_first)
     st = spec_verify_accept(verify, verify_workspace, verify_workspace_bytes, dev_status, branch ? s2 : s);
   // the join is captured even after a failure, so that the capture ends cleanly
   if (branch && (cudaEventRecord(e_join, s2) != cudaSuccess || cudaStreamWaitEvent(s, e_join, 0) != cudaSuccess) &&
@@ -211,6 +236,7 @@ extern "C" spec_status spec_round_create(const spec_attn_args* attn, void* attn_
   }
   r->graph = graph;
   r->exec = exec;
+  r->verify_first = verify_first;
   if (branch)
     make_parts(r, attn, attn_workspace, attn_workspace_bytes, verify, verify_workspace, verify_workspace_bytes,
                compact, dev_status);
@@ -263,10 +289,10 @@ extern "C" spec_status spec_round_launch_host(const spec_round* round, const spe
     // both.  The side stream starts after everything enqueued on `s` so far (the previous
     // round included), so no copy overwrites a buffer still being read.
     // The copy groups take the host link one after another rather than sharing it, so that each
-    // consumer starts as early as it can: the verification's inputs first (its LM head is
-    // issued first and holds the SMs it needs; the attention fills the rest and follows), then
-    // the attention's inputs, then the draft distributions, which only the rejection walk at
-    // the end of the verification reads.
+    // consumer starts as early as it can: the longer branch's inputs first (that branch is
+    // issued first and holds the SMs it needs; the other fills the rest), then the other
+    // branch's, then the draft distributions, which only the rejection walk at the end of the
+    // verification reads.
     auto extent = [](const spec_host_copy& c, uintptr_t& lo, uintptr_t& hi) {
       lo = reinterpret_cast<uintptr_t>(c.device);
       hi = lo + (c.rows > 1 ? (size_t)(c.rows - 1) * c.device_pitch : 0) + c.row_bytes;
@@ -287,23 +313,26 @@ extern "C" spec_status spec_round_launch_host(const spec_round* round, const spe
         if (route(inputs[i]) == group && enqueue_copy(inputs[i], true, on) != cudaSuccess) return false;
       return true;
     };
-    if (!copies(1, round->side) || cudaEventRecord(round->e_vin, round->side) != cudaSuccess ||
-        cudaStreamWaitEvent(s, round->e_vin, 0) != cudaSuccess || !copies(0, s))
+    const int first = round->verify_first ? 1 : 0, second = 1 - first;
+    cudaStream_t on[2] = {s, round->side};
+    if (!copies(first, on[first]) || cudaEventRecord(round->e_vin, on[first]) != cudaSuccess ||
+        cudaStreamWaitEvent(on[second], round->e_vin, 0) != cudaSuccess || !copies(second, on[second]))
       return SPEC_ERR_CUDA;
     if (round->direct_verify &&
-        (cudaEventRecord(round->e_ain, s) != cudaSuccess || cudaStreamWaitEvent(round->side_d, round->e_ain, 0) != cudaSuccess ||
-         !copies(2, round->side_d)))
+        (cudaEventRecord(round->e_ain, on[second]) != cudaSuccess ||
+         cudaStreamWaitEvent(round->side_d, round->e_ain, 0) != cudaSuccess || !copies(2, round->side_d)))
       return SPEC_ERR_CUDA;
     // the draft distributions are complete once e_draft (recorded after their copies, before the
     // walk's wait is enqueued) completes
     if (round->direct_verify && cudaEventRecord(round->e_draft, round->side_d) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (!round->verify_first && cudaGraphLaunch(round->x_part[0], s) != cudaSuccess) return SPEC_ERR_CUDA;
     if (round->direct_verify) {
       const spec_status vs = spec_verify_accept(&round->vargs, round->vws, round->vws_bytes, round->dev_status, round->side);
       if (vs != SPEC_OK) return vs;
     } else if (cudaGraphLaunch(round->x_part[1], round->side) != cudaSuccess) {
       return SPEC_ERR_CUDA;
     }
-    if (cudaGraphLaunch(round->x_part[0], s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (round->verify_first && cudaGraphLaunch(round->x_part[0], s) != cudaSuccess) return SPEC_ERR_CUDA;
     if (cudaEventRecord(round->e_join, round->side) != cudaSuccess || cudaStreamWaitEvent(s, round->e_join, 0) != cudaSuccess)
       return SPEC_ERR_CUDA;
     if (round->x_part[2] && cudaGraphLaunch(round->x_part[2], s) != cudaSuccess) return SPEC_ERR_CUDA;
