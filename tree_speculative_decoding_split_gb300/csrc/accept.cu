@@ -506,9 +506,11 @@ constexpr int kRcSlice = kRcThreads * kRcEpt;  // vocabulary entries per CTA at 
 constexpr int kRcSmem = kRcSlice * (int)sizeof(float);
 
 // T(v) = softmax(z / tau)[v], and one residual step relu(R / S - D): written with explicit fused
-// operations so that every CTA of a cluster evaluates them bit for bit alike.
+// operations so that every CTA of a cluster evaluates them bit for bit alike.  T uses the fast
+// exponential (__expf: a few ulp, relative error near 1e-6 over these arguments), far inside the
+// 1e-4 band of the decisions it feeds.
 __device__ __forceinline__ float target_prob(float z, float inv_tau, float lse) {
-  return expf(fmaf(z, inv_tau, -lse));
+  return __expf(fmaf(z, inv_tau, -lse));
 }
 __device__ __forceinline__ float residual_step(float r, float inv_s, float d) {
   return fmaxf(fmaf(r, inv_s, -d), 0.f);
@@ -551,8 +553,9 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
   __shared__ float s_part[2][kRcMaxCluster];         // per-CTA residual sums
   __shared__ double s_tot[kRcMaxCluster];            // per-CTA mass of the final distribution
   __shared__ float s_red[kRcThreads / 32];
-  __shared__ double s_dred[kRcThreads / 32];
-  __shared__ int s_owner;
+  __shared__ double s_dred[kRcThreads / 32];         // bonus: mass of the warps before each warp
+  __shared__ double s_bonus[3];                      // bonus: total, this CTA's start, target
+  __shared__ int s_owner, s_owner_cta;
 
   const int kc = (int)cl.num_blocks(), rank = (int)cl.block_rank();
   const int b = blockIdx.x / kc;
@@ -590,19 +593,16 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
       const size_t erow = rb + e;
       const float* lg = p.logits + erow * (size_t)V + base;
       const float* drow = c_first >= 0 ? draft_row(p, b, e) : nullptr;
-      if (drow && p.inv_map) {  // draft indices first (asynchronously, into s_D), then the gathers
-#pragma unroll
-        for (int j = 0; j < kRcEpt; ++j) {
-          const int li = j * kRcThreads + tid;
-          if (li < Lc) cp_async_4(s_D + li, p.inv_map + base + li);
-        }
+      // The copies into s_D touch no registers of r: rolled loops leave the register file to r.
+      // A mapped draft vocabulary: the slice's inverse map first, the logits while it lands,
+      // then the gather of the draft entries it names.
+      if (drow && p.inv_map) {
+#pragma unroll 4
+        for (int li = tid; li < Lc; li += kRcThreads) cp_async_4(s_D + li, p.inv_map + base + li);
         asm volatile("cp.async.commit_group;\n" ::: "memory");
-      } else if (drow) {
-#pragma unroll
-        for (int j = 0; j < kRcEpt; ++j) {
-          const int li = j * kRcThreads + tid;
-          if (li < Lc) cp_async_4(s_D + li, drow + base + li);
-        }
+      } else if (drow) {  // draft row in target order: this slice, asynchronously
+#pragma unroll 4
+        for (int li = tid; li < Lc; li += kRcThreads) cp_async_4(s_D + li, drow + base + li);
         asm volatile("cp.async.commit_group;\n" ::: "memory");
       }
 #pragma unroll
@@ -612,16 +612,13 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
       }
       if (drow && p.inv_map) {
         cp_async_wait_all();
-#pragma unroll
-        for (int j = 0; j < kRcEpt; ++j) {
-          const int li = j * kRcThreads + tid;
-          if (li < Lc) {
-            const int m = __float_as_int(s_D[li]);
-            if (m >= 0)
-              cp_async_4(s_D + li, drow + m);
-            else
-              s_D[li] = 0.f;
-          }
+#pragma unroll 4
+        for (int li = tid; li < Lc; li += kRcThreads) {
+          const int m = __float_as_int(s_D[li]);
+          if (m >= 0)
+            cp_async_4(s_D + li, drow + m);
+          else
+            s_D[li] = 0.f;
         }
         asm volatile("cp.async.commit_group;\n" ::: "memory");
       }
@@ -757,59 +754,72 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
   const int v0 = min(Lc, tid * CH), v1 = min(Lc, v0 + CH);
   float csum = 0.f;
   for (int v = v0; v < v1; ++v) csum += s_D[v];
-  double incl = (double)csum;
+  // Prefix masses: the chunk sums and their scan within a warp in float (their rounding, about
+  // 1e-7 of the mass, is far inside the 1e-4 band that flags a near-boundary draw); the sums
+  // over warps and over the cluster's CTAs in double, each formed once by one thread (FP64
+  // issue is scarce) and read by all.
+  float incl = csum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xffffffffu, incl, o);
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += t;
   }
-  if (lane == 31) s_dred[warp] = incl;
+  if (lane == 31) s_red[warp] = incl;
   if (tid == 0) s_owner = -1;
   __syncthreads();
-  double wpre = 0.0, cta = 0.0;
-  for (int w = 0; w < kRcThreads / 32; ++w) {
-    if (w < warp) wpre += s_dred[w];
-    cta += s_dred[w];
+  if (tid == 0) {
+    double run = 0.0;
+    for (int w = 0; w < kRcThreads / 32; ++w) {
+      s_dred[w] = run;
+      run += (double)s_red[w];
+    }
+    for (int q = 0; q < kc; ++q) cl.map_shared_rank(&s_tot[0], q)[rank] = run;
   }
-  const double excl = wpre + incl - (double)csum;  // mass of this slice before the chunk
-  if (tid == 0)
-    for (int q = 0; q < kc; ++q) cl.map_shared_rank(&s_tot[0], q)[rank] = cta;
   cl.sync();
-  double total = 0.0, pre = 0.0;
-  for (int q = 0; q < kc; ++q) {
-    if (q == rank) pre = total;
-    total += s_tot[q];
-  }
-  const float u2 = accept_uniform(p.seed, (uint32_t)b, (uint32_t)e, 1u);
-  const double target = (double)u2 * total;
-  const double band = (double)kMargin * total;
-  int owner_cta = -1;
-  {
+  if (tid == 0) {
+    const float u2 = accept_uniform(p.seed, (uint32_t)b, (uint32_t)e, 1u);
+    double total = 0.0, pre = 0.0;
+    for (int q = 0; q < kc; ++q) {
+      if (q == rank) pre = total;
+      total += s_tot[q];
+    }
+    const double target = (double)u2 * total;
+    int oc = -1;
     double run = 0.0;
     for (int q = 0; q < kc; ++q) {  // last CTA with mass that starts at or below the target
-      if (s_tot[q] > 0.0 && run <= target) owner_cta = q;
+      if (s_tot[q] > 0.0 && run <= target) oc = q;
       run += s_tot[q];
     }
+    s_bonus[0] = total;
+    s_bonus[1] = pre;
+    s_bonus[2] = target;
+    s_owner_cta = oc;
   }
+  __syncthreads();
+  const double total = s_bonus[0], pre = s_bonus[1], target = s_bonus[2];
+  const double band = (double)kMargin * total;
+  const int owner_cta = s_owner_cta;
+  const double excl = s_dred[warp] + (double)(incl - csum);  // mass of this slice before the chunk
   if (owner_cta == rank) {
     // owner: the last chunk with mass that starts at or below the target
     if (csum > 0.f && pre + excl <= target) atomicMax(&s_owner, tid);
     __syncthreads();
-    if (tid == s_owner) {
-      double acc = pre + excl, prev = acc;
+    if (tid == s_owner) {  // the chunk's scan in float, from the target's offset into the chunk
+      const float rem = (float)(target - (pre + excl)), bandf = (float)band;
+      float acc = 0.f, prev = 0.f;
       int found = -1, last_nz = -1;
       for (int v = v0; v < v1; ++v) {
         const float rv = s_D[v];
         if (rv > 0.f) last_nz = v;
         prev = acc;
-        acc += (double)rv;
-        if (acc > target) { found = v; break; }
+        acc += rv;
+        if (acc > rem) { found = v; break; }
       }
       if (found < 0) {
         found = last_nz;
         prev = acc;
       }
-      const bool near = (target - prev < band) || (acc - target < band) || (target < band);
+      const bool near = (rem - prev < bandf) || (acc - rem < bandf) || (target < band);
       p.bonus[b] = found >= 0 ? base + found : V - 1;
       if (p.bonus_margin) p.bonus_margin[b] = near ? 1 : 0;
     }
