@@ -306,3 +306,54 @@ def test_host_round_with_compact_draft_rows():
     assert torch.equal(res_nl, ref_nl.cpu())
     assert torch.equal(t2["k"].view(torch.int16), ref_k.view(torch.int16))
     r.close()
+
+
+def test_host_round_attention_first_with_draft_rows():
+    """A round whose attention is the longer branch (prefixes of thousands of keys, a 64-token
+    vocabulary): the host-buffer round copies the attention's inputs first, then the
+    verification's, then the compact draft rows, and issues the attention first -- with the same
+    results as the device round."""
+    d = H.dev()
+    rng = np.random.default_rng(31)
+    parents = [T.random_bfs_tree(rng, 24, 4)[0], T.chain_tree(6), T.random_bfs_tree(rng, 24, 3)[0]]
+    case = make_case(dtype="bf16", Hq=8, Hkv=2, d=128, Hd=64, V=64, prefix_len=[6000, 3100, 7777],
+                     parents=parents, rule="rejection", tau=0.9, seed=8, tokens=("iid", 0.8, 0.4), rng=rng)
+    rows, index = compact_draft(case.draft_probs, case.parent, case.n_nodes, rng=rng)
+    t = H.to_device(case, d)
+    t["rows"], t["index"] = H.tensor(rows, d), H.tensor(index, d)
+    aa, out, lse = st.attn_args(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"])
+    va, outs = st.verify_args(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], case.rule, case.tau,
+                              case.eps, case.delta, case.seed, t["rows"], t["map"], path_cap=case.N,
+                              draft_rows=t["index"])
+    ca, src, nl = st.compact_args(t["k"], t["v"], t["prefix_len"], outs["path"], outs["accept_len"])
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    r = st.Round(aa, va, ca, dev_status=status)
+    r.launch()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = {k: v.clone() for k, v in outs.items()}
+    ref_out, ref_k, ref_nl = out.clone(), t["k"].clone(), nl.clone()
+    fresh = H.to_device(case, d)
+    t["k"].copy_(fresh["k"])
+    t["v"].copy_(fresh["v"])
+    keys = ("q", "hidden", "tokens", "parent", "rows", "index")
+    host = {k: t[k].cpu().pin_memory() for k in keys}
+    for k in keys:
+        t[k].zero_()
+    for v in outs.values():
+        v.fill_(-7)
+    out.zero_()
+    ins = [st.host_copy(host[k], t[k]) for k in keys]
+    res = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    res_nl = torch.empty(nl.shape, dtype=nl.dtype).pin_memory()
+    outs_c = [st.host_copy(res[k], outs[k]) for k in res] + [st.host_copy(res_nl, nl)]
+    torch.cuda.synchronize()
+    r.launch_host(ins, outs_c)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for k in res:
+        assert torch.equal(res[k], ref[k].cpu()), k
+    assert torch.equal(res_nl, ref_nl.cpu())
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(t["k"].view(torch.int16), ref_k.view(torch.int16))
+    r.close()
