@@ -464,8 +464,8 @@ def measure_workload(a, cfg, rank, world, dist, seed, with_cpu):
                         case.name)
     rf_lm = _roofline(lm_kernel, w["lm_flops"], w["lm_kernel_bytes"], lm_med, hbm, tc, peak_kind, case.name)
     dominant = rf_attn if attn_med >= lm_med else rf_lm
-    # the benchmark spec's combined roofline of the step: max(KV + weight bytes at HBM bandwidth,
-    # LM-head FLOPs at the bf16 tensor peak); the full one adds every byte and the attention FLOPs
+    # the step's combined roofline: max(KV + weight bytes at HBM bandwidth, LM-head FLOPs at the
+    # bf16 tensor peak); the full one adds every byte and the attention FLOPs
     step_bytes = w["kv_bytes"] + w["qo_bytes"] + w["w_bytes"] + w["h_bytes"] + w["logits_bytes"]
     t_comb = max((w["kv_bytes"] + w["w_bytes"]) / (hbm * 1e9), w["lm_flops"] / (tc * 1e12))
     t_full = max(step_bytes / (hbm * 1e9), (w["lm_flops"] + w["attn_flops"]) / (tc * 1e12))
