@@ -73,6 +73,8 @@ def _args():
                    help="profiling harness: run the workload's three calls --warmup + --steps times "
                         "without timing anything and print nothing (for ncu)")
     p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--ref-budget", type=float, default=150.0,
+                   help="--impl reference: stop taking steps after this many seconds of oracle work")
     return p.parse_args()
 
 
@@ -793,15 +795,21 @@ def run_reference(a):
     for i in range(min(a.warmup, 1)):
         oracle_request_sample(case, i % case.B, i % case.Hkv)
     nodes = est = 0.0
-    for i in range(a.steps):
+    steps = 0
+    t_start = time.perf_counter()
+    for i in range(a.steps):  # at least one step; then as many as fit the time budget
+        if steps and time.perf_counter() - t_start > a.ref_budget:
+            break
         n, e = oracle_request_sample(case, i % case.B, i % case.Hkv)
         nodes += n
         est += e
+        steps += 1
     v = nodes / est
     ms = float(case.n_nodes.sum()) / v * 1e3
-    sample = (f"{a.steps} steps, step i = request i mod {case.B}: tree attention of KV head i mod {case.Hkv} "
-              f"scaled by {case.Hkv}, plus LM head, acceptance and compaction of that request in full")
-    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
+    sample = (f"{steps} steps of {a.steps} requested (stopped after {a.ref_budget:.0f} s of oracle work), step i = "
+              f"request i mod {case.B}: tree attention of KV head i mod {case.Hkv} scaled by {case.Hkv}, plus LM "
+              f"head, acceptance and compaction of that request in full")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": a.gpus, "steps": steps,
             "warmup": min(a.warmup, 1), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": case.name, "batch": case.B, "prefix_len": [int(x) for x in case.prefix_len][:8],
