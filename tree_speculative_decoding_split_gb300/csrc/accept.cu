@@ -73,6 +73,29 @@ __device__ int load_and_validate(const AcceptParams& p, int b, int* s_par, int* 
   return bad_tree ? SPEC_ERR_BAD_TREE : (bad_tok ? SPEC_ERR_BAD_TOKEN : 0);
 }
 
+// ln sum_v exp(z_v / tau) of tree row `row` (rejection), merged by one warp from the LM head's
+// per-slice records {max, sum of exp(z / tau - max)}: every lane a strided share, then a shuffle
+// merge -- the same order in every CTA, so every CTA of a cluster gets the same value.
+__device__ __forceinline__ float row_lse_warp(const AcceptParams& p, size_t row, int lane) {
+  float m = -INFINITY, s = 0.f;
+  for (int k = lane; k < p.n_parts; k += 32) {
+    const float4 f = p.part[(size_t)k * p.R + row];
+    const float mm = fmaxf(m, f.x);
+    if (mm > -INFINITY)
+      s = (s > 0.f ? s * expf(m - mm) : 0.f) + (f.y > 0.f ? f.y * expf(f.x - mm) : 0.f);
+    m = mm;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o), os = __shfl_xor_sync(0xffffffffu, s, o);
+    const float mm = fmaxf(m, om);
+    if (mm > -INFINITY)
+      s = (s > 0.f ? s * expf(m - mm) : 0.f) + (os > 0.f ? os * expf(om - mm) : 0.f);
+    m = mm;
+  }
+  return m + logf(s);
+}
+
 // Node e's draft distribution (rejection): row b * N + e, or the compact row draft_rows[b][e].
 // Called only for nodes with children, whose rows load_and_validate has checked.
 __device__ __forceinline__ const float* draft_row(const AcceptParams& p, int b, int e) {
@@ -344,6 +367,7 @@ __device__ void rejection_block_walk(const AcceptParams& p) {
   __shared__ int s_nk, s_accept, s_owner;
   __shared__ int s_found;
   __shared__ float s_mgflag;
+  __shared__ float s_lse;
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int err = load_and_validate(p, b, s_parent, s_tok);
   if (err || (p.map_bad && *p.map_bad)) {
@@ -369,17 +393,21 @@ __device__ void rejection_block_walk(const AcceptParams& p) {
   };
 
   while (true) {
-    if (tid == 0) {
-      int k = 0;
-      for (int c = e + 1; c < n; ++c)
-        if (s_parent[c] == e) s_kids[k++] = c;
-      s_nk = k;
+    if (warp == 0) {
+      const float l = row_lse_warp(p, rb + e, lane);
+      if (lane == 0) {
+        int k = 0;
+        for (int c = e + 1; c < n; ++c)
+          if (s_parent[c] == e) s_kids[k++] = c;
+        s_nk = k;
+        s_lse = l;
+      }
     }
     __syncthreads();
     const int nk = s_nk;
     const size_t erow = rb + e;
     const float* lg = p.logits + erow * (size_t)V;
-    const float lse_e = p.rlse[erow];
+    const float lse_e = s_lse;
     const float* de = nk > 0 ? draft_row(p, b, e) : nullptr;
     bool moved = false;
     for (int k = 0; k < nk; ++k) {
@@ -435,7 +463,7 @@ __device__ void rejection_block_walk(const AcceptParams& p) {
   // ---- bonus token: inverse CDF of R at u' = U(seed, b, e, 1) ----
   const size_t erow = rb + e;
   const float* lg = p.logits + erow * (size_t)V;
-  const float lse_e = p.rlse[erow];
+  const float lse_e = s_lse;  // node e's, from its arrival
   const float* Rc = Rb[cur];
   auto rval = [&](int v) -> float { return lazy ? expf(lg[v] * p.inv_tau - lse_e) : Rc[v]; };
   const int CH = (V + kRejThreads - 1) / kRejThreads;
@@ -556,6 +584,7 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
   __shared__ double s_dred[kRcThreads / 32];         // bonus: mass of the warps before each warp
   __shared__ double s_bonus[3];                      // bonus: total, this CTA's start, target
   __shared__ int s_owner, s_owner_cta;
+  __shared__ float s_lse[2];                         // the visited row's LSE, by visit parity
 
   const int kc = (int)cl.num_blocks(), rank = (int)cl.block_rank();
   const int b = blockIdx.x / kc;
@@ -583,16 +612,21 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
   const size_t rb = (size_t)b * p.N;
   float r[kRcEpt];
   float S = 1.f;  // sum of the residual held in r (1 while r holds T_e itself)
-  int e = 0, dep = 0, margins = 0, sp = 0;
+  int e = 0, dep = 0, margins = 0, sp = 0, lp = 0;
   bool moved = true;
 
   while (moved) {
     // ---- arrive at node e: r <- T_e, s_D <- D_e (this slice; a leaf has no D_e) ----
     const int c_first = next_child(s_kids, e, -1);
+    float lse_e;
     {
       const size_t erow = rb + e;
       const float* lg = p.logits + erow * (size_t)V + base;
       const float* drow = c_first >= 0 ? draft_row(p, b, e) : nullptr;
+      if (warp == 0) {
+        const float l = row_lse_warp(p, erow, lane);
+        if (lane == 0) s_lse[lp] = l;
+      }
       // The copies into s_D touch no registers of r: rolled loops leave the register file to r.
       // A mapped draft vocabulary: the slice's inverse map first, the logits while it lands,
       // then the gather of the draft entries it names.
@@ -622,11 +656,13 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
         }
         asm volatile("cp.async.commit_group;\n" ::: "memory");
       }
-      const float lse = p.rlse[erow];
+      __syncthreads();  // the row's LSE is in s_lse[lp] (written a visit ago: a barrier between)
+      lse_e = s_lse[lp];
+      lp ^= 1;
 #pragma unroll
       for (int j = 0; j < kRcEpt; ++j) {
         const int li = j * kRcThreads + tid;
-        r[j] = (li < Lc) ? target_prob(r[j], p.inv_tau, lse) : 0.f;
+        r[j] = (li < Lc) ? target_prob(r[j], p.inv_tau, lse_e) : 0.f;
       }
       S = 1.f;
       cp_async_wait_all();  // each thread reads back only the entries it copied
@@ -639,7 +675,7 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
     {
       const int x = s_tok[c];
       const float* drow = draft_row(p, b, e);
-      float rx = target_prob(__ldg(p.logits + erow * (size_t)V + x), p.inv_tau, p.rlse[erow]);
+      float rx = target_prob(__ldg(p.logits + erow * (size_t)V + x), p.inv_tau, lse_e);
       float dx;
       if (p.inv_map) {
         const int m = __ldg(p.inv_map + x);

@@ -464,6 +464,7 @@ spec_status verify_accept_impl(const spec_verify_args* a, void* workspace, size_
   ap.tokens = a->tokens; ap.parent = a->parent; ap.n_nodes = a->n_nodes;
   ap.rmax = l.rmax; ap.rlse = l.rlse; ap.rent = l.rent; ap.rgap = l.rgap; ap.rarg = l.rarg; ap.clog = l.clog;
   ap.logits = l.logits; ap.draft = a->draft_probs; ap.inv_map = l.inv; ap.map_bad = l.map_bad; ap.rbuf = l.rbuf;
+  ap.part = l.part; ap.n_parts = l.n_parts; ap.R = l.R;
   if (a->rule == SPEC_RULE_REJECTION && a->draft_rows) {
     ap.draft_rows = a->draft_rows;
     ap.n_draft_rows = a->n_draft_rows;
@@ -486,7 +487,10 @@ spec_status verify_accept_impl(const spec_verify_args* a, void* workspace, size_
   fp.fuse_accept = a->rule != SPEC_RULE_REJECTION;
   fp.counters = l.counters;
   fp.acc = ap;
-  launch_row_finalize(fp, stream);
+  // Rejection sampling reads only the visited rows' LSE, which the walk merges from the records
+  // itself; the row finalisation then runs only for the optional per-row outputs.
+  const bool hooks = a->row_max || a->row_lse || a->row_entropy || a->row_argmax;
+  if (a->rule != SPEC_RULE_REJECTION || hooks) launch_row_finalize(fp, stream);
   if (a->rule == SPEC_RULE_REJECTION && a->draft_ready) {  // the walk is the first reader of draft_probs
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return SPEC_ERR_CUDA;

@@ -125,6 +125,8 @@ struct AcceptParams {
   const float* rmax; const float* rlse; const float* rent; const float* rgap;
   const int32_t* rarg; const float* clog;
   const float* logits;         // [R][V] (rejection)
+  const float4* part;          // [n_parts][R] LM-head records {max, sumexp, ...} of z / tau (rejection)
+  int n_parts, R;
   const float* draft;          // [B][N][Vd], or [n_draft_rows][Vd] with draft_rows (rejection)
   const int32_t* draft_rows;   // [B][N] node -> row of draft, or nullptr (row b * N + e)
   int n_draft_rows;
