@@ -262,11 +262,11 @@ def _launches_per_step(case, n_split, stream_k, fused):
         attn = 2                                                       # tree prep + fp32 rows
     else:
         attn = 2 if (stream_k or n_split > 1) else 1                   # counters memset + stream-K | split-KV [+ merge]
-    verify = 2 if case.dtype == "bf16" else 3                          # LM head, row finalise [+ fp32 stats]
-    if case.rule == "rejection":
-        verify += 0                                                    # the walk replaces the row finalisation
-        if case.draft_to_target is not None:                           # (no per-row outputs requested)
-            verify += 1                                                # draft-map inversion
+    # LM head, then the row finalisation -- or for rejection the walk, which merges its rows'
+    # statistics itself (no per-row outputs are requested here) [+ fp32 statistics]
+    verify = 2 if case.dtype == "bf16" else 3
+    if case.rule == "rejection" and case.draft_to_target is not None:
+        verify += 1                                                    # draft-map inversion
     return attn + verify + (0 if fused else 1)                         # compaction folded into acceptance
 
 
