@@ -247,12 +247,16 @@ def test_compact_draft_rows_on_the_eagle3_b32_workload():
     case = H.config_case(4, 2)
     t = H.to_device(case, d)
     full = H.gpu_verify(case, t, hooks=False)
+    # with the per-row outputs requested the row finalisation runs as well; the walk's decisions
+    # must not depend on it (the oracle-checked tests request them, the benchmark does not)
+    hooked = H.gpu_verify(case, t, hooks=True)
     rows, index = compact_draft(case.draft_probs, case.parent, case.n_nodes, rng=np.random.default_rng(1))
     assert rows.shape[0] * 4 < case.B * case.N
     got = _verify_compact(case, t, rows, index)
-    assert got["status"] == 0 and full["status"] == 0
+    assert got["status"] == 0 and full["status"] == 0 and hooked["status"] == 0
     for k in _VERIFY_OUT:
         assert (got[k] == full[k]).all(), k
+        assert (hooked[k] == full[k]).all(), k
 
 
 def test_missing_draft_row_zeroes_only_that_request():
