@@ -366,6 +366,20 @@ spec_status spec_tree_attention(const spec_attn_args* a, void* workspace, size_t
     if (!make_map_bf16(&tmK, a->k_cache, 3, dims, strides, box) ||
         !make_map_bf16(&tmV, a->v_cache, 3, dims, strides, box))
       return SPEC_ERR_CUDA;
+    p.v_rows = 64;
+    if (paged && a->block_size < 64 && d == 128 && !l.plan.sk) {
+      // a pool block's V rows as one box of both 64-column halves: (64, block, d / 64 with a
+      // 128-byte stride, num_blocks*Hkv), landing as [half][block rows][128 B] -- the layout the
+      // P V MMA then reads with a block-sized stride between the halves
+      const cuuint64_t vd[4] = {64, (cuuint64_t)a->block_size, 2, (cuuint64_t)a->num_blocks * Hkv};
+      const cuuint64_t vs[3] = {(cuuint64_t)d * 2, 128, (cuuint64_t)a->block_size * d * 2};
+      const cuuint32_t vb[4] = {64, (cuuint32_t)a->block_size, 2, 1};
+      CUtensorMap tmV4;
+      if (make_map_bf16(&tmV4, a->v_cache, 4, vd, vs, vb)) {
+        tmV = tmV4;
+        p.v_rows = a->block_size;
+      }
+    }
     // Q as (d, Hq, N, B): one box of (64, G, 128 / G, 1) is a 128-row group of (node, head) rows
     // of one KV head.  Other G stage Q through registers.
     CUtensorMap tmQ;

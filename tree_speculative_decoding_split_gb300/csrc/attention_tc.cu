@@ -168,9 +168,14 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
           }
         }
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sK + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmK, &full[st], c * 64, y, z);
-          tma_load_3d(sV + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmV, &full[st], c * 64, y, z);
+        if (p.v_rows < kKT) {  // both halves of the block's V rows in one box: [half][rows][128 B]
+          tma_load_4d(sV + st * C::kTile + i * (D / 64) * rows * 128, &tmV, &full[st], 0, y, 0, z);
+        } else {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sV + st * C::kTile + c * kKT * 128 + i * rows * 128, &tmV, &full[st], c * 64, y, z);
         }
       }
     }
@@ -415,6 +420,8 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kGR, kKT, 0);
       constexpr uint32_t idP = idesc_bf16_f32(kGR, D, 1);
+      const int vr = p.v_rows;  // rows per V box group (the tile's layout): 16, 32 or 64
+      const int vr_shift = 31 - __clz(vr);
       bool ok = true;
       // Issue order for the group: S(0), then per tile t: S(t + 1) as soon as the softmax has
       // read S(t) (early in its work on tile t, so the next scores are ready when it finishes),
@@ -444,7 +451,11 @@ __global__ void __launch_bounds__(AttnTcCfg<D, NG>::kThreads, 1)
         const uint32_t va = smem_u32(sV + (t % kStages) * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < kKT / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(va + kk * 16 * 128, kKT * 128, 1024);
+          // keys 16 kk .. 16 kk + 15 of the tile: in V block (16 kk) / v_rows, at row (16 kk) % v_rows;
+          // the two 64-column halves of d lie v_rows * 128 bytes apart
+          const int kr = kk * 16;
+          const uint32_t voff = (uint32_t)(((kr >> vr_shift) * (D / 64) << vr_shift) * 128 + (kr & (vr - 1)) * 128);
+          const uint64_t bd = sdesc_sw128(va + voff, (uint32_t)vr * 128, 1024);
           umma_bf16_tmem_a(tmem + C::kColO + ga * D, pt + kk * 8, bd, idP, (t > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&ofull[2 * ga + (t & 1)]);

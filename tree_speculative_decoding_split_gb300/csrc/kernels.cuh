@@ -46,6 +46,9 @@ struct AttnParams {
   int32_t* tree_bad; // [B] bf16: written by CTA (split 0, row group 0, KV head 0) of each request --
                      // the request's tree or capacity check failed (the merge zeroes its rows)
   int q_tma;         // bf16: Q rows arrive by TMA through the (d, Hq, N, B) map (128 % G == 0)
+  int v_rows;        // bf16: V tile layout [64 / v_rows][d / 64][v_rows][128 B]; 64 = one block of
+                     // rows per d/64 chunk; a paged block size below 64 when its V rows arrive as
+                     // one (64, block, d / 64) box per block
   int direct;        // bf16, one split: the kernel writes out / lse itself and no merge runs
   // persistent stream-K kernel (n_rg then counts 256-row blocks)
   float* sk_o;       // [grid][2][256][d] normalised partial outputs of the CTAs' partial pieces
