@@ -656,7 +656,9 @@ __device__ void rejection_cluster_walk(const AcceptParams& p) {
         }
         asm volatile("cp.async.commit_group;\n" ::: "memory");
       }
-      __syncthreads();  // the row's LSE is in s_lse[lp] (written a visit ago: a barrier between)
+      // s_lse[lp] now holds this row's LSE; warp 0 writes this buffer again two visits on, after
+      // every thread has passed the next visit's barrier (and so has read it)
+      __syncthreads();
       lse_e = s_lse[lp];
       lp ^= 1;
 #pragma unroll
