@@ -204,3 +204,26 @@ def test_paged_round_matches_direct_calls():
         assert torch.equal(a, b), k
     assert int(ref["accept_len"].max().item()) >= 1, "no request accepted a node: the compaction was not exercised"
     r.close()
+
+
+def test_paged_matches_contiguous_at_70b_shapes():
+    """70B-shaped attention (Hq 64, Hkv 8, d 128, 255-node BFS trees) at batch 4 with 8192-slot
+    prefixes, from a shuffled pool of 16-slot blocks (V rows arriving one box per block) and from
+    the contiguous caches: the same outputs within the bf16 tolerance and LSE within 1e-3."""
+    d = H.dev()
+    rng = np.random.default_rng(3)
+    B, n = 4, 255
+    parents = [T.random_bfs_tree(rng, n, 8)[0] for _ in range(B)]
+    case = make_case(dtype="bf16", Hq=64, Hkv=8, d=128, Hd=64, V=16, prefix_len=[8192] * B, parents=parents,
+                     tokens=("given", np.zeros((B, n), dtype=np.int32)), N=n, seed=4, rng=rng)
+    t = H.to_device(case, d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    out_c, lse_c = st.tree_attention(t["q"], t["k"], t["v"], t["prefix_len"], t["n_nodes"], t["parent"],
+                                     dev_status=status)
+    table, pk, pv = _pool(case, 16, rng)
+    out_p, lse_p = st.tree_attention(t["q"], H.tensor(pk, d, True), H.tensor(pv, d, True), t["prefix_len"],
+                                     t["n_nodes"], t["parent"], dev_status=status, block_table=H.tensor(table, d))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert (out_c.float() - out_p.float()).abs().max().item() < 2e-2
+    assert ((lse_c - lse_p).abs() / lse_c.abs().clamp_min(1.0)).max().item() < 1e-3
