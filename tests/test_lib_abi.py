@@ -104,6 +104,18 @@ def test_host_argument_errors_return_before_launch(L):
     assert L.spec_verify_accept(ctypes.byref(v), None, 0, None, None) == 2           # bf16 hidden % 64
     v.hidden, v.rule, v.temperature = 128, 2, 0.0
     assert L.spec_verify_accept(ctypes.byref(v), None, 0, None, None) == 1           # tau must be > 0
+    # compact draft rows: a row index needs at least one row; the reserved word must be 0
+    fake2 = ctypes.c_void_p(1 << 20)
+    r = st.VerifyArgs(dtype=1, batch=1, n_max=4, hidden=128, vocab=50, rule=2, temperature=1.0, draft_vocab=50,
+                      path_cap=4, hidden_states=fake2, lm_head_weight=fake2, tokens=fake2, parent=fake2,
+                      n_nodes=fake2, draft_probs=fake2, accept_len=fake2, path=fake2, bonus_token=fake2)
+    assert L.spec_verify_accept_workspace(ctypes.byref(r)) > 0
+    r.draft_rows = fake2
+    assert L.spec_verify_accept_workspace(ctypes.byref(r)) == 0                       # n_draft_rows 0
+    r.n_draft_rows = 7
+    assert L.spec_verify_accept_workspace(ctypes.byref(r)) > 0
+    r.reserved1 = 1
+    assert L.spec_verify_accept_workspace(ctypes.byref(r)) == 0                       # reserved word set
     c = st.CompactArgs(dtype=0, batch=1, num_kv_heads=1, head_dim=64, kv_capacity=8, path_cap=0)
     assert L.spec_compact_kv(ctypes.byref(c), None, None) == 1                        # path_cap 0
     handle = ctypes.c_void_p(123)
