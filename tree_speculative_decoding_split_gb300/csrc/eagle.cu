@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kEgThreads) eagle_expand_kernel(const EagleExp
   const int C = p.F * p.k;
   const int nc = p.n_chunks * p.k;  // chunk candidates per frontier row (<= 256)
   const size_t ob = (size_t)b * p.cand_stride;
+  pdl_wait();  // the chunk candidates of the kernel before are complete
   for (int f = warp; f < p.F; f += kEgThreads / 32) {
     const bool valid = !p.frontier_valid || p.frontier_valid[(size_t)b * p.F + f] != 0;
     const unsigned long long* cand = p.chunk_keys + (size_t)(b * p.F + f) * nc;
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(kEgTreeThreads) eagle_tree_kernel(const EagleT
 
 void launch_eagle_expand(const EagleExpandParams& p, const MedusaParams& chunks, cudaStream_t stream) {
   launch_row_topk_chunks(chunks, stream);
-  eagle_expand_kernel<<<p.B, kEgThreads, 0, stream>>>(p);
+  launch_dependent(eagle_expand_kernel, dim3(p.B), dim3(kEgThreads), 0, stream, p);
 }
 
 void launch_eagle_tree(const EagleTreeParams& p, cudaStream_t stream) {

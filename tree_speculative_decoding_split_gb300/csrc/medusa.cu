@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const Med
   const int v0 = chunk * p.chunk;
   const int v1 = min(p.V, v0 + p.chunk);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_launch_dependents();  // the merge may launch now; it waits for this grid before reading
   const int mode = load_mode(p);
   float x[kMxEpt];
   load_vals(p, mode, row, v0, v1, x);
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) medusa_expand_kernel(const Medu
     }
   }
   bad = __syncthreads_or(bad);
+  pdl_wait();  // the chunk candidates are complete (the topology above is an input of its own)
   // every head's top-k from its chunk candidates: one warp per head, k rounds of a warp-wide
   // maximum below the previous winner (the candidates are re-read from L1 each round), so the
   // heads proceed side by side with no block barrier
@@ -322,7 +324,7 @@ void launch_row_topk_chunks(const MedusaParams& p, cudaStream_t stream) {
 
 void launch_medusa(const MedusaParams& p, cudaStream_t stream) {
   medusa_chunk_topk_kernel<<<dim3(p.n_chunks, p.B * p.K), kMxThreads, 0, stream>>>(p);
-  medusa_expand_kernel<<<p.B, kMxThreads, 0, stream>>>(p);
+  launch_dependent(medusa_expand_kernel, dim3(p.B), dim3(kMxThreads), 0, stream, p);
 }
 
 }  // namespace spectree
