@@ -8,6 +8,7 @@ import torch
 import oracle
 import tree_speculative_decoding_split_gb300 as st
 import gpu_helpers as H
+from gen import compact_draft as gen_compact_draft
 
 pytestmark = pytest.mark.gpu
 
@@ -129,3 +130,69 @@ def test_tree_errors():
     tree = st.eagle_tree(S, Tk, P, 5, draft_to_target=m, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 6
+
+
+def test_dynamic_tree_verified_by_rejection_with_compact_draft_rows():
+    """The dynamic draft tree end to end on the device: expansion layers and tree selection over a
+    mapped draft vocabulary, then rejection-sampling verification of that tree whose draft
+    distributions are the expanded nodes' rows only (draft_rows) -- against the oracle's
+    verification of the same tree with the full [B][N][Vd] layout."""
+    import dataclasses
+    from gen import make_case
+    d = H.dev()
+    rng = np.random.default_rng(2024)
+    B, F, k, Vd, D, N = 3, 4, 4, 500, 4, 31
+    V = 4 * Vd
+    d2t = rng.permutation(V)[:Vd].astype(np.int32)
+    C = F * k
+    S = torch.full((B, D, C), float("-inf"), dtype=torch.float32, device=d)
+    Tk = torch.full((B, D, C), -1, dtype=torch.int32, device=d)
+    P = torch.full((B, D, C), -1, dtype=torch.int32, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    fs = torch.zeros((B, 1), dtype=torch.float32, device=d)
+    valid = torch.ones((B, 1), dtype=torch.int32, device=d)
+    fc = torch.full((B, 1), -1, dtype=torch.int32, device=d)
+    lps, fronts = [], []  # per layer: log-probabilities of its frontier rows, and the candidates they are
+    for l in range(D):
+        lp = _logp(rng, (B, fs.shape[1], Vd), False)
+        lps.append(lp)
+        fronts.append(fc.cpu().numpy())  # frontier row f of layer l = candidate fronts[l][b][f] of layer l - 1
+        outs = {"token": Tk[:, l], "score": S[:, l], "parent": P[:, l]}
+        res = st.eagle_expand(H.tensor(lp, d), fs, k, F, frontier_valid=valid, frontier_cand=fc, outputs=outs,
+                              cand_stride=D * C, dev_status=status)
+        fs, fc = res["next_score"].clone(), res["next_index"].clone()
+        valid = (fc >= 0).to(torch.int32)
+    root = torch.from_numpy(rng.integers(0, V, B).astype(np.int32)).to(d)
+    tree = st.eagle_tree(S, Tk, P, N, draft_to_target=H.tensor(d2t, d), root_token=root, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    parent = tree["parent"].cpu().numpy()
+    tokens = tree["tokens"].cpu().numpy()
+    n_nodes = tree["n_nodes"].cpu().numpy()
+    node_cand = tree["node_cand"].cpu().numpy()
+    # each node's draft distribution: the frontier row its children were drawn from
+    full = np.zeros((B, N, Vd), dtype=np.float32)
+    for b in range(B):
+        full[b, 0] = np.exp(lps[0][b, 0])
+        for i in range(1, int(n_nodes[b])):
+            l, j = divmod(int(node_cand[b, i]), C)
+            if l + 1 < D:
+                f = np.nonzero(fronts[l + 1][b] == j)[0]
+                if len(f):
+                    full[b, i] = np.exp(lps[l + 1][b, f[0]])
+    parents = [parent[b, : int(n_nodes[b])] for b in range(B)]
+    case = make_case(dtype="bf16", Hq=4, Hkv=1, d=64, Hd=128, V=V, prefix_len=[4] * B, parents=parents, N=N,
+                     rule="rejection", tau=1.0, seed=17, tokens=("given", tokens), rng=rng)
+    case = dataclasses.replace(case, draft_probs=full, draft_to_target=d2t)
+    rows, index = gen_compact_draft(full, case.parent, case.n_nodes)
+    assert rows.shape[0] < B * N
+    t = H.to_device(case, d)
+    status.zero_()
+    res = st.verify_accept(t["hidden"], t["W"], t["tokens"], t["parent"], t["n_nodes"], "rejection", 1.0,
+                           seed=case.seed, draft_probs=H.tensor(rows, d), draft_to_target=t["map"],
+                           draft_rows=H.tensor(index, d), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = {k_: v.cpu().numpy() for k_, v in res.items()}
+    c = H.check_verify(case, got, H.oracle_verify(case))
+    assert c.exact + c.excluded == case.B and c.paths_exact >= 1
