@@ -1,6 +1,8 @@
 """GPU parity of the static Medusa tree expansion (spec_medusa_expand) with the oracle, bit for
 bit: every head's top-k (ties to the lower id), every node's token, and the shared topology."""
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -120,3 +122,38 @@ def test_plateaus_and_constant_rows(dtype, topk_heads):
     assert (got["topk_index"] == idx).all()
     assert (got["tokens"] == tokens).all()
     assert idx[0, 0].tolist() == list(range(k))  # a constant row: the lowest ids
+
+
+def test_expansion_captured_in_a_graph():
+    """The expansion's merge launches as a programmatic dependent of the chunk kernel; captured
+    into a CUDA graph and replayed (twice, the logits refilled in between) it gives what direct
+    calls give."""
+    d = H.dev()
+    rng = np.random.default_rng(99)
+    topk_heads = (3, 3, 2, 2, 1)
+    parent, rank = st.medusa_topology(topk_heads, 63)
+    x1, x2 = (BF.f32_to_bf16_bits(rng.standard_normal((2, 5, 128256)).astype(np.float32)) for _ in range(2))
+    logits = H.tensor(x1, d, True)
+    tp, tr = torch.from_numpy(parent).to(d), torch.from_numpy(rank).to(d)
+    ma, outs = st.medusa_args(logits, tp, tr, 3)
+    L = st.lib()
+    need = L.spec_medusa_expand_workspace(ctypes.byref(ma))
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        code = L.spec_medusa_expand(ctypes.byref(ma), ctypes.c_void_p(ws.data_ptr()), need,
+                                    ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(s.cuda_stream))
+    assert code == 0
+    for x in (x1, x2):
+        logits.copy_(H.tensor(x, d, True))
+        g.replay()
+        torch.cuda.synchronize()
+        got = {k: v.clone() for k, v in outs.items()}
+        ref = st.medusa_expand(H.tensor(x, d, True), tp, tr, 3)
+        torch.cuda.synchronize()
+        for k in ref:
+            assert torch.equal(got[k], ref[k]), k
+    assert int(status.item()) == 0
