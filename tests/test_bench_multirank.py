@@ -48,3 +48,24 @@ def test_reference_arm_prints_only_on_rank_zero(capsys, monkeypatch):
     monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference"])
     bench.main()  # rank 1: no work, no output
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_the_tiny_workload(capsys, monkeypatch):
+    """The reference arm (the fp64 oracle on the host cores) prints one JSON line with the
+    native arm's metric, unit and direction, the e2e object with zero copy bytes, and a
+    cpu_baseline describing the run; it stops at the requested step count."""
+    import json
+    import bench
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference", "--workload", "1", "--steps", "2",
+                                     "--warmup", "1"])
+    bench.main()
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["metric"] == bench.METRIC and j["unit"] == bench.UNIT
+    assert j["higher_is_better"] is True and j["steps"] == 2 and j["value"] > 0
+    assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    cb = j["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == j["value"] and cb["cores"] >= 1 and cb["sample"]
