@@ -21,36 +21,9 @@ constexpr int kEgThreads = 256;
 constexpr int kEgPerLane = 8;           // candidate keys per lane in the warp merges (<= 256)
 constexpr int kEgTreeThreads = 512;
 
-__device__ __forceinline__ uint32_t order_bits(float f) {  // monotone map, NaN -> 0, -0 = +0
-  if (f != f) return 0u;
-  const uint32_t b = __float_as_uint(f == 0.f ? 0.f : f);
-  const uint32_t u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return u == 0u ? 1u : u;
-}
-__device__ __forceinline__ float order_value(uint32_t u) {
-  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
-}
 // score key: better score first, equal scores by the lower candidate id; 0 = absent
 __device__ __forceinline__ unsigned long long score_key(float s, int c) {
-  if (!(s > -INFINITY)) return 0ull;
-  return ((unsigned long long)order_bits(s) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)c);
-}
-__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, o);
-    x = y > x ? y : x;
-  }
-  return x;
-}
-// the best key strictly below `below` among the warp's keys (0 if none)
-__device__ __forceinline__ unsigned long long warp_best_below(const unsigned long long (&k)[kEgPerLane],
-                                                              unsigned long long below) {
-  unsigned long long m = 0ull;
-#pragma unroll
-  for (int e = 0; e < kEgPerLane; ++e)
-    if (k[e] < below && k[e] > m) m = k[e];
-  return warp_max_key(m);
+  return s > -INFINITY ? order_key(order_u(s), c) : 0ull;
 }
 
 }  // namespace
@@ -76,7 +49,7 @@ __global__ void __launch_bounds__(kEgThreads) eagle_expand_kernel(const EagleExp
     const int par = p.frontier_cand ? p.frontier_cand[(size_t)b * p.F + f] : -1;
     unsigned long long below = ~0ull;
     for (int r = 0; r < p.k; ++r) {
-      below = warp_best_below(keys, below);
+      below = warp_max_below(keys, below);
       const int c = f * p.k + r;
       if (lane == 0) {
         int tok = -1;
@@ -102,7 +75,7 @@ __global__ void __launch_bounds__(kEgThreads) eagle_expand_kernel(const EagleExp
     }
     unsigned long long below = ~0ull;
     for (int r = 0; r < p.next_k; ++r) {
-      below = warp_best_below(keys, below);
+      below = warp_max_below(keys, below);
       if (lane == 0) {
         const int c = below ? (int)(0xFFFFFFFFu - (uint32_t)(below & 0xFFFFFFFFull)) : -1;
         p.next_index[(size_t)b * p.next_k + r] = c;

@@ -21,42 +21,6 @@ namespace {
 constexpr int kMxThreads = 256;
 constexpr int kMxEpt = 16;  // vocabulary entries per thread in K5a (chunk <= 4096)
 
-// Order key: larger is better.  Values order as floats (-0 = +0, NaN below -inf); equal values
-// order by the lower token id.  The upper half (order_u) alone orders the values.
-__device__ __forceinline__ uint32_t order_u(float f) {
-  if (f != f) return 0u;
-  const uint32_t b = __float_as_uint(f == 0.f ? 0.f : f);
-  const uint32_t u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return u == 0u ? 1u : u;  // keep 0 for NaN
-}
-__device__ __forceinline__ float order_value(uint32_t u) {  // the value order_u maps to u (u >= 1)
-  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
-}
-__device__ __forceinline__ unsigned long long order_key(uint32_t u, int v) {
-  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)v);
-}
-__device__ __forceinline__ int key_token(unsigned long long k) {
-  return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
-}
-
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, o);
-    x = y > x ? y : x;
-  }
-  return x;
-}
-
-// Largest of `n` keys below `below` over the warp (0 when there is none); every lane gets it.
-__device__ __forceinline__ unsigned long long warp_max_below(const unsigned long long* keys, int n,
-                                                             unsigned long long below) {
-  unsigned long long m = 0ull;
-  for (int e = 0; e < n; ++e)
-    if (keys[e] < below && keys[e] > m) m = keys[e];
-  return warp_max_u64(m);
-}
-
 // Where this thread's entries lie in its chunk: with rows and chunk starts on 16-byte boundaries
 // a thread reads 16-byte vectors (8 bf16 or 4 fp32 neighbours each), the threads side by side;
 // otherwise single entries.  Entry e of thread t is token v0 + entry_offset(mode, t, e).
@@ -208,7 +172,7 @@ __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const Med
   }
   unsigned long long below = ~0ull;
   for (int r = 0; r < p.k; ++r) {
-    below = warp_max_below(keys, kMxEpt, below);
+    below = warp_max_below(keys, below);
     if (lane == 0) s_cand[warp * kMaxTopk + r] = below;  // 0 once the warp's keys are exhausted
   }
   __syncthreads();
@@ -222,7 +186,7 @@ __global__ void __launch_bounds__(kMxThreads) medusa_chunk_topk_kernel(const Med
     }
     below = ~0ull;
     for (int r = 0; r < p.k; ++r) {
-      below = warp_max_below(c, kPerC, below);
+      below = warp_max_below(c, below);
       if (lane == 0) out[r] = below;
     }
   }
