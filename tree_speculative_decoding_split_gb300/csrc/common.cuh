@@ -6,8 +6,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <utility>
-
 #include "spectree.h"
 
 namespace spectree {
@@ -16,45 +14,6 @@ constexpr int kMaxNodes = SPEC_MAX_NODES;
 constexpr int kAncWords = (kMaxNodes + 31) / 32;  // 8 words of ancestor bits per node
 constexpr float kMargin = 1e-4f;                  // decision margin band
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
-
-// ---- order keys (top-k) -------------------------------------------------------------------
-// A 64-bit key orders candidates best first: the upper half maps the value monotonically
-// (-0 = +0; NaN maps to 0, below -inf), the lower half breaks ties by the lower id; key 0 means
-// "no candidate".
-
-__device__ __forceinline__ uint32_t order_u(float f) {
-  if (f != f) return 0u;
-  const uint32_t b = __float_as_uint(f == 0.f ? 0.f : f);
-  const uint32_t u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return u == 0u ? 1u : u;  // keep 0 for NaN
-}
-__device__ __forceinline__ float order_value(uint32_t u) {  // the value order_u maps to u (u >= 1)
-  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
-}
-__device__ __forceinline__ unsigned long long order_key(uint32_t u, int id) {
-  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
-}
-__device__ __forceinline__ int key_token(unsigned long long k) {
-  return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
-}
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, o);
-    x = y > x ? y : x;
-  }
-  return x;
-}
-// Largest of the warp's keys strictly below `below` (0 when there is none); every lane gets it.
-template <int N>
-__device__ __forceinline__ unsigned long long warp_max_below(const unsigned long long (&keys)[N],
-                                                             unsigned long long below) {
-  unsigned long long m = 0ull;
-#pragma unroll
-  for (int e = 0; e < N; ++e)
-    if (keys[e] < below && keys[e] > m) m = keys[e];
-  return warp_max_u64(m);
-}
 
 // ---- status ---------------------------------------------------------------------------------
 
@@ -261,32 +220,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// ---- programmatic dependent launch -------------------------------------------------------------
-// A kernel launched with launch_dependent (below) may start while the kernel before it in the
-// stream is still running: it does its independent set-up, then pdl_wait() returns once that
-// kernel has completed and its memory writes are visible (a no-op for an ordinary launch).  A
-// kernel that calls pdl_launch_dependents() lets its dependent launch as soon as every one of
-// its CTAs has made the call (or exited), instead of when the last one exits.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-// Host: launches `kernel` as a programmatic dependent of the previous kernel in `stream`.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                             Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---- bf16 helpers ---------------------------------------------------------------------------

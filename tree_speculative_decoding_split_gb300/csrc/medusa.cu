@@ -13,6 +13,8 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "pdl.cuh"
+#include "topk.cuh"
 
 namespace spectree {
 
