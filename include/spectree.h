@@ -473,14 +473,16 @@ void spec_round_destroy(spec_round* round);
  * (Deployment convenience, like the round itself: the pages describe what a round computes, not
  * where its inputs come from.)  When the round has both tree attention and verification, a copy
  * whose destination lies wholly inside a buffer only the verification reads (hidden_states,
- * tokens, lm_head_weight, draft_probs) goes to a stream of the round's own: it starts after
- * everything already enqueued on `stream`, carries the verification beside the attention, and
- * rejoins `stream` before the compaction and the result copies.  Every other input copy, and
- * every output copy, is on `stream`.  Those verification-only buffers must therefore not overlap
- * any buffer the attention reads.  The input copies run group after group, each with the whole
- * host link: the longer branch's first (that branch is also issued first, as in the graph), then
- * the other's, then the draft distributions (and with draft_rows, the compact rows), which only
- * the rejection walk at the end of the verification reads.
+ * tokens, lm_head_weight, draft_probs, draft_rows, draft_to_target) goes to a stream of the
+ * round's own: it starts after everything already enqueued on `stream`, carries the verification
+ * beside the attention, and rejoins `stream` before the compaction and the result copies.  When
+ * the verification is the longer branch, so do the copies that touch its parent or n_nodes
+ * (read by both branches; the attention's stream waits for that group).  Every other input copy,
+ * and every output copy, is on `stream`.  Those verification-only buffers must therefore not
+ * overlap any buffer the attention reads.  The input copies run group after group, each with the
+ * whole host link: the longer branch's first (that branch is also issued first, as in the
+ * graph), then the other's, then the draft distributions (and with draft_rows, the compact rows),
+ * which only the rejection walk at the end of the verification reads.
  *
  * Each spec_host_copy moves `rows` rows of `row_bytes` bytes; row r starts at
  * host + r * host_pitch and at device + r * device_pitch (pitches are ignored when rows == 1).

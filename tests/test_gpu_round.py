@@ -287,7 +287,9 @@ def test_host_round_with_compact_draft_rows():
                               draft_rows=t2["index"])
     ca, src, nl = st.compact_args(t2["k"], t2["v"], t2["prefix_len"], outs["path"], outs["accept_len"])
     r = st.Round(aa, va, ca, dev_status=status)
-    keys = ("q", "hidden", "tokens", "parent", "rows", "index")
+    # parent and n_nodes are read by both branches (with the verification first, they are copied
+    # with its group), prefix_len by the attention and the compaction
+    keys = ("q", "hidden", "tokens", "parent", "n_nodes", "prefix_len", "rows", "index")
     host = {k: t2[k].cpu().pin_memory() for k in keys}
     for k in keys:
         t2[k].zero_()

@@ -23,8 +23,9 @@ struct spec_round {
   cudaEvent_t e_fork, e_join;
   cudaEvent_t e_vin, e_ain;   // the first / the second group of input copies is done
   bool verify_first;          // the verification is the longer branch: it is issued first
-  uintptr_t vonly[5][2];      // [lo, hi) of the buffers only the verification reads (but draft_probs)
+  uintptr_t vonly[6][2];      // [lo, hi) of the buffers only the verification reads (but draft_probs)
   int n_vonly;
+  uintptr_t vshared[2][2];    // [lo, hi) of the verification's parent and n_nodes (the attention reads them too)
   // Rejection with draft distributions: their copies run on `side_d` beside the LM head, and
   // the verification is issued as direct calls whose rejection walk waits for e_draft (a wait
   // with well-defined host-order semantics, recorded afresh every launch).
@@ -112,11 +113,16 @@ void make_parts(spec_round* r, const spec_attn_args* attn, void* attn_ws, size_t
     r->vonly[r->n_vonly][1] = reinterpret_cast<uintptr_t>(p) + bytes;
     ++r->n_vonly;
   };
+  r->vshared[0][0] = reinterpret_cast<uintptr_t>(verify->parent);
+  r->vshared[0][1] = r->vshared[0][0] + rows * sizeof(int32_t);
+  r->vshared[1][0] = reinterpret_cast<uintptr_t>(verify->n_nodes);
+  r->vshared[1][1] = r->vshared[1][0] + (size_t)verify->batch * sizeof(int32_t);
   add(verify->hidden_states, rows * verify->hidden * es);
   add(verify->tokens, rows * sizeof(int32_t));
   add(verify->lm_head_weight, (size_t)verify->vocab * verify->hidden * es);
   const bool compact_draft = verify->rule == SPEC_RULE_REJECTION && verify->draft_rows;
   if (compact_draft) add(verify->draft_rows, rows * sizeof(int32_t));
+  if (verify->rule == SPEC_RULE_REJECTION) add(verify->draft_to_target, (size_t)verify->draft_vocab * sizeof(int32_t));
   const size_t draft_bytes = (compact_draft ? (size_t)verify->n_draft_rows : rows) * verify->draft_vocab * sizeof(float);
   if (verify->rule == SPEC_RULE_REJECTION && verify->draft_probs && !verify->draft_ready &&
       cudaStreamCreateWithFlags(&r->side_d, cudaStreamNonBlocking) == cudaSuccess &&
@@ -297,13 +303,18 @@ extern "C" spec_status spec_round_launch_host(const spec_round* round, const spe
       lo = reinterpret_cast<uintptr_t>(c.device);
       hi = lo + (c.rows > 1 ? (size_t)(c.rows - 1) * c.device_pitch : 0) + c.row_bytes;
     };
-    // 0: the caller's stream; 1: the verification's stream; 2: the draft distributions' stream
+    // 0: the caller's stream; 1: the verification's stream; 2: the draft distributions' stream.
+    // Inputs both branches read go with the first group, which the other branch's stream waits
+    // for: with the verification first, its parent and n_nodes are copied on its own stream.
     auto route = [&](const spec_host_copy& c) {
       uintptr_t lo, hi;
       extent(c, lo, hi);
       if (round->direct_verify && lo >= round->draft[0] && hi <= round->draft[1]) return 2;
       for (int k = 0; k < round->n_vonly; ++k)
         if (lo >= round->vonly[k][0] && hi <= round->vonly[k][1]) return 1;
+      if (round->verify_first)
+        for (int k = 0; k < 2; ++k)
+          if (hi > round->vshared[k][0] && lo < round->vshared[k][1]) return 1;
       return 0;
     };
     if (cudaEventRecord(round->e_fork, s) != cudaSuccess || cudaStreamWaitEvent(round->side, round->e_fork, 0) != cudaSuccess)
